@@ -1,0 +1,553 @@
+"""Benchmark of the routed-expert GEMV path on GB300.
+
+One step = one token through the 8-expert Q4 decode (d_model 4096, d_ff 1536,
+group 64): for each expert the fused gate/up call and the down call of the C
+ABI, 16 calls, captured once into a CUDA graph and replayed.  The metric is
+effective HBM bandwidth, (packed codes + scales + x + out bytes) / device
+time, and the time per 8-expert FFN.  Weights rotate over several copies
+whose total is far larger than L2, so every step reads its weights from HBM.
+
+Printed: one JSON line (rank 0).  Besides the contract keys it carries the
+roofline of the dominant kernel, the end-to-end figure through host buffers,
+the oracle timed on the host cores, sampled clocks, and `rows`: the other
+rows of the hot path (Q2 decode, bf16 matvec shapes, token batch, the small
+256/256 expert) each timed the same way.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--no-rows] [--no-cpu]
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import smoe_inputs as inp  # noqa: E402
+
+METRIC = "effective HBM GB/s (and % of GB300 peak) per GEMV; µs per 8-expert Q4 FFN"
+D_MODEL, D_FF, GROUP, N_EXPERTS = 4096, 1536, 64, 8
+L2_BYTES = 129 * 1024 * 1024
+WORKLOAD = (f"q4_8expert_decode: 8 experts x (gate/up [{D_FF},{D_MODEL}] + down [{D_MODEL},{D_FF}]), "
+            f"Q4 group {GROUP}, f32 scales, one f32 token")
+
+
+def q_bytes(bits, rows, cols, group):
+    return rows * cols * bits // 8 + rows * (cols // group) * 4
+
+
+def expert_bytes(bits, d_model=D_MODEL, d_ff=D_FF, group=GROUP):
+    return 2 * q_bytes(bits, d_ff, d_model, group) + q_bytes(bits, d_model, d_ff, group)
+
+
+def step_bytes(bits, n_experts=N_EXPERTS, d_model=D_MODEL, d_ff=D_FF, group=GROUP):
+    """Algorithmic bytes of one token through n experts: every expert's codes
+    and scales, x once, the [n, d_model] outputs (hidden not counted)."""
+    return n_experts * expert_bytes(bits, d_model, d_ff, group) + d_model * 4 + n_experts * d_model * 4
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [c.strip() for c in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v, world, dev=None):
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ the GPU arm
+
+class DecodeWorkload:
+    """n_copies independent sets of 8 experts (bits = 4 or 2) resident on the
+    device, one captured graph per copy, plus the token and outputs."""
+
+    def __init__(self, smoe, dev, bits, seed, n_copies):
+        import torch
+        self.smoe, self.dev, self.bits = smoe, dev, bits
+        self.gate_up = smoe.smoe_gate_up_q4 if bits == 4 else smoe.smoe_gate_up_q2
+        self.down = smoe.smoe_down_q4 if bits == 4 else smoe.smoe_down_q2
+        self.copies = []
+        for c in range(n_copies):
+            ex = []
+            for e in range(N_EXPERTS):
+                h = inp.expert(bits, D_MODEL, D_FF, GROUP, seed + 1000 * c, e)
+                ex.append({k: torch.from_numpy(v).to(dev) for k, v in h.items()})
+            self.copies.append(ex)
+        self.x = torch.from_numpy(inp.activations(D_MODEL, seed)).to(dev)
+        self.hidden = torch.empty((N_EXPERTS, D_FF), device=dev)
+        self.out = torch.empty((N_EXPERTS, D_MODEL), device=dev)
+        self.stream = torch.cuda.Stream(device=dev)
+        self.graphs = []
+
+    def calls(self, c, stream):
+        for i, t in enumerate(self.copies[c]):
+            self.gate_up(t["gate_codes"], t["gate_scales"], t["up_codes"], t["up_scales"], self.x,
+                         self.hidden[i], D_FF, D_MODEL, GROUP, stream=stream)
+            self.down(t["down_codes"], t["down_scales"], self.hidden[i], self.out[i], D_MODEL, D_FF,
+                      GROUP, stream=stream)
+
+    def capture(self):
+        """One graph per copy (one step each) and one graph for a whole
+        rotation (len(copies) steps), so that host-side replay cost stays far
+        below the device time of the steps it launches."""
+        import torch
+        s = self.stream
+        with torch.cuda.stream(s):
+            for c in range(len(self.copies)):
+                self.calls(c, s)
+        s.synchronize()
+        for c in range(len(self.copies)):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=s):
+                self.calls(c, s)
+            self.graphs.append(g)
+        self.cycle = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.cycle, stream=s):
+            for c in range(len(self.copies)):
+                self.calls(c, s)
+        s.synchronize()
+
+    def run(self, steps):
+        """`steps` consecutive steps, each on the next weight copy."""
+        import torch
+        n = len(self.copies)
+        with torch.cuda.stream(self.stream):
+            for _ in range(steps // n):
+                self.cycle.replay()
+            for i in range(steps % n):
+                self.graphs[i].replay()
+
+
+def time_steps(fn, steps, stream):
+    import torch
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    fn(steps)
+    e1.record(stream)
+    e1.synchronize()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / 1000.0
+
+
+def kernel_alone_seconds(launch, n, stream):
+    """Average device time of one launch, each bracketed by its own events."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i, (a, b) in enumerate(evs):
+            a.record(stream)
+            launch(i)
+            b.record(stream)
+    torch.cuda.synchronize()
+    return sum(a.elapsed_time(b) for a, b in evs) / n / 1000.0
+
+
+def roofline_traffic(kernel_name):
+    """dram read+write bytes per launch from the committed ncu summary, only
+    while the kernel sources still hash to the value the counters were taken at."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "roofline_traffic.json")) as f:
+            rec = json.load(f).get(kernel_name)
+    except Exception:
+        return None
+    if not rec:
+        return None
+    h = hashlib.sha256()
+    for rel in rec["sources"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return rec["traffic_bytes"] if h.hexdigest() == rec["sha256"] else None
+
+
+def gpu_arm(args, rank, world, local):
+    import torch
+    from moe_expert_ffn_smoe_gb300 import _build
+    _build.build()
+    import moe_expert_ffn_smoe_gb300 as smoe
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    n_copies = max(2, -(-4 * L2_BYTES // step_bytes(4)))  # working set >= 4x L2
+    wl = DecodeWorkload(smoe, dev, 4, 5, n_copies)
+    wl.capture()
+    wl.run(max(3, args.warmup))
+    wl.stream.synchronize()
+
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.2)
+    t = time_steps(lambda k: wl.run(k), args.steps, wl.stream)
+    clock_rec = clocks.stop()
+    barrier(world)
+    t = max_over_ranks(t, world, dev)
+
+    sb = step_bytes(4)
+    value = sb * args.steps * world / t / 1e9
+    ms = t / args.steps * 1e3
+    hbm_peak, peak_kind = peaks()
+
+    # Dominant kernel: the fused gate/up launch (2/3 of the bytes), timed alone.
+    gu_bytes = 2 * q_bytes(4, D_FF, D_MODEL, GROUP) + D_MODEL * 4 + D_FF * 4
+    nlaunch = len(wl.copies) * N_EXPERTS
+
+    def gu_launch(i):
+        tt = wl.copies[i // N_EXPERTS % len(wl.copies)][i % N_EXPERTS]
+        smoe.smoe_gate_up_q4(tt["gate_codes"], tt["gate_scales"], tt["up_codes"], tt["up_scales"],
+                             wl.x, wl.hidden[i % N_EXPERTS], D_FF, D_MODEL, GROUP, stream=wl.stream)
+
+    kernel_alone_seconds(gu_launch, nlaunch, wl.stream)  # warm
+    t_gu = kernel_alone_seconds(gu_launch, 4 * nlaunch, wl.stream)
+    achieved = gu_bytes / t_gu / 1e9
+    roof = {"kernel": "qgemv_fast<Q4,gate_up> (smoe_gate_up_q4, 1536x4096)", "bound": "hbm",
+            "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+            "frac": round(achieved / hbm_peak, 4), "traffic": roofline_traffic("gate_up_q4"),
+            "algorithmic_bytes_per_launch": gu_bytes, "us_per_launch": round(t_gu * 1e6, 3),
+            "peak_kind": f"{peak_kind} burst HBM copy bandwidth"}
+
+    # End to end: token in from pinned host memory, outputs back to pinned host memory.
+    x_host = torch.from_numpy(inp.activations(D_MODEL, 5)).pin_memory()
+    out_host = torch.empty((N_EXPERTS, D_MODEL)).pin_memory()
+
+    def e2e_steps(k):
+        for i in range(k):
+            wl.x.copy_(x_host, non_blocking=True)
+            wl.graphs[i % len(wl.graphs)].replay()
+            out_host.copy_(wl.out, non_blocking=True)
+
+    with torch.cuda.stream(wl.stream):
+        e2e_steps(3)
+    e2e_n = max(3, min(args.steps, 2000))
+    with torch.cuda.stream(wl.stream):
+        t_e2e = time_steps(e2e_steps, e2e_n, wl.stream)
+    t_e2e = max_over_ranks(t_e2e, world, dev)
+    e2e = {"value": round(sb * e2e_n * world / t_e2e / 1e9, 2), "unit": "GB/s",
+           "h2d_bytes_per_step": D_MODEL * 4, "d2h_bytes_per_step": N_EXPERTS * D_MODEL * 4,
+           "us_per_step": round(t_e2e / e2e_n * 1e6, 3)}
+
+    result = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded uniform codes, U[0.01,0.05] scales, N(0,1) token)",
+        "config": {"workload": WORKLOAD, "bytes_per_step": sb,
+                   "l2": f"{len(wl.copies)} rotating weight copies ({len(wl.copies) * sb / 1e6:.0f} MB) "
+                         f"> {L2_BYTES >> 20} MB L2",
+                   "launch": "16 C-ABI calls per step captured in a CUDA graph, programmatic "
+                             "dependent launch between kernels",
+                   "parallelism": f"replicas x{world} (experts are independent; no collective)"},
+        "us_per_8expert_ffn": round(ms * 1e3, 3),
+        "hbm_frac": round(value / world / hbm_peak, 4),
+        "roofline": roof, "e2e": e2e, "gpu_launches": 2 * N_EXPERTS * args.steps,
+        "clocks": clock_rec,
+    }
+    return result, wl, smoe, dev
+
+
+# ------------------------------------------------------------ other rows
+
+def rows_breakdown(smoe, dev, steps):
+    """Each remaining row of the hot path, timed with events on its own stream
+    over `steps` launches with rotating inputs larger than L2."""
+    import torch
+    hbm_peak, _ = peaks()
+    out = {}
+    s = torch.cuda.Stream(device=dev)
+
+    def timed(launch, n):
+        with torch.cuda.stream(s):
+            for i in range(3):
+                launch(i)
+            return time_steps(lambda k: [launch(i) for i in range(k)], n, s)
+
+    # Q2 8-expert decode
+    n_copies = max(2, -(-4 * L2_BYTES // step_bytes(2)))
+    q2 = DecodeWorkload(smoe, dev, 2, 6, n_copies)
+    q2.capture()
+    q2.run(5)
+    t = time_steps(lambda k: q2.run(k), max(50, steps // 4), q2.stream)
+    n = max(50, steps // 4)
+    sb = step_bytes(2)
+    out["q2_8expert_decode"] = {"GB/s": round(sb * n / t / 1e9, 1), "us_per_step": round(t / n * 1e6, 3),
+                                "frac": round(sb * n / t / 1e9 / hbm_peak, 4), "bytes_per_step": sb}
+    del q2
+    torch.cuda.empty_cache()
+
+    # bf16 matvec, four shapes
+    for (rows, cols), seed in zip(inp.CONFIGS["bf16_matvec"]["shapes"], inp.CONFIGS["bf16_matvec"]["seeds"]):
+        wbytes = rows * cols * 2
+        ncp = max(1, min(8, -(-2 * L2_BYTES // wbytes)))
+        ws = [torch.from_numpy(inp.bf16_rows(rows, cols, seed, 1 + c).view(np.int16)).to(dev)
+              for c in range(ncp)]
+        x = torch.from_numpy(inp.activations(cols, seed)).to(dev)
+        y = torch.empty(rows, device=dev)
+        nl = max(20, min(steps // 4, int(2e9 // wbytes)))
+        t = timed(lambda i: smoe.matvec_bf16(ws[i % ncp], x, y, rows, cols, stream=s), nl)
+        b = wbytes + cols * 4 + rows * 4
+        out[f"bf16_{rows}x{cols}"] = {"GB/s": round(b * nl / t / 1e9, 1), "us_per_call": round(t / nl * 1e6, 3),
+                                      "frac": round(b * nl / t / 1e9 / hbm_peak, 4), "bytes_per_call": b}
+        del ws
+        torch.cuda.empty_cache()
+
+    # token batch, one Q4 expert
+    ncp = 16
+    experts = [{k: torch.from_numpy(v).to(dev) for k, v in inp.expert(4, D_MODEL, D_FF, GROUP, 7 + 1000 * c).items()}
+               for c in range(ncp)]
+    for T in inp.CONFIGS["q4_token_batch"]["tokens"]:
+        X = torch.from_numpy(inp.activations((T, D_MODEL), 7)).to(dev)
+        Y = torch.empty((T, D_MODEL), device=dev)
+        need = smoe.smoe_ffn_batch_workspace_bytes(T, D_MODEL, D_FF, GROUP)
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+
+        def launch(i, T=T, X=X, Y=Y, ws=ws, need=need):
+            e = experts[i % ncp]
+            smoe.ffn_batch_q4(e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"],
+                              e["down_codes"], e["down_scales"], X, Y, T, D_MODEL, D_FF, GROUP, ws,
+                              need, stream=s)
+        nl = max(20, min(steps // 8, 400))
+        t = timed(launch, nl)
+        b = expert_bytes(4) + 2 * T * D_MODEL * 4
+        flops = 2 * T * 3 * D_FF * D_MODEL
+        out[f"q4_token_batch_T{T}"] = {"GB/s": round(b * nl / t / 1e9, 1), "us_per_call": round(t / nl * 1e6, 3),
+                                       "frac": round(b * nl / t / 1e9 / hbm_peak, 4),
+                                       "TFLOP/s": round(flops * nl / t / 1e12, 2), "bytes_per_call": b}
+    del experts
+    torch.cuda.empty_cache()
+
+    # the small 256/256 expert (latency bound)
+    small = [{k: torch.from_numpy(v).to(dev) for k, v in inp.expert(4, 256, 256, 64, c).items()} for c in range(4)]
+    xs = torch.from_numpy(inp.activations(256, 0)).to(dev)
+    hs = torch.empty(256, device=dev)
+    ys = torch.empty(256, device=dev)
+
+    def small_launch(i):
+        e = small[i % 4]
+        smoe.smoe_gate_up_q4(e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"], xs, hs,
+                             256, 256, 64, stream=s)
+        smoe.smoe_down_q4(e["down_codes"], e["down_scales"], hs, ys, 256, 256, 64, stream=s)
+    nl = max(50, min(steps // 4, 2000))
+    t = timed(small_launch, nl)
+    out["q4_ffn_256"] = {"us_per_ffn": round(t / nl * 1e6, 3), "bytes_per_ffn": expert_bytes(4, 256, 256, 64)}
+    return out
+
+
+# ------------------------------------------------------------ the CPU arm
+
+def cpu_sample(seconds, frac=None):
+    """Times the oracle on the host cores on whole or sliced 8-expert steps.
+    Returns (GB/s by the step's byte formula, threads, description, sec/step)."""
+    import oracle
+    threads = oracle.host_threads()
+    oracle.set_threads(threads)
+    experts = [inp.expert(4, D_MODEL, D_FF, GROUP, 5, e) for e in range(N_EXPERTS)]
+    x = inp.activations(D_MODEL, 5).astype(np.float64)
+    gu_rows = D_FF if frac is None else max(1, int(D_FF * frac))
+    dn_rows = D_MODEL if frac is None else max(1, int(D_MODEL * frac))
+    hidden = np.zeros(D_FF)
+
+    def one_step():
+        for e in experts:
+            r = oracle.gate_up(4, e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"],
+                               D_FF, D_MODEL, GROUP, x, 0, gu_rows)
+            hidden[:gu_rows] = r["hidden"]
+            oracle.qgemv(4, e["down_codes"], e["down_scales"], D_MODEL, D_FF, GROUP, hidden, 0, dn_rows)
+
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        one_step()
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    b = (N_EXPERTS * (2 * q_bytes(4, gu_rows, D_MODEL, GROUP) + q_bytes(4, dn_rows, D_FF, GROUP))
+         + D_MODEL * 4 + N_EXPERTS * dn_rows * 4)
+    desc = (f"{steps} oracle step(s) of the 8-expert decode"
+            + ("" if frac is None else f", each on rows [0,{gu_rows}) of gate/up and [0,{dn_rows}) of down")
+            + f"; {el:.1f} s wall")
+    return b * steps / el / 1e9, threads, desc, el / steps, b
+
+
+def reference_arm(args, rank, world):
+    """The oracle, as it stands, on this host's cores: K steps after W warm-up
+    steps, each step a row slice of the 8-expert decode sized so the whole run
+    stays within about a minute and a half."""
+    if rank != 0:
+        return None
+    # size the slice: one probe step on 1/64 of the rows
+    _, _, _, per, _ = cpu_sample(0.0, frac=1 / 64)
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    frac = max(1 / D_FF, min(1.0, (1 / 64) * budget / max(per, 1e-9)))
+    import oracle
+    experts = [inp.expert(4, D_MODEL, D_FF, GROUP, 5, e) for e in range(N_EXPERTS)]
+    x = inp.activations(D_MODEL, 5).astype(np.float64)
+    gu_rows, dn_rows = max(1, int(D_FF * frac)), max(1, int(D_MODEL * frac))
+    hidden = np.zeros(D_FF)
+
+    def step():
+        for e in experts:
+            r = oracle.gate_up(4, e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"],
+                               D_FF, D_MODEL, GROUP, x, 0, gu_rows)
+            hidden[:gu_rows] = r["hidden"]
+            oracle.qgemv(4, e["down_codes"], e["down_scales"], D_MODEL, D_FF, GROUP, hidden, 0, dn_rows)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    t = time.perf_counter() - t0
+    b = (N_EXPERTS * (2 * q_bytes(4, gu_rows, D_MODEL, GROUP) + q_bytes(4, dn_rows, D_FF, GROUP))
+         + D_MODEL * 4 + N_EXPERTS * dn_rows * 4)
+    v = b * args.steps / t / 1e9
+    sample = (f"each step: the 8-expert Q4 decode on rows [0,{gu_rows}) of every gate/up and "
+              f"[0,{dn_rows}) of every down matrix ({b} algorithmic bytes)")
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(t / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "bytes_per_step": b},
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": oracle.get_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-row breakdown")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        # rank 0 alone times the oracle; the other ranks exit without work
+        rank = int(os.environ.get("RANK", "0"))
+        res = reference_arm(args, rank, int(os.environ.get("WORLD_SIZE", "1")))
+        if rank == 0:
+            print(json.dumps(res), flush=True)
+        return
+    rank, world, local = dist_setup()
+
+    res, wl, smoe, dev = gpu_arm(args, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_cpu:
+        v, threads, desc, _, _ = cpu_sample(args.cpu_seconds)
+        res["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                               "sample": desc}
+    if rank == 0 and world == 1 and not args.no_rows:
+        del wl
+        res["rows"] = rows_breakdown(smoe, dev, args.steps)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

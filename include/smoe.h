@@ -1,0 +1,182 @@
+/*
+ * smoe.h -- C ABI of libsmoe.so: group-quantized matrix-vector products for
+ * routed mixture-of-experts FFN layers on NVIDIA GB300 (sm_103a).
+ *
+ * Every operation is defined by the S-MoE documentation page
+ * "Metal Compute Kernels"; each declaration names the section it follows.
+ *
+ * Common conventions
+ * ------------------
+ * Pointers.  Every pointer argument except `stream` and the results of the
+ *   query functions is a DEVICE pointer owned by the caller.  The library
+ *   allocates no memory of its own on any call and keeps no pointer after the
+ *   call returns.
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
+ *   default stream).  Calls enqueue their kernels on it and return at once;
+ *   results are ready when the stream's work has completed.  Kernels are
+ *   launched with programmatic dependent launch: each kernel may prefetch its
+ *   WEIGHTS into L2 before the previous kernel in the stream has finished,
+ *   but reads its activations and writes its outputs only after the previous
+ *   kernel's writes are visible.  Weights must not be written by a kernel
+ *   that is still running when the call is made on the same stream unless
+ *   that kernel finishes before this call's kernel starts (ordinary stream
+ *   order does this for every non-kernel operation and every kernel launched
+ *   without programmatic dependent launch).
+ * Packed codes.  A Q4 row of `cols` weights is cols/2 bytes: byte j holds
+ *   column 2j in its low nibble and column 2j+1 in its high nibble.  A Q2 row
+ *   is cols/4 bytes: byte j holds columns 4j..4j+3, the first in the lowest
+ *   two bits.  Rows are stored one after another with no padding, so a
+ *   [rows x cols] matrix is rows*cols*bits/8 bytes.
+ * Scales.  f32, row-major [rows][cols/group]: scales[r][g] applies to columns
+ *   g*group .. g*group+group-1 of row r.
+ * Dequantisation.  w = (code - Z) * (1/Z) * s with Z = 7.5 (Q4) or 1.5 (Q2)
+ *   ("Fused FFN Kernels -- One Simdgroup Per Output Row").
+ * Layout contract ("Layout assumptions the kernels rely on"): cols is a
+ *   multiple of 32 (Q4) or 64 (Q2); group is a positive multiple of 32 (Q4)
+ *   or 64 (Q2) that divides cols; codes, x, hidden, out, X, Y and workspace
+ *   are 16-byte aligned; scales are 16-byte aligned.  Sizes are >= 0 and
+ *   cols <= SMOE_MAX_COLS.
+ * Empty work.  A call whose output is empty (0 rows, or T == 0) returns
+ *   SMOE_OK without launching anything and without looking at the pointers.
+ *   A call with cols == 0 and rows > 0 writes zeros (an empty sum).
+ * Aliasing.  Outputs must not overlap any input or each other; an overlap
+ *   is refused with SMOE_ERR_ALIAS.
+ * Errors.  Every contract check runs on the host before any launch and
+ *   returns a status without touching the GPU.  There is no fallback to
+ *   another kernel or to the CPU: a call either runs the kernels below or
+ *   returns an error.  SMOE_ERR_LAUNCH reports a CUDA launch error (the CUDA
+ *   error itself stays readable with cudaGetLastError()).
+ * Numerics.  Sums are reassociated (lanes, warps, groups), so results are not
+ *   bit-identical to a sequential sum; they agree with an exact (f64) result
+ *   within 1e-4 * sum_i |w_i x_i| + 1e-6 per output element.
+ */
+#ifndef SMOE_H
+#define SMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SMOE_ABI_VERSION 1
+
+/* Largest `cols` (input length) any call accepts: the input vector of a
+ * call is staged whole in one SM's shared memory (f32). */
+#define SMOE_MAX_COLS 32768
+
+typedef enum smoe_status {
+    SMOE_OK = 0,
+    SMOE_ERR_NULL = 1,      /* a required pointer is NULL                       */
+    SMOE_ERR_ALIGN = 2,     /* a pointer breaks the alignment contract          */
+    SMOE_ERR_SHAPE = 3,     /* sizes break the layout contract or the limits    */
+    SMOE_ERR_WORKSPACE = 4, /* workspace missing or smaller than required       */
+    SMOE_ERR_LAUNCH = 5,    /* CUDA refused a launch or a device query          */
+    SMOE_ERR_TIMEOUT = 6,   /* a device-side bounded wait gave up               */
+    SMOE_ERR_ALIAS = 7      /* an output overlaps an input or another output    */
+} smoe_status;
+
+/* ABI version (SMOE_ABI_VERSION of the built library). */
+int smoe_abi_version(void);
+
+/* Static text for a status code (never NULL). */
+const char *smoe_status_string(int status);
+
+/*
+ * Fused gate/up pass of one routed expert for one token
+ * ("Fused FFN Kernels -- One Simdgroup Per Output Row"):
+ *
+ *   hidden[i] = SiLU(gate . x)[i] * (up . x)[i],  i in [0, d_ff),
+ *   SiLU(v) = v / (1 + e^-v).
+ *
+ * gate_codes, up_codes: packed [d_ff x d_model] (Q4 or Q2), row i = output i.
+ * gate_scales, up_scales: f32 [d_ff x d_model/group].
+ * x: f32 [d_model].  hidden: f32 [d_ff], written.
+ * Both matrices are read in one pass over a shared copy of x.
+ */
+int smoe_gate_up_q4(const uint8_t *gate_codes, const float *gate_scales,
+                    const uint8_t *up_codes, const float *up_scales,
+                    const float *x, float *hidden,
+                    int d_ff, int d_model, int group, void *stream);
+int smoe_gate_up_q2(const uint8_t *gate_codes, const float *gate_scales,
+                    const uint8_t *up_codes, const float *up_scales,
+                    const float *x, float *hidden,
+                    int d_ff, int d_model, int group, void *stream);
+
+/*
+ * Down projection of one routed expert for one token
+ * ("Fused FFN Kernels -- One Simdgroup Per Output Row"):
+ *
+ *   out[j] = (down . hidden)[j],  j in [0, d_model).
+ *
+ * down_codes: packed [d_model x d_ff], grouped along d_ff.
+ * down_scales: f32 [d_model x d_ff/group].  hidden: f32 [d_ff].
+ * out: f32 [d_model], written.
+ */
+int smoe_down_q4(const uint8_t *down_codes, const float *down_scales,
+                 const float *hidden, float *out,
+                 int d_model, int d_ff, int group, void *stream);
+int smoe_down_q2(const uint8_t *down_codes, const float *down_scales,
+                 const float *hidden, float *out,
+                 int d_model, int d_ff, int group, void *stream);
+
+/*
+ * Dense bf16 matvec ("Coalesced Dense Matvec -- the Same Contract for bf16"):
+ *
+ *   y[r] = sum_k bf16(w[r][k]) * x[k],  r in [0, rows).
+ *
+ * w: bf16 bit patterns, row-major [rows x cols], 16-byte aligned; cols is a
+ * multiple of 8 (so every row starts on a 16-byte boundary) and at most
+ * SMOE_MAX_COLS.  x: f32 [cols], 16-byte aligned.  y: f32 [rows], written.
+ */
+int matvec_bf16(const uint16_t *w, const float *x, float *y,
+                int rows, int cols, void *stream);
+
+/*
+ * Bytes of device workspace ffn_batch_q4 needs for these sizes (the hidden
+ * activations [T x d_ff] f32 and any partial sums), rounded up to 256.
+ * Returns 0 for T <= 0 and (size_t)-1 for sizes the call would refuse.
+ */
+size_t smoe_ffn_batch_workspace_bytes(int T, int d_model, int d_ff, int group);
+
+/*
+ * Token-batch fused FFN of one Q4 expert ("Token-Batch Fused FFN"): the
+ * one-token FFN above applied to every row of X:
+ *
+ *   H[t][i] = SiLU(gate . X[t])[i] * (up . X[t])[i]
+ *   Y[t][j] = (down . H[t])[j]
+ *
+ * gate/up: packed Q4 [d_ff x d_model] with f32 scales [d_ff x d_model/group];
+ * down: packed Q4 [d_model x d_ff] with f32 scales [d_model x d_ff/group].
+ * X: f32 [T x d_model] row-major; Y: f32 [T x d_model], written.
+ * workspace: device memory of at least
+ * smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group) bytes, 16-byte
+ * aligned, owned by the caller; its contents on entry do not matter and on
+ * return are unspecified.  Two calls in flight at once need two workspaces.
+ * The batch is not limited to the page's 64 tokens: any T >= 0 is accepted.
+ * For larger T the contraction runs on the tensor cores (codes as exact bf16
+ * integers, X split into two bf16 halves, f32 accumulation).
+ */
+int ffn_batch_q4(const uint8_t *gate_codes, const float *gate_scales,
+                 const uint8_t *up_codes, const float *up_scales,
+                 const uint8_t *down_codes, const float *down_scales,
+                 const float *X, float *Y,
+                 int T, int d_model, int d_ff, int group,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Reads and clears the library's device status word for the current device
+ * after synchronising `stream`.  Kernels that wait on the device (bounded
+ * mbarrier waits of the tensor-core batch path) set it when a wait gives up
+ * instead of hanging; such a kernel skips its remaining work and exits.
+ * Returns SMOE_OK, SMOE_ERR_TIMEOUT, or SMOE_ERR_LAUNCH if the stream or the
+ * status word cannot be read.
+ */
+int smoe_last_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMOE_H */

@@ -1,0 +1,141 @@
+"""Python binding of libsmoe.so (include/smoe.h): group-quantized routed-expert
+GEMVs for GB300.
+
+Argument marshalling only: each function below has the name of the C entry
+point it calls, turns tensors into device pointers and a stream into a
+cudaStream_t, and raises SmoeError when the call returns a non-zero status.
+Every step of the computation runs in the library's CUDA kernels; there is no
+Python or CPU implementation here and no fallback.  If the library has not
+been built, importing this package raises ImportError.
+
+Pointer arguments accept a torch.Tensor (its data_ptr()), an int device
+address, or None (NULL).  `stream` accepts a torch.cuda.Stream, an int
+cudaStream_t, or None for torch's current stream on the current device.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libsmoe.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"{LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; g.build()\"` "
+        "(the library has no CPU fallback)")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+SMOE_OK = 0
+SMOE_ERR_NULL = 1
+SMOE_ERR_ALIGN = 2
+SMOE_ERR_SHAPE = 3
+SMOE_ERR_WORKSPACE = 4
+SMOE_ERR_LAUNCH = 5
+SMOE_ERR_TIMEOUT = 6
+SMOE_ERR_ALIAS = 7
+SMOE_MAX_COLS = 32768
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "smoe_abi_version": ([], _I),
+    "smoe_status_string": ([_I], ctypes.c_char_p),
+    "smoe_gate_up_q4": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P], _I),
+    "smoe_gate_up_q2": ([_P, _P, _P, _P, _P, _P, _I, _I, _I, _P], _I),
+    "smoe_down_q4": ([_P, _P, _P, _P, _I, _I, _I, _P], _I),
+    "smoe_down_q2": ([_P, _P, _P, _P, _I, _I, _I, _P], _I),
+    "matvec_bf16": ([_P, _P, _P, _I, _I, _P], _I),
+    "smoe_ffn_batch_workspace_bytes": ([_I, _I, _I, _I], _SZ),
+    "ffn_batch_q4": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "smoe_last_device_status": ([_P], _I),
+}
+for _name, (_args, _res) in _SIGS.items():
+    _f = getattr(_lib, _name)
+    _f.argtypes = _args
+    _f.restype = _res
+
+EXPORTED = tuple(_SIGS)
+
+
+class SmoeError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: status {status} ({smoe_status_string(status)})")
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    if isinstance(a, int):
+        return a
+    return a.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        if not torch.cuda.is_available():
+            return None
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(status, where):
+    if status != SMOE_OK:
+        raise SmoeError(status, where)
+
+
+def smoe_abi_version():
+    return _lib.smoe_abi_version()
+
+
+def smoe_status_string(status):
+    return _lib.smoe_status_string(int(status)).decode()
+
+
+def smoe_gate_up_q4(gate_codes, gate_scales, up_codes, up_scales, x, hidden, d_ff, d_model, group,
+                    stream=None):
+    _check(_lib.smoe_gate_up_q4(_ptr(gate_codes), _ptr(gate_scales), _ptr(up_codes), _ptr(up_scales),
+                                _ptr(x), _ptr(hidden), d_ff, d_model, group, _stream(stream)),
+           "smoe_gate_up_q4")
+
+
+def smoe_gate_up_q2(gate_codes, gate_scales, up_codes, up_scales, x, hidden, d_ff, d_model, group,
+                    stream=None):
+    _check(_lib.smoe_gate_up_q2(_ptr(gate_codes), _ptr(gate_scales), _ptr(up_codes), _ptr(up_scales),
+                                _ptr(x), _ptr(hidden), d_ff, d_model, group, _stream(stream)),
+           "smoe_gate_up_q2")
+
+
+def smoe_down_q4(down_codes, down_scales, hidden, out, d_model, d_ff, group, stream=None):
+    _check(_lib.smoe_down_q4(_ptr(down_codes), _ptr(down_scales), _ptr(hidden), _ptr(out), d_model,
+                             d_ff, group, _stream(stream)), "smoe_down_q4")
+
+
+def smoe_down_q2(down_codes, down_scales, hidden, out, d_model, d_ff, group, stream=None):
+    _check(_lib.smoe_down_q2(_ptr(down_codes), _ptr(down_scales), _ptr(hidden), _ptr(out), d_model,
+                             d_ff, group, _stream(stream)), "smoe_down_q2")
+
+
+def matvec_bf16(w, x, y, rows, cols, stream=None):
+    _check(_lib.matvec_bf16(_ptr(w), _ptr(x), _ptr(y), rows, cols, _stream(stream)), "matvec_bf16")
+
+
+def smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group):
+    return _lib.smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group)
+
+
+def ffn_batch_q4(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X, Y, T,
+                 d_model, d_ff, group, workspace, workspace_bytes, stream=None):
+    _check(_lib.ffn_batch_q4(_ptr(gate_codes), _ptr(gate_scales), _ptr(up_codes), _ptr(up_scales),
+                             _ptr(down_codes), _ptr(down_scales), _ptr(X), _ptr(Y), T, d_model,
+                             d_ff, group, _ptr(workspace), workspace_bytes, _stream(stream)),
+           "ffn_batch_q4")
+
+
+def smoe_last_device_status(stream=None):
+    return _lib.smoe_last_device_status(_stream(stream))

@@ -1,0 +1,263 @@
+// The extern "C" entry points declared in include/smoe.h: argument checks
+// on the host, then the kernel launches.  Nothing here allocates memory.
+#include <mutex>
+
+#include "internal.h"
+#include "smoe.h"
+
+namespace smoe {
+
+const DeviceInfo *device_info()
+{
+    constexpr int kMaxDevices = 64;
+    static DeviceInfo cache[kMaxDevices];
+    static bool ready[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ready[dev]) {
+        DeviceInfo d = {};
+        d.device = dev;
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return nullptr;
+        if (cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+            cudaSuccess)
+            return nullptr;
+        cache[dev] = d;
+        ready[dev] = true;
+    }
+    return &cache[dev];
+}
+
+}  // namespace smoe
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Span {
+    const void *p;
+    size_t bytes;
+};
+
+bool overlap(Span a, Span b)
+{
+    if (a.bytes == 0 || b.bytes == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.bytes && b0 < a0 + a.bytes;
+}
+
+// True if any output span overlaps any input span or another output span.
+bool any_alias(const Span *outs, int nout, const Span *ins, int nin)
+{
+    for (int i = 0; i < nout; ++i) {
+        for (int j = 0; j < nin; ++j)
+            if (overlap(outs[i], ins[j])) return true;
+        for (int j = i + 1; j < nout; ++j)
+            if (overlap(outs[i], outs[j])) return true;
+    }
+    return false;
+}
+
+int to_status(cudaError_t e) { return e == cudaSuccess ? SMOE_OK : SMOE_ERR_LAUNCH; }
+
+// Layout contract of a packed [rows x cols] matrix ("Layout assumptions the
+// kernels rely on"): cols % 32 (Q4) / % 64 (Q2), group a positive multiple of
+// the same unit dividing cols, cols <= SMOE_MAX_COLS.
+int check_q_shape(int bits, int rows, int cols, int group)
+{
+    if (rows < 0 || cols < 0) return SMOE_ERR_SHAPE;
+    if (cols > SMOE_MAX_COLS) return SMOE_ERR_SHAPE;
+    const int unit = bits == 4 ? 32 : 64;
+    if (cols % unit != 0) return SMOE_ERR_SHAPE;
+    if (group <= 0 || group % unit != 0) return SMOE_ERR_SHAPE;
+    if (cols > 0 && cols % group != 0) return SMOE_ERR_SHAPE;
+    return SMOE_OK;
+}
+
+size_t q_bytes(int bits, int rows, int cols)
+{
+    return static_cast<size_t>(rows) * static_cast<size_t>(cols) * bits / 8;
+}
+
+size_t scale_bytes(int rows, int cols, int group)
+{
+    return static_cast<size_t>(rows) * static_cast<size_t>(cols / group) * sizeof(float);
+}
+
+int gate_up_impl(int bits, const uint8_t *gc, const float *gs, const uint8_t *uc, const float *us,
+                 const float *x, float *hidden, int d_ff, int d_model, int group, void *stream)
+{
+    int st = check_q_shape(bits, d_ff, d_model, group);
+    if (st != SMOE_OK) return st;
+    if (d_ff == 0) return SMOE_OK;
+    if (!hidden) return SMOE_ERR_NULL;
+    if (!aligned16(hidden)) return SMOE_ERR_ALIGN;
+    if (d_model > 0) {
+        if (!gc || !gs || !uc || !us || !x) return SMOE_ERR_NULL;
+        if (!aligned16(gc) || !aligned16(uc) || !aligned16(gs) || !aligned16(us) || !aligned16(x))
+            return SMOE_ERR_ALIGN;
+    }
+    const Span out[1] = {{hidden, static_cast<size_t>(d_ff) * sizeof(float)}};
+    const Span in[5] = {{gc, q_bytes(bits, d_ff, d_model)},
+                        {gs, scale_bytes(d_ff, d_model, group)},
+                        {uc, q_bytes(bits, d_ff, d_model)},
+                        {us, scale_bytes(d_ff, d_model, group)},
+                        {x, static_cast<size_t>(d_model) * sizeof(float)}};
+    if (any_alias(out, 1, in, 5)) return SMOE_ERR_ALIAS;
+    const uint8_t *codes[2] = {gc, uc};
+    const float *scales[2] = {gs, us};
+    return to_status(smoe::launch_qgemv(bits, 2, codes, scales, x, hidden, d_ff, d_model, group,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int down_impl(int bits, const uint8_t *dc, const float *ds, const float *hidden, float *out,
+              int d_model, int d_ff, int group, void *stream)
+{
+    int st = check_q_shape(bits, d_model, d_ff, group);
+    if (st != SMOE_OK) return st;
+    if (d_model == 0) return SMOE_OK;
+    if (!out) return SMOE_ERR_NULL;
+    if (!aligned16(out)) return SMOE_ERR_ALIGN;
+    if (d_ff > 0) {
+        if (!dc || !ds || !hidden) return SMOE_ERR_NULL;
+        if (!aligned16(dc) || !aligned16(ds) || !aligned16(hidden)) return SMOE_ERR_ALIGN;
+    }
+    const Span o[1] = {{out, static_cast<size_t>(d_model) * sizeof(float)}};
+    const Span in[3] = {{dc, q_bytes(bits, d_model, d_ff)},
+                        {ds, scale_bytes(d_model, d_ff, group)},
+                        {hidden, static_cast<size_t>(d_ff) * sizeof(float)}};
+    if (any_alias(o, 1, in, 3)) return SMOE_ERR_ALIAS;
+    const uint8_t *codes[2] = {dc, dc};
+    const float *scales[2] = {ds, ds};
+    return to_status(smoe::launch_qgemv(bits, 1, codes, scales, hidden, out, d_model, d_ff, group,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+}  // namespace
+
+extern "C" {
+
+int smoe_abi_version(void) { return SMOE_ABI_VERSION; }
+
+const char *smoe_status_string(int status)
+{
+    switch (status) {
+    case SMOE_OK: return "ok";
+    case SMOE_ERR_NULL: return "a required pointer is NULL";
+    case SMOE_ERR_ALIGN: return "a pointer is not 16-byte aligned";
+    case SMOE_ERR_SHAPE: return "sizes break the layout contract or the limits";
+    case SMOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case SMOE_ERR_LAUNCH: return "CUDA launch or device query failed";
+    case SMOE_ERR_TIMEOUT: return "a device-side bounded wait gave up";
+    case SMOE_ERR_ALIAS: return "an output overlaps an input or another output";
+    default: return "unknown status";
+    }
+}
+
+int smoe_gate_up_q4(const uint8_t *gate_codes, const float *gate_scales, const uint8_t *up_codes,
+                    const float *up_scales, const float *x, float *hidden, int d_ff, int d_model,
+                    int group, void *stream)
+{
+    return gate_up_impl(4, gate_codes, gate_scales, up_codes, up_scales, x, hidden, d_ff, d_model,
+                        group, stream);
+}
+
+int smoe_gate_up_q2(const uint8_t *gate_codes, const float *gate_scales, const uint8_t *up_codes,
+                    const float *up_scales, const float *x, float *hidden, int d_ff, int d_model,
+                    int group, void *stream)
+{
+    return gate_up_impl(2, gate_codes, gate_scales, up_codes, up_scales, x, hidden, d_ff, d_model,
+                        group, stream);
+}
+
+int smoe_down_q4(const uint8_t *down_codes, const float *down_scales, const float *hidden,
+                 float *out, int d_model, int d_ff, int group, void *stream)
+{
+    return down_impl(4, down_codes, down_scales, hidden, out, d_model, d_ff, group, stream);
+}
+
+int smoe_down_q2(const uint8_t *down_codes, const float *down_scales, const float *hidden,
+                 float *out, int d_model, int d_ff, int group, void *stream)
+{
+    return down_impl(2, down_codes, down_scales, hidden, out, d_model, d_ff, group, stream);
+}
+
+int matvec_bf16(const uint16_t *w, const float *x, float *y, int rows, int cols, void *stream)
+{
+    if (rows < 0 || cols < 0 || cols > SMOE_MAX_COLS || cols % 8 != 0) return SMOE_ERR_SHAPE;
+    if (rows == 0) return SMOE_OK;
+    if (!y) return SMOE_ERR_NULL;
+    if (!aligned16(y)) return SMOE_ERR_ALIGN;
+    if (cols > 0) {
+        if (!w || !x) return SMOE_ERR_NULL;
+        if (!aligned16(w) || !aligned16(x)) return SMOE_ERR_ALIGN;
+    }
+    const Span o[1] = {{y, static_cast<size_t>(rows) * sizeof(float)}};
+    const Span in[2] = {{w, static_cast<size_t>(rows) * static_cast<size_t>(cols) * 2},
+                        {x, static_cast<size_t>(cols) * sizeof(float)}};
+    if (any_alias(o, 1, in, 2)) return SMOE_ERR_ALIAS;
+    return to_status(smoe::launch_bf16_gemv(w, x, y, rows, cols, static_cast<cudaStream_t>(stream)));
+}
+
+size_t smoe_ffn_batch_workspace_bytes(int T, int d_model, int d_ff, int group)
+{
+    if (T <= 0) return 0;
+    if (check_q_shape(4, d_ff, d_model, group) != SMOE_OK ||
+        check_q_shape(4, d_model, d_ff, group) != SMOE_OK)
+        return static_cast<size_t>(-1);
+    return smoe::ffn_batch_workspace(T, d_model, d_ff, group);
+}
+
+int ffn_batch_q4(const uint8_t *gate_codes, const float *gate_scales, const uint8_t *up_codes,
+                 const float *up_scales, const uint8_t *down_codes, const float *down_scales,
+                 const float *X, float *Y, int T, int d_model, int d_ff, int group,
+                 void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (T < 0) return SMOE_ERR_SHAPE;
+    int st = check_q_shape(4, d_ff, d_model, group);
+    if (st != SMOE_OK) return st;
+    st = check_q_shape(4, d_model, d_ff, group);
+    if (st != SMOE_OK) return st;
+    if (T == 0 || d_model == 0) return SMOE_OK;
+    if (!X || !Y) return SMOE_ERR_NULL;
+    if (!aligned16(X) || !aligned16(Y)) return SMOE_ERR_ALIGN;
+    if (d_ff > 0) {
+        if (!gate_codes || !gate_scales || !up_codes || !up_scales || !down_codes || !down_scales)
+            return SMOE_ERR_NULL;
+        if (!aligned16(gate_codes) || !aligned16(gate_scales) || !aligned16(up_codes) ||
+            !aligned16(up_scales) || !aligned16(down_codes) || !aligned16(down_scales))
+            return SMOE_ERR_ALIGN;
+    }
+    const size_t need = smoe::ffn_batch_workspace(T, d_model, d_ff, group);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return SMOE_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return SMOE_ERR_ALIGN;
+    }
+    const size_t xy = static_cast<size_t>(T) * static_cast<size_t>(d_model) * sizeof(float);
+    const Span outs[2] = {{Y, xy}, {workspace, need}};
+    const Span ins[7] = {{gate_codes, q_bytes(4, d_ff, d_model)},
+                         {gate_scales, scale_bytes(d_ff, d_model, group)},
+                         {up_codes, q_bytes(4, d_ff, d_model)},
+                         {up_scales, scale_bytes(d_ff, d_model, group)},
+                         {down_codes, q_bytes(4, d_model, d_ff)},
+                         {down_scales, scale_bytes(d_model, d_ff, group)},
+                         {X, xy}};
+    if (any_alias(outs, 2, ins, 7)) return SMOE_ERR_ALIAS;
+    const uint8_t *gu_codes[2] = {gate_codes, up_codes};
+    const float *gu_scales[2] = {gate_scales, up_scales};
+    return to_status(smoe::launch_ffn_batch(gu_codes, gu_scales, down_codes, down_scales, X, Y, T,
+                                            d_model, d_ff, group, workspace,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
+int smoe_last_device_status(void *stream)
+{
+    unsigned v = 0;
+    if (smoe::read_and_clear_device_status(static_cast<cudaStream_t>(stream), &v) != cudaSuccess)
+        return SMOE_ERR_LAUNCH;
+    return v ? SMOE_ERR_TIMEOUT : SMOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,246 @@
+// Token-batch fused FFN of one Q4 expert, the S-MoE page "Metal Compute
+// Kernels", section "Token-Batch Fused FFN": the one-token FFN applied to
+// every row of X [T x d_model], gate/up+SiLU into H [T x d_ff] (the caller's
+// workspace), then down into Y [T x d_model].
+//
+// This file holds the CUDA-core path: a multi-token GEMV in which a warp
+// unpacks each 16-byte chunk of codes once and applies it to TT tokens whose
+// x rows are staged in shared memory.  One token goes through the decode
+// kernels instead (qgemv.cu).
+#include "common.cuh"
+#include "internal.h"
+#include "qformat.cuh"
+
+namespace smoe {
+
+// Device status word: set by device-side bounded waits that gave up.
+__device__ unsigned int g_device_status = 0;
+
+struct QTokArgs {
+    const uint8_t *codes[2];
+    const float *scales[2];
+    const float *X;  // [T x K]
+    float *Y;        // [T x units]
+    int T;
+    int units;
+    int K;
+    int group;
+};
+
+template <int BITS, int NMAT, int TT>
+__global__ void __launch_bounds__(256) qgemm_tokens(QTokArgs a)
+{
+    using F = QFmt<BITS>;
+    constexpr int F4W = F::CODES_PER_WORD / 4;
+    extern __shared__ __align__(16) float4 smem4[];
+    const int KC = a.K / F::CODES_PER_CHUNK;
+    const int nq = a.K >> 2;
+    float4 *xs = smem4;                                                   // [TT][nq]
+    float *sx = reinterpret_cast<float *>(smem4 + static_cast<size_t>(TT) * nq);  // [TT][KC]
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int ngroups = a.K / a.group;
+    const int cpg = a.group / F::CODES_PER_CHUNK;
+    const size_t row_bytes = static_cast<size_t>(KC) * 16;
+
+    pdl_wait();
+
+    const uint32_t xs_base = smem_addr(xs);
+    uint32_t xo[8];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) xo[m] = static_cast<uint32_t>(m ^ (lane & 7)) * 16u;
+
+    for (int tb = blockIdx.y * TT; tb < a.T; tb += gridDim.y * TT) {
+        __syncthreads();  // the previous tile's readers are done
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+            const int tok = tb + t < a.T ? tb + t : a.T - 1;  // repeat the last token as padding
+            stage_x_chunks<BITS>(a.X + static_cast<size_t>(tok) * a.K, a.K, xs + static_cast<size_t>(t) * nq,
+                                 sx + static_cast<size_t>(t) * KC);
+        }
+        __syncthreads();
+
+        for (int unit = blockIdx.x * nwarps + warp; unit < a.units; unit += gridDim.x * nwarps) {
+            float acc1[NMAT][TT], acc2[NMAT][TT];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                for (int t = 0; t < TT; ++t) acc1[m][t] = acc2[m][t] = 0.f;
+
+            for (int cc = lane; cc < KC; cc += 32) {
+                uint4 cw[NMAT];
+                float sc[NMAT];
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m) {
+                    cw[m] = ldg_stream(a.codes[m] + unit * row_bytes + static_cast<size_t>(cc) * 16);
+                    sc[m] = ldg_f32(a.scales[m] + static_cast<size_t>(unit) * ngroups + cc / cpg);
+                }
+                float P[NMAT][TT];
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                    for (int t = 0; t < TT; ++t) P[m][t] = 0.f;
+                const uint32_t cbase = xs_base + static_cast<uint32_t>(cc * F::F4_PER_CHUNK) * 16u;
+#pragma unroll
+                for (int wi = 0; wi < 4; ++wi) {
+                    float f[NMAT][F::CODES_PER_WORD];
+#pragma unroll
+                    for (int m = 0; m < NMAT; ++m) {
+                        const uint32_t w = word_of(cw[m], wi);
+#pragma unroll
+                        for (int i = 0; i < F::CODES_PER_WORD; ++i) f[m][i] = code_as_f32<BITS>(w, i);
+                    }
+#pragma unroll
+                    for (int t = 0; t < TT; ++t) {
+                        const uint32_t tbase = cbase + static_cast<uint32_t>(t) * static_cast<uint32_t>(nq) * 16u;
+#pragma unroll
+                        for (int q = 0; q < F4W; ++q) {
+                            const int mq = wi * F4W + q;
+                            const float4 v = lds128(tbase + static_cast<uint32_t>((mq & 8) * 16) + xo[mq & 7]);
+#pragma unroll
+                            for (int m = 0; m < NMAT; ++m) {
+                                P[m][t] = fmaf(f[m][4 * q + 0], v.x, P[m][t]);
+                                P[m][t] = fmaf(f[m][4 * q + 1], v.y, P[m][t]);
+                                P[m][t] = fmaf(f[m][4 * q + 2], v.z, P[m][t]);
+                                P[m][t] = fmaf(f[m][4 * q + 3], v.w, P[m][t]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    const float sxc = sx[t * KC + cc];
+#pragma unroll
+                    for (int m = 0; m < NMAT; ++m) {
+                        acc1[m][t] = fmaf(sc[m], P[m][t], acc1[m][t]);
+                        acc2[m][t] = fmaf(sc[m], sxc, acc2[m][t]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                for (int t = 0; t < TT; ++t)
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) {
+                        acc1[m][t] += __shfl_xor_sync(FULL_MASK, acc1[m][t], off);
+                        acc2[m][t] += __shfl_xor_sync(FULL_MASK, acc2[m][t], off);
+                    }
+            if (lane == 0) {
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    if (tb + t < a.T) {
+                        const float y0 = F::A * acc1[0][t] - (F::A + 1.0f) * acc2[0][t];
+                        float out = y0;
+                        if (NMAT == 2) {
+                            const float y1 = F::A * acc1[NMAT - 1][t] - (F::A + 1.0f) * acc2[NMAT - 1][t];
+                            out = silu_f32(y0) * y1;
+                        }
+                        a.Y[static_cast<size_t>(tb + t) * a.units + unit] = out;
+                    }
+                }
+            }
+        }
+    }
+    pdl_launch_dependents();
+}
+
+namespace {
+
+template <int BITS, int NMAT, int TT>
+cudaError_t launch_tok(const QTokArgs &a, cudaStream_t stream)
+{
+    using F = QFmt<BITS>;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return cudaErrorInvalidDevice;
+    const int KC = a.K / F::CODES_PER_CHUNK;
+    const size_t smem = static_cast<size_t>(TT) * (static_cast<size_t>(a.K) + KC) * sizeof(float);
+    if (smem > static_cast<size_t>(dev->max_smem_optin)) return cudaErrorInvalidValue;
+    const int warps = 8;
+    long long gx = (static_cast<long long>(a.units) + warps - 1) / warps;
+    const int tiles = (a.T + TT - 1) / TT;
+    long long gy = tiles < 65535 ? tiles : 65535;
+    const long long cap = static_cast<long long>(dev->sm_count) * 2;
+    if (gx * gy > cap * 8 && gx > cap) gx = cap;
+    auto k = qgemm_tokens<BITS, NMAT, TT>;
+    cudaError_t e = ensure_dynamic_smem(k, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k, dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), dim3(warps * 32),
+                      smem, stream, a);
+}
+
+template <int NMAT>
+cudaError_t launch_tok_pick(const QTokArgs &a, cudaStream_t stream)
+{
+    // Token tile: enough tokens to amortise the unpack, few enough that the
+    // x rows of a tile fit in shared memory.
+    const size_t per_token = (static_cast<size_t>(a.K) + a.K / 32) * sizeof(float);
+    if (a.T >= 8 && per_token * 8 <= 200 * 1024) return launch_tok<4, NMAT, 8>(a, stream);
+    if (a.T >= 4 && per_token * 4 <= 200 * 1024) return launch_tok<4, NMAT, 4>(a, stream);
+    if (a.T >= 2 && per_token * 2 <= 200 * 1024) return launch_tok<4, NMAT, 2>(a, stream);
+    return launch_tok<4, NMAT, 1>(a, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_qgemm_tokens(int bits, int nmat, const uint8_t *const codes[2],
+                                const float *const scales[2], const float *X, float *Y, int T,
+                                int units, int K, int group, cudaStream_t stream)
+{
+    if (bits != 4) return cudaErrorInvalidValue;
+    QTokArgs a = {};
+    a.codes[0] = codes[0];
+    a.codes[1] = nmat == 2 ? codes[1] : codes[0];
+    a.scales[0] = scales[0];
+    a.scales[1] = nmat == 2 ? scales[1] : scales[0];
+    a.X = X;
+    a.Y = Y;
+    a.T = T;
+    a.units = units;
+    a.K = K;
+    a.group = group;
+    return nmat == 2 ? launch_tok_pick<2>(a, stream) : launch_tok_pick<1>(a, stream);
+}
+
+size_t ffn_batch_workspace(int T, int d_model, int d_ff, int group)
+{
+    (void)d_model;
+    (void)group;
+    if (T <= 0) return 0;
+    const size_t hidden = static_cast<size_t>(T) * static_cast<size_t>(d_ff) * sizeof(float);
+    return (hidden + 255) & ~static_cast<size_t>(255);
+}
+
+cudaError_t launch_ffn_batch(const uint8_t *const gu_codes[2], const float *const gu_scales[2],
+                             const uint8_t *down_codes, const float *down_scales, const float *X,
+                             float *Y, int T, int d_model, int d_ff, int group, void *workspace,
+                             cudaStream_t stream)
+{
+    float *H = static_cast<float *>(workspace);
+    const uint8_t *dc[2] = {down_codes, down_codes};
+    const float *ds[2] = {down_scales, down_scales};
+    cudaError_t e = cudaSuccess;
+    if (T == 1) {
+        if (d_ff > 0) e = launch_qgemv(4, 2, gu_codes, gu_scales, X, H, d_ff, d_model, group, stream);
+        if (e != cudaSuccess) return e;
+        return launch_qgemv(4, 1, dc, ds, H, Y, d_model, d_ff, group, stream);
+    }
+    if (d_ff > 0)
+        e = launch_qgemm_tokens(4, 2, gu_codes, gu_scales, X, H, T, d_ff, d_model, group, stream);
+    if (e != cudaSuccess) return e;
+    return launch_qgemm_tokens(4, 1, dc, ds, H, Y, T, d_model, d_ff, group, stream);
+}
+
+cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned *value)
+{
+    cudaError_t e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemcpyFromSymbol(value, g_device_status, sizeof(unsigned));
+    if (e != cudaSuccess) return e;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_device_status, &zero, sizeof(unsigned));
+}
+
+}  // namespace smoe

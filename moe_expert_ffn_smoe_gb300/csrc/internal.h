@@ -1,0 +1,78 @@
+// Host-side interfaces between the C ABI (api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace smoe {
+
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int max_smem_optin;  // largest dynamic shared memory one block may opt into
+};
+
+// Properties of the current device, cached per device; nullptr if the
+// device cannot be queried.
+const DeviceInfo *device_info();
+
+// Launches y = W x for `units` output rows of a packed Q4/Q2 matrix, or the
+// fused gate/up pass when nmat == 2 (codes[0]/scales[0] = gate,
+// codes[1]/scales[1] = up, y = hidden).  Shapes are already validated.
+cudaError_t launch_qgemv(int bits, int nmat, const uint8_t *const codes[2],
+                         const float *const scales[2], const float *x, float *y,
+                         int units, int K, int group, cudaStream_t stream);
+
+// Launches y = W x for a bf16 [rows x K] matrix.  Shapes already validated.
+cudaError_t launch_bf16_gemv(const uint16_t *w, const float *x, float *y, int rows, int K,
+                             cudaStream_t stream);
+
+// Token batch: Y[T x units] = W X^T for T tokens (nmat == 2: fused gate/up,
+// Y = hidden).  Shapes already validated.
+cudaError_t launch_qgemm_tokens(int bits, int nmat, const uint8_t *const codes[2],
+                                const float *const scales[2], const float *X, float *Y,
+                                int T, int units, int K, int group, cudaStream_t stream);
+
+// Bytes of workspace the batch FFN needs (0 for T <= 0).
+size_t ffn_batch_workspace(int T, int d_model, int d_ff, int group);
+
+// The whole batch FFN: gate/up into the workspace, then down into Y.
+cudaError_t launch_ffn_batch(const uint8_t *const gu_codes[2], const float *const gu_scales[2],
+                             const uint8_t *down_codes, const float *down_scales,
+                             const float *X, float *Y, int T, int d_model, int d_ff, int group,
+                             void *workspace, cudaStream_t stream);
+
+// Reads and clears the device status word of the current device after
+// synchronising `stream`.
+cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned *value);
+
+// cudaLaunchKernelEx with programmatic dependent launch enabled.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Opts a kernel into more than 48 KB of dynamic shared memory when needed.
+template <typename K>
+cudaError_t ensure_dynamic_smem(K kernel, size_t bytes)
+{
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel),
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(bytes));
+}
+
+}  // namespace smoe

@@ -1,0 +1,136 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library validates every argument on the host before touching CUDA, so
+calls that break the contract return their status here without a device.
+Pointer arguments in these tests are plain integers that are never
+dereferenced: every call below is refused before any launch (a call that
+passed the checks would launch, so none is made here).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "smoe.h")
+
+
+@pytest.fixture(scope="module")
+def smoe():
+    from moe_expert_ffn_smoe_gb300 import _build
+    _build.build()
+    import moe_expert_ffn_smoe_gb300 as m
+    return m
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\**\s*([a-z_][a-z_0-9]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_function(smoe):
+    names = _declared_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(smoe.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in smoe.h but not exported"
+    assert set(names) == set(smoe.EXPORTED)
+
+
+def test_abi_version_and_status_strings(smoe):
+    assert smoe.smoe_abi_version() == 1
+    for s in range(8):
+        assert smoe.smoe_status_string(s)
+    assert smoe.smoe_status_string(99) == "unknown status"
+
+
+A = 1 << 20  # an aligned fake device address (never dereferenced)
+
+
+def _gu(smoe, fn, d_ff=256, d_model=256, group=64, ptrs=None, stream=0):
+    p = ptrs or [A, A + 0x100000, A + 0x200000, A + 0x300000, A + 0x400000, A + 0x500000]
+    return fn(*p, d_ff, d_model, group, stream)
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_gate_up_refuses_bad_shapes(smoe, bits):
+    f = smoe._lib.smoe_gate_up_q4 if bits == 4 else smoe._lib.smoe_gate_up_q2
+    unit = 32 if bits == 4 else 64
+    assert _gu(smoe, f, d_model=unit + 16) == smoe.SMOE_ERR_SHAPE        # cols not a multiple
+    assert _gu(smoe, f, group=unit // 2) == smoe.SMOE_ERR_SHAPE           # group not a multiple
+    assert _gu(smoe, f, d_model=3 * unit, group=2 * unit) == smoe.SMOE_ERR_SHAPE  # group !| cols
+    assert _gu(smoe, f, group=0) == smoe.SMOE_ERR_SHAPE
+    assert _gu(smoe, f, d_ff=-1) == smoe.SMOE_ERR_SHAPE
+    assert _gu(smoe, f, d_model=smoe.SMOE_MAX_COLS + 64 * 16) == smoe.SMOE_ERR_SHAPE
+
+
+def test_gate_up_refuses_null_misaligned_alias(smoe):
+    f = smoe._lib.smoe_gate_up_q4
+    base = [A, A + 0x100000, A + 0x200000, A + 0x300000, A + 0x400000, A + 0x500000]
+    for i in range(6):
+        p = list(base)
+        p[i] = None
+        assert _gu(smoe, f, ptrs=p) == smoe.SMOE_ERR_NULL
+        p = list(base)
+        p[i] += 4
+        assert _gu(smoe, f, ptrs=p) == smoe.SMOE_ERR_ALIGN
+    p = list(base)
+    p[5] = p[4] + 512          # hidden overlaps x (x is 1 KB)
+    assert _gu(smoe, f, ptrs=p) == smoe.SMOE_ERR_ALIAS
+    p = list(base)
+    p[5] = p[0] + 16           # hidden inside the gate codes
+    assert _gu(smoe, f, ptrs=p) == smoe.SMOE_ERR_ALIAS
+
+
+def test_empty_output_is_a_no_op_without_pointers(smoe):
+    L = smoe._lib
+    assert L.smoe_gate_up_q4(None, None, None, None, None, None, 0, 256, 64, None) == 0
+    assert L.smoe_down_q2(None, None, None, None, 0, 256, 64, None) == 0
+    assert L.matvec_bf16(None, None, None, 0, 64, None) == 0
+    assert L.ffn_batch_q4(None, None, None, None, None, None, None, None, 0, 256, 256, 64, None, 0,
+                          None) == 0
+
+
+def test_down_refusals(smoe):
+    L = smoe._lib
+    ok = [A, A + 0x100000, A + 0x200000, A + 0x300000]
+    assert L.smoe_down_q4(*ok, 256, 96, 64, None) == smoe.SMOE_ERR_SHAPE     # 96 % 64 != 0
+    assert L.smoe_down_q2(*ok, 256, 96, 64, None) == smoe.SMOE_ERR_SHAPE     # Q2 wants % 64
+    assert L.smoe_down_q4(ok[0], ok[1], ok[2], None, 256, 256, 64, None) == smoe.SMOE_ERR_NULL
+    assert L.smoe_down_q4(ok[0], ok[1] + 8, ok[2], ok[3], 256, 256, 64, None) == smoe.SMOE_ERR_ALIGN
+    assert L.smoe_down_q4(ok[0], ok[1], ok[2], ok[2] + 64, 256, 256, 64, None) == smoe.SMOE_ERR_ALIAS
+
+
+def test_bf16_refusals(smoe):
+    L = smoe._lib
+    assert L.matvec_bf16(A, A + 0x100000, A + 0x200000, 16, 12, None) == smoe.SMOE_ERR_SHAPE
+    assert L.matvec_bf16(A, A + 0x100000, A + 0x200000, 16, smoe.SMOE_MAX_COLS + 8, None) == \
+        smoe.SMOE_ERR_SHAPE
+    assert L.matvec_bf16(A + 2, A + 0x100000, A + 0x200000, 16, 64, None) == smoe.SMOE_ERR_ALIGN
+    assert L.matvec_bf16(A, None, A + 0x200000, 16, 64, None) == smoe.SMOE_ERR_NULL
+    assert L.matvec_bf16(A, A + 0x100000, A + 16, 16, 64, None) == smoe.SMOE_ERR_ALIAS
+
+
+def test_batch_workspace_size_and_refusals(smoe):
+    L = smoe._lib
+    need = L.smoe_ffn_batch_workspace_bytes(16, 4096, 1536, 64)
+    assert need >= 16 * 1536 * 4 and need % 256 == 0
+    assert L.smoe_ffn_batch_workspace_bytes(0, 4096, 1536, 64) == 0
+    assert L.smoe_ffn_batch_workspace_bytes(4, 4096, 1536, 48) == ctypes.c_size_t(-1).value
+    w = [A + i * 0x1000000 for i in range(6)]
+    X, Y, ws = A + 0x8000000, A + 0x9000000, A + 0xA000000
+    args = lambda T, wsp, wsb: (*w, X, Y, T, 4096, 1536, 64, wsp, wsb, None)
+    assert L.ffn_batch_q4(*args(16, ws, need - 256)) == smoe.SMOE_ERR_WORKSPACE
+    assert L.ffn_batch_q4(*args(16, None, need)) == smoe.SMOE_ERR_WORKSPACE
+    assert L.ffn_batch_q4(*args(16, ws + 8, need)) == smoe.SMOE_ERR_ALIGN
+    assert L.ffn_batch_q4(*args(-1, ws, need)) == smoe.SMOE_ERR_SHAPE
+    assert L.ffn_batch_q4(*args(16, X + 1024, need)) == smoe.SMOE_ERR_ALIAS   # workspace inside X
+
+
+def test_binding_raises_with_status(smoe):
+    with pytest.raises(smoe.SmoeError) as ei:
+        smoe.smoe_gate_up_q4(A, A, A, A, A, A, 256, 100, 64, stream=0)
+    assert ei.value.status == smoe.SMOE_ERR_SHAPE
