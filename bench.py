@@ -261,8 +261,8 @@ def roofline_traffic(kernel_name):
 
 def gpu_arm(args, rank, world, local):
     import torch
-    from moe_expert_ffn_smoe_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build_library()
     import moe_expert_ffn_smoe_gb300 as smoe
 
     dev = torch.device(f"cuda:{local}")

@@ -18,8 +18,8 @@ HEADER = os.path.join(ROOT, "include", "smoe.h")
 
 @pytest.fixture(scope="module")
 def smoe():
-    from moe_expert_ffn_smoe_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build_library()
     import moe_expert_ffn_smoe_gb300 as m
     return m
 

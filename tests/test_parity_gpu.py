@@ -21,8 +21,8 @@ Z = {4: 7.5, 2: 1.5}
 def dev():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
-    from moe_expert_ffn_smoe_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__.build_library()
     d = torch.device("cuda:0")
     torch.cuda.set_device(d)
     return d
