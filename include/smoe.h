@@ -165,6 +165,39 @@ int ffn_batch_q4(const uint8_t *gate_codes, const float *gate_scales,
                  int T, int d_model, int d_ff, int group,
                  void *workspace, size_t workspace_bytes, void *stream);
 
+/* Size of the device array ffn_batch_q4_noalloc uses as its workspace. */
+#define SMOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+
+/*
+ * ffn_batch_q4 for callers that must not allocate device memory: a host
+ * program that has already divided all device memory among its own pools, a
+ * plugin loaded into such a program, or a latency-critical caller for which
+ * cudaMalloc's implicit device-wide synchronisation is not acceptable.  The
+ * paper has no counterpart to this entry point; it exists only for such
+ * callers.
+ *
+ * Same arguments, results and checks as ffn_batch_q4, without `workspace`:
+ * the workspace is a file-scope device array of SMOE_NOALLOC_SCRATCH_BYTES
+ * inside the library, which every GPU that loads the library holds until
+ * the process exits.  Calls whose workspace need,
+ * smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group), exceeds that size
+ * are refused with SMOE_ERR_SHAPE before anything is launched (4 MiB holds
+ * T * d_ff <= 1,048,576 hidden values, e.g. T = 682 at d_ff = 1536).
+ * The function calls no cudaMalloc, cudaFree or other allocating routine.
+ *
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress while that device is current; make that first call
+ * before any stream capture on the device.  All calls share the one array,
+ * and it keeps the last call's contents: calls that overlap on the GPU (on
+ * different streams, or from different host threads without ordering) race
+ * on it and must be serialised by the caller.
+ */
+int ffn_batch_q4_noalloc(const uint8_t *gate_codes, const float *gate_scales,
+                         const uint8_t *up_codes, const float *up_scales,
+                         const uint8_t *down_codes, const float *down_scales,
+                         const float *X, float *Y,
+                         int T, int d_model, int d_ff, int group, void *stream);
+
 /*
  * Reads and clears the library's device status word for the current device
  * after synchronising `stream`.  Kernels that wait on the device (bounded

@@ -34,6 +34,7 @@ SMOE_ERR_LAUNCH = 5
 SMOE_ERR_TIMEOUT = 6
 SMOE_ERR_ALIAS = 7
 SMOE_MAX_COLS = 32768
+SMOE_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -49,6 +50,7 @@ _SIGS = {
     "matvec_bf16": ([_P, _P, _P, _I, _I, _P], _I),
     "smoe_ffn_batch_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "ffn_batch_q4": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "ffn_batch_q4_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "smoe_last_device_status": ([_P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
@@ -135,6 +137,16 @@ def ffn_batch_q4(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_
                              _ptr(down_codes), _ptr(down_scales), _ptr(X), _ptr(Y), T, d_model,
                              d_ff, group, _ptr(workspace), workspace_bytes, _stream(stream)),
            "ffn_batch_q4")
+
+
+def ffn_batch_q4_noalloc(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X,
+                         Y, T, d_model, d_ff, group, stream=None):
+    """ffn_batch_q4 with the library's static device workspace, for callers
+    that must not allocate device memory (see include/smoe.h)."""
+    _check(_lib.ffn_batch_q4_noalloc(_ptr(gate_codes), _ptr(gate_scales), _ptr(up_codes),
+                                     _ptr(up_scales), _ptr(down_codes), _ptr(down_scales), _ptr(X),
+                                     _ptr(Y), T, d_model, d_ff, group, _stream(stream)),
+           "ffn_batch_q4_noalloc")
 
 
 def smoe_last_device_status(stream=None):
