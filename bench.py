@@ -1,11 +1,14 @@
 """Benchmark of the routed-expert GEMV path on GB300.
 
 One step = one token through the 8-expert Q4 decode (d_model 4096, d_ff 1536,
-group 64): for each expert the fused gate/up call and the down call of the C
-ABI, 16 calls, captured once into a CUDA graph and replayed.  The metric is
-effective HBM bandwidth, (packed codes + scales + x + out bytes) / device
-time, and the time per 8-expert FFN.  Weights rotate over several copies
-whose total is far larger than L2, so every step reads its weights from HBM.
+group 64): the fused gate/up of all 8 experts in one grouped C-ABI call, then
+their down projections in a second (smoe_experts_gate_up_q4 /
+smoe_experts_down_q4), captured into a CUDA graph and replayed.  The same
+step as 16 single-expert calls is timed alongside (`per_expert_calls`).
+The metric is effective HBM bandwidth, (packed codes + scales + x + out
+bytes) / device time, and the time per 8-expert FFN.  Weights rotate over
+several copies whose total is far larger than L2, so every step reads its
+weights from HBM.
 
 Printed: one JSON line (rank 0).  Besides the contract keys it carries the
 roofline of the dominant kernel, the end-to-end figure through host buffers,
@@ -157,11 +160,13 @@ class DecodeWorkload:
     """n_copies independent sets of 8 experts (bits = 4 or 2) resident on the
     device, one captured graph per copy, plus the token and outputs."""
 
-    def __init__(self, smoe, dev, bits, seed, n_copies):
+    def __init__(self, smoe, dev, bits, seed, n_copies, grouped=False):
         import torch
-        self.smoe, self.dev, self.bits = smoe, dev, bits
+        self.smoe, self.dev, self.bits, self.grouped = smoe, dev, bits, grouped
         self.gate_up = smoe.smoe_gate_up_q4 if bits == 4 else smoe.smoe_gate_up_q2
         self.down = smoe.smoe_down_q4 if bits == 4 else smoe.smoe_down_q2
+        self.g_gate_up = smoe.smoe_experts_gate_up_q4 if bits == 4 else smoe.smoe_experts_gate_up_q2
+        self.g_down = smoe.smoe_experts_down_q4 if bits == 4 else smoe.smoe_experts_down_q2
         self.copies = []
         for c in range(n_copies):
             ex = []
@@ -176,6 +181,14 @@ class DecodeWorkload:
         self.graphs = []
 
     def calls(self, c, stream):
+        if self.grouped:
+            ex = self.copies[c]
+            self.g_gate_up([t["gate_codes"] for t in ex], [t["gate_scales"] for t in ex],
+                           [t["up_codes"] for t in ex], [t["up_scales"] for t in ex], self.x, self.hidden,
+                           D_FF, D_MODEL, GROUP, stream=stream)
+            self.g_down([t["down_codes"] for t in ex], [t["down_scales"] for t in ex], self.hidden, self.out,
+                        D_MODEL, D_FF, GROUP, stream=stream)
+            return
         for i, t in enumerate(self.copies[c]):
             self.gate_up(t["gate_codes"], t["gate_scales"], t["up_codes"], t["up_scales"], self.x,
                          self.hidden[i], D_FF, D_MODEL, GROUP, stream=stream)
@@ -268,10 +281,17 @@ def gpu_arm(args, rank, world, local):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     n_copies = max(2, -(-4 * L2_BYTES // step_bytes(4)))  # working set >= 4x L2
-    wl = DecodeWorkload(smoe, dev, 4, 5, n_copies)
+    wl = DecodeWorkload(smoe, dev, 4, 5, n_copies, grouped=True)
     wl.capture()
     wl.run(max(3, args.warmup))
     wl.stream.synchronize()
+    # the same step as 16 single-expert calls (8 x gate/up + down)
+    calls = DecodeWorkload(smoe, dev, 4, 5, 0, grouped=False)
+    calls.copies = wl.copies
+    calls.x, calls.hidden, calls.out = wl.x, wl.hidden, wl.out
+    calls.capture()
+    calls.run(max(3, args.warmup))
+    calls.stream.synchronize()
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     barrier(world)
@@ -282,25 +302,29 @@ def gpu_arm(args, rank, world, local):
     clock_rec = clocks.stop()
     barrier(world)
     t = max_over_ranks(t, world, dev)
+    t_calls = time_steps(lambda k: calls.run(k), args.steps, calls.stream)
+    t_calls = max_over_ranks(t_calls, world, dev)
 
     sb = step_bytes(4)
     value = sb * args.steps * world / t / 1e9
     ms = t / args.steps * 1e3
     hbm_peak, peak_kind = peaks()
 
-    # Dominant kernel: the fused gate/up launch (2/3 of the bytes), timed alone.
-    gu_bytes = 2 * q_bytes(4, D_FF, D_MODEL, GROUP) + D_MODEL * 4 + D_FF * 4
-    nlaunch = len(wl.copies) * N_EXPERTS
+    # Dominant kernel: the grouped gate/up launch (2/3 of the bytes), timed alone.
+    gu_bytes = N_EXPERTS * 2 * q_bytes(4, D_FF, D_MODEL, GROUP) + D_MODEL * 4 + N_EXPERTS * D_FF * 4
+    nlaunch = 4 * len(wl.copies)
+    ptrs = [[[t[k] for t in ex] for k in ("gate_codes", "gate_scales", "up_codes", "up_scales")]
+            for ex in wl.copies]
 
     def gu_launch(i):
-        tt = wl.copies[i // N_EXPERTS % len(wl.copies)][i % N_EXPERTS]
-        smoe.smoe_gate_up_q4(tt["gate_codes"], tt["gate_scales"], tt["up_codes"], tt["up_scales"],
-                             wl.x, wl.hidden[i % N_EXPERTS], D_FF, D_MODEL, GROUP, stream=wl.stream)
+        smoe.smoe_experts_gate_up_q4(*ptrs[i % len(wl.copies)], wl.x, wl.hidden, D_FF, D_MODEL, GROUP,
+                                     stream=wl.stream)
 
     kernel_alone_seconds(gu_launch, nlaunch, wl.stream)  # warm
-    t_gu = kernel_alone_seconds(gu_launch, 4 * nlaunch, wl.stream)
+    t_gu = kernel_alone_seconds(gu_launch, nlaunch, wl.stream)
     achieved = gu_bytes / t_gu / 1e9
-    roof = {"kernel": "qgemv_fast<Q4,gate_up> (smoe_gate_up_q4, 1536x4096)", "bound": "hbm",
+    roof = {"kernel": "qgemv_tma<Q4,gate_up> (smoe_experts_gate_up_q4, 8 experts x 1536x4096)",
+            "bound": "hbm",
             "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "traffic": roofline_traffic("gate_up_q4"),
             "algorithmic_bytes_per_launch": gu_bytes, "us_per_launch": round(t_gu * 1e6, 3),
@@ -334,12 +358,17 @@ def gpu_arm(args, rank, world, local):
         "config": {"workload": WORKLOAD, "bytes_per_step": sb,
                    "l2": f"{len(wl.copies)} rotating weight copies ({len(wl.copies) * sb / 1e6:.0f} MB) "
                          f"> {L2_BYTES >> 20} MB L2",
-                   "launch": "16 C-ABI calls per step captured in a CUDA graph, programmatic "
-                             "dependent launch between kernels",
+                   "launch": "2 grouped C-ABI calls per step (smoe_experts_gate_up_q4 over the 8 "
+                             "experts, then smoe_experts_down_q4), captured in a CUDA graph, "
+                             "programmatic dependent launch between kernels",
                    "parallelism": f"replicas x{world} (experts are independent; no collective)"},
         "us_per_8expert_ffn": round(ms * 1e3, 3),
+        "per_expert_calls": {"GB/s": round(sb * args.steps * world / t_calls / 1e9, 2),
+                             "us_per_8expert_ffn": round(t_calls / args.steps * 1e6, 3),
+                             "launch": "16 single-expert calls (8 x smoe_gate_up_q4 + smoe_down_q4) per "
+                                       "step in a CUDA graph"},
         "hbm_frac": round(value / world / hbm_peak, 4),
-        "roofline": roof, "e2e": e2e, "gpu_launches": 2 * N_EXPERTS * args.steps,
+        "roofline": roof, "e2e": e2e, "gpu_launches": 2 * args.steps,
         "clocks": clock_rec,
     }
     return result, wl, smoe, dev
@@ -363,7 +392,7 @@ def rows_breakdown(smoe, dev, steps):
 
     # Q2 8-expert decode
     n_copies = max(2, -(-4 * L2_BYTES // step_bytes(2)))
-    q2 = DecodeWorkload(smoe, dev, 2, 6, n_copies)
+    q2 = DecodeWorkload(smoe, dev, 2, 6, n_copies, grouped=True)
     q2.capture()
     q2.run(5)
     t = time_steps(lambda k: q2.run(k), max(50, steps // 4), q2.stream)

@@ -48,7 +48,9 @@
  *   error itself stays readable with cudaGetLastError()).
  * Numerics.  Sums are reassociated (lanes, warps, groups), so results are not
  *   bit-identical to a sequential sum; they agree with an exact (f64) result
- *   within 1e-4 * sum_i |w_i x_i| + 1e-6 per output element.
+ *   within 1e-4 * sum_i |w_i x_i| + 1e-6 per output element.  Activations
+ *   must be finite: a NaN or infinity in x makes the outputs that read it
+ *   NaN.
  */
 #ifndef SMOE_H
 #define SMOE_H
@@ -120,6 +122,51 @@ int smoe_down_q4(const uint8_t *down_codes, const float *down_scales,
 int smoe_down_q2(const uint8_t *down_codes, const float *down_scales,
                  const float *hidden, float *out,
                  int d_model, int d_ff, int group, void *stream);
+
+/*
+ * Grouped expert dispatch ("Grouped Expert Dispatch"): the fused gate/up
+ * pass of n_experts experts for the same token in one launch,
+ *
+ *   hidden[e][i] = SiLU(gate_e . x)[i] * (up_e . x)[i],  e in [0, n_experts).
+ *
+ * gate_codes, gate_scales, up_codes, up_scales: HOST arrays of n_experts
+ * DEVICE pointers, expert e's tensors laid out as for smoe_gate_up_q4/q2
+ * (all experts share d_ff, d_model and group).  x: f32 [d_model], shared
+ * by all experts.  hidden: f32 [n_experts x d_ff] (expert-major), written.
+ * The pointer arrays are read during the call only; the parameters travel
+ * with the launch (up to 64 experts per launch), so nothing is allocated.
+ * n_experts >= 0.  Each row is computed exactly as the single-expert call
+ * computes it.
+ */
+int smoe_experts_gate_up_q4(int n_experts, const uint8_t *const *gate_codes,
+                            const float *const *gate_scales,
+                            const uint8_t *const *up_codes,
+                            const float *const *up_scales, const float *x,
+                            float *hidden, int d_ff, int d_model, int group,
+                            void *stream);
+int smoe_experts_gate_up_q2(int n_experts, const uint8_t *const *gate_codes,
+                            const float *const *gate_scales,
+                            const uint8_t *const *up_codes,
+                            const float *const *up_scales, const float *x,
+                            float *hidden, int d_ff, int d_model, int group,
+                            void *stream);
+
+/*
+ * Grouped down projection ("Grouped Expert Dispatch"):
+ *
+ *   out[e][j] = (down_e . hidden[e])[j],  e in [0, n_experts).
+ *
+ * down_codes, down_scales: HOST arrays of n_experts DEVICE pointers (as for
+ * smoe_down_q4/q2).  hidden: f32 [n_experts x d_ff]; out: f32
+ * [n_experts x d_model] (expert-major), written.  Per-expert outputs are
+ * kept separate: no router weighting or sum over experts is applied.
+ */
+int smoe_experts_down_q4(int n_experts, const uint8_t *const *down_codes,
+                         const float *const *down_scales, const float *hidden,
+                         float *out, int d_model, int d_ff, int group, void *stream);
+int smoe_experts_down_q2(int n_experts, const uint8_t *const *down_codes,
+                         const float *const *down_scales, const float *hidden,
+                         float *out, int d_model, int d_ff, int group, void *stream);
 
 /*
  * Dense bf16 matvec ("Coalesced Dense Matvec -- the Same Contract for bf16"):

@@ -48,6 +48,10 @@ _SIGS = {
     "smoe_down_q4": ([_P, _P, _P, _P, _I, _I, _I, _P], _I),
     "smoe_down_q2": ([_P, _P, _P, _P, _I, _I, _I, _P], _I),
     "matvec_bf16": ([_P, _P, _P, _I, _I, _P], _I),
+    "smoe_experts_gate_up_q4": ([_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P], _I),
+    "smoe_experts_gate_up_q2": ([_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P], _I),
+    "smoe_experts_down_q4": ([_I, _P, _P, _P, _P, _I, _I, _I, _P], _I),
+    "smoe_experts_down_q2": ([_I, _P, _P, _P, _P, _I, _I, _I, _P], _I),
     "smoe_ffn_batch_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "ffn_batch_q4": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "ffn_batch_q4_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
@@ -121,6 +125,55 @@ def smoe_down_q4(down_codes, down_scales, hidden, out, d_model, d_ff, group, str
 def smoe_down_q2(down_codes, down_scales, hidden, out, d_model, d_ff, group, stream=None):
     _check(_lib.smoe_down_q2(_ptr(down_codes), _ptr(down_scales), _ptr(hidden), _ptr(out), d_model,
                              d_ff, group, _stream(stream)), "smoe_down_q2")
+
+
+def _ptr_array(items):
+    """A host array of device pointers (ctypes), kept alive by the caller."""
+    arr = (ctypes.c_void_p * max(1, len(items)))()
+    for i, t in enumerate(items):
+        arr[i] = _ptr(t)
+    return arr
+
+
+def _experts_gate_up(fn, name, gate_codes, gate_scales, up_codes, up_scales, x, hidden, d_ff, d_model,
+                     group, stream):
+    n = len(gate_codes)
+    if not (len(gate_scales) == len(up_codes) == len(up_scales) == n):
+        raise ValueError(f"{name}: per-expert lists differ in length")
+    arrs = [_ptr_array(a) for a in (gate_codes, gate_scales, up_codes, up_scales)]
+    _check(fn(n, *arrs, _ptr(x), _ptr(hidden), d_ff, d_model, group, _stream(stream)), name)
+
+
+def smoe_experts_gate_up_q4(gate_codes, gate_scales, up_codes, up_scales, x, hidden, d_ff, d_model,
+                            group, stream=None):
+    """Per-expert lists of tensors; hidden is [n_experts, d_ff]."""
+    _experts_gate_up(_lib.smoe_experts_gate_up_q4, "smoe_experts_gate_up_q4", gate_codes, gate_scales,
+                     up_codes, up_scales, x, hidden, d_ff, d_model, group, stream)
+
+
+def smoe_experts_gate_up_q2(gate_codes, gate_scales, up_codes, up_scales, x, hidden, d_ff, d_model,
+                            group, stream=None):
+    _experts_gate_up(_lib.smoe_experts_gate_up_q2, "smoe_experts_gate_up_q2", gate_codes, gate_scales,
+                     up_codes, up_scales, x, hidden, d_ff, d_model, group, stream)
+
+
+def _experts_down(fn, name, down_codes, down_scales, hidden, out, d_model, d_ff, group, stream):
+    n = len(down_codes)
+    if len(down_scales) != n:
+        raise ValueError(f"{name}: per-expert lists differ in length")
+    arrs = [_ptr_array(a) for a in (down_codes, down_scales)]
+    _check(fn(n, *arrs, _ptr(hidden), _ptr(out), d_model, d_ff, group, _stream(stream)), name)
+
+
+def smoe_experts_down_q4(down_codes, down_scales, hidden, out, d_model, d_ff, group, stream=None):
+    """Per-expert lists of tensors; hidden [n_experts, d_ff], out [n_experts, d_model]."""
+    _experts_down(_lib.smoe_experts_down_q4, "smoe_experts_down_q4", down_codes, down_scales, hidden, out,
+                  d_model, d_ff, group, stream)
+
+
+def smoe_experts_down_q2(down_codes, down_scales, hidden, out, d_model, d_ff, group, stream=None):
+    _experts_down(_lib.smoe_experts_down_q2, "smoe_experts_down_q2", down_codes, down_scales, hidden, out,
+                  d_model, d_ff, group, stream)
 
 
 def matvec_bf16(w, x, y, rows, cols, stream=None):

@@ -135,9 +135,102 @@ int down_impl(int bits, const uint8_t *dc, const float *ds, const float *hidden,
                                         static_cast<cudaStream_t>(stream)));
 }
 
+constexpr int kExpertsPerLaunch = 64;
+
+// Grouped calls: per-expert checks, then launches of up to 64 experts each
+// (experts of one launch share the grid; a shape the grouped kernel does not
+// take is run expert by expert with the single-expert launcher).
+int experts_impl(int bits, int nmat, int n, const uint8_t *const *c0, const float *const *s0,
+                 const uint8_t *const *c1, const float *const *s1, const float *x, float *y, int units, int K,
+                 int group, void *stream)
+{
+    if (n < 0) return SMOE_ERR_SHAPE;
+    int st = check_q_shape(bits, units, K, group);
+    if (st != SMOE_OK) return st;
+    if (n == 0 || units == 0) return SMOE_OK;
+    if (!c0 || !s0 || (nmat == 2 && (!c1 || !s1))) return SMOE_ERR_NULL;
+    if (!y) return SMOE_ERR_NULL;
+    if (!aligned16(y)) return SMOE_ERR_ALIGN;
+    // x: one shared vector for gate/up, one row per expert for down
+    const size_t x_bytes = static_cast<size_t>(K) * sizeof(float) * (nmat == 2 ? 1 : static_cast<size_t>(n));
+    const Span out = {y, static_cast<size_t>(n) * static_cast<size_t>(units) * sizeof(float)};
+    if (K > 0) {
+        if (!x) return SMOE_ERR_NULL;
+        if (!aligned16(x)) return SMOE_ERR_ALIGN;
+        if (overlap(out, Span{x, x_bytes})) return SMOE_ERR_ALIAS;
+        for (int e = 0; e < n; ++e) {
+            const uint8_t *cs[2] = {c0[e], nmat == 2 ? c1[e] : c0[e]};
+            const float *ss[2] = {s0[e], nmat == 2 ? s1[e] : s0[e]};
+            for (int m = 0; m < nmat; ++m) {
+                if (!cs[m] || !ss[m]) return SMOE_ERR_NULL;
+                if (!aligned16(cs[m]) || !aligned16(ss[m])) return SMOE_ERR_ALIGN;
+                if (overlap(out, Span{cs[m], q_bytes(bits, units, K)}) ||
+                    overlap(out, Span{ss[m], scale_bytes(units, K, group)}))
+                    return SMOE_ERR_ALIAS;
+            }
+        }
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const float *xs[kExpertsPerLaunch];
+    float *ys[kExpertsPerLaunch];
+    for (int e0 = 0; e0 < n; e0 += kExpertsPerLaunch) {
+        const int cnt = (n - e0) < kExpertsPerLaunch ? (n - e0) : kExpertsPerLaunch;
+        for (int i = 0; i < cnt; ++i) {
+            xs[i] = nmat == 2 ? x : (x ? x + static_cast<size_t>(e0 + i) * K : nullptr);
+            ys[i] = y + static_cast<size_t>(e0 + i) * units;
+        }
+        bool unsupported = true;
+        cudaError_t err = cudaSuccess;
+        if (K > 0)
+            err = smoe::launch_qgemv_experts(bits, nmat, cnt, c0 + e0, nmat == 2 ? c1 + e0 : c0 + e0, s0 + e0,
+                                             nmat == 2 ? s1 + e0 : s0 + e0, xs, ys, units, K, group, s,
+                                             &unsupported);
+        if (err != cudaSuccess) return SMOE_ERR_LAUNCH;
+        if (unsupported) {
+            for (int i = 0; i < cnt; ++i) {
+                const uint8_t *codes[2] = {c0[e0 + i], nmat == 2 ? c1[e0 + i] : c0[e0 + i]};
+                const float *scales[2] = {s0[e0 + i], nmat == 2 ? s1[e0 + i] : s0[e0 + i]};
+                err = smoe::launch_qgemv(bits, nmat, codes, scales, xs[i], ys[i], units, K, group, s);
+                if (err != cudaSuccess) return SMOE_ERR_LAUNCH;
+            }
+        }
+    }
+    return SMOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+int smoe_experts_gate_up_q4(int n_experts, const uint8_t *const *gate_codes, const float *const *gate_scales,
+                            const uint8_t *const *up_codes, const float *const *up_scales, const float *x,
+                            float *hidden, int d_ff, int d_model, int group, void *stream)
+{
+    return experts_impl(4, 2, n_experts, gate_codes, gate_scales, up_codes, up_scales, x, hidden, d_ff,
+                        d_model, group, stream);
+}
+
+int smoe_experts_gate_up_q2(int n_experts, const uint8_t *const *gate_codes, const float *const *gate_scales,
+                            const uint8_t *const *up_codes, const float *const *up_scales, const float *x,
+                            float *hidden, int d_ff, int d_model, int group, void *stream)
+{
+    return experts_impl(2, 2, n_experts, gate_codes, gate_scales, up_codes, up_scales, x, hidden, d_ff,
+                        d_model, group, stream);
+}
+
+int smoe_experts_down_q4(int n_experts, const uint8_t *const *down_codes, const float *const *down_scales,
+                         const float *hidden, float *out, int d_model, int d_ff, int group, void *stream)
+{
+    return experts_impl(4, 1, n_experts, down_codes, down_scales, nullptr, nullptr, hidden, out, d_model,
+                        d_ff, group, stream);
+}
+
+int smoe_experts_down_q2(int n_experts, const uint8_t *const *down_codes, const float *const *down_scales,
+                         const float *hidden, float *out, int d_model, int d_ff, int group, void *stream)
+{
+    return experts_impl(2, 1, n_experts, down_codes, down_scales, nullptr, nullptr, hidden, out, d_model,
+                        d_ff, group, stream);
+}
 
 int smoe_abi_version(void) { return SMOE_ABI_VERSION; }
 

@@ -87,3 +87,86 @@ __device__ __forceinline__ float silu_f32(float v)
 }
 
 }  // namespace smoe
+
+namespace smoe {
+
+// ---- mbarrier and bulk-copy (TMA engine) helpers, CTA-local shared memory.
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Makes mbarrier initialisation visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's earlier generic-proxy shared-memory accesses before
+// later async-proxy (bulk copy) writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// One bulk copy global -> shared, completing `bytes` of transaction count on
+// the mbarrier.  dst, src 16-byte aligned; bytes a positive multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(bar)
+        : "memory");
+}
+
+// Tests phase `parity` of an mbarrier (the hardware may hold the thread for
+// a short, system-defined time while the phase is still incomplete).
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Named barrier over `nthreads` threads (a multiple of 32) of the block.
+__device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Waits for phase `parity` of an mbarrier, giving up after about two seconds
+// of SM clock (or 2^24 polls); on giving up it records `code` in *status
+// (if not null) and returns false instead of hanging.  Between polls the
+// thread sleeps briefly so that waiting warps leave the issue slots to the
+// warps that have work.  A parity test cannot tell a phase from the one two
+// before it, so the caller must know that the phase preceding the awaited
+// one has already completed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, unsigned *status,
+                                                  unsigned code)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 0; i < (1u << 24); ++i) {
+        __nanosleep(64);
+        if (mbar_try_wait(bar, parity)) return true;
+        if (clock64() - t0 > 4000000000LL) break;
+    }
+    if (status) atomicExch(status, code);
+    return false;
+}
+
+}  // namespace smoe

@@ -7,6 +7,8 @@
 // unpacks each 16-byte chunk of codes once and applies it to TT tokens whose
 // x rows are staged in shared memory.  One token goes through the decode
 // kernels instead (qgemv.cu).
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 #include "qformat.cuh"
@@ -231,6 +233,22 @@ cudaError_t launch_ffn_batch(const uint8_t *const gu_codes[2], const float *cons
         e = launch_qgemm_tokens(4, 2, gu_codes, gu_scales, X, H, T, d_ff, d_model, group, stream);
     if (e != cudaSuccess) return e;
     return launch_qgemm_tokens(4, 1, dc, ds, H, Y, T, d_model, d_ff, group, stream);
+}
+
+unsigned *device_status_word()
+{
+    constexpr int kMaxDevices = 64;
+    static unsigned *addr[kMaxDevices] = {};
+    static std::mutex mu;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        addr[dev] = static_cast<unsigned *>(p);
+    }
+    return addr[dev];
 }
 
 cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned *value)

@@ -24,6 +24,18 @@ cudaError_t launch_qgemv(int bits, int nmat, const uint8_t *const codes[2],
                          const float *const scales[2], const float *x, float *y,
                          int units, int K, int group, cudaStream_t stream);
 
+// Bulk-copy + integer-dot decode kernel over n_experts experts at once
+// (one grid slice per expert).  codes1/scales1 are used when nmat == 2.
+// x[e], y[e] are expert e's input and output.  Sets *unsupported (and
+// launches nothing) for shapes this kernel does not take.
+cudaError_t launch_qgemv_experts(int bits, int nmat, int n_experts, const uint8_t *const *codes0,
+                                 const uint8_t *const *codes1, const float *const *scales0,
+                                 const float *const *scales1, const float *const *x, float *const *y,
+                                 int units, int K, int group, cudaStream_t stream, bool *unsupported);
+
+// Device address of the library's device status word on the current device.
+unsigned *device_status_word();
+
 // Launches y = W x for a bf16 [rows x K] matrix.  Shapes already validated.
 cudaError_t launch_bf16_gemv(const uint16_t *w, const float *x, float *y, int rows, int K,
                              cudaStream_t stream);

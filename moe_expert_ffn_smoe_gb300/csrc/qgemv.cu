@@ -368,6 +368,15 @@ cudaError_t launch_qgemv(int bits, int nmat, const uint8_t *const codes[2],
     a.units = units;
     a.K = K;
     a.group = group;
+    // The bulk-copy kernel (qgemv_tma.cu) takes every shape whose rows are a
+    // multiple of 8 chunks and whose staging fits in shared memory; the
+    // kernels above serve the rest (narrow or ragged rows, K = 0).
+    bool unsupported = true;
+    const uint8_t *c1 = a.codes[1];
+    const float *s1 = a.scales[1];
+    cudaError_t e = launch_qgemv_experts(bits, nmat, 1, &a.codes[0], &c1, &a.scales[0], &s1, &a.x, &a.y, units,
+                                         K, group, stream, &unsupported);
+    if (!unsupported) return e;
     if (bits == 4) return nmat == 2 ? launch_q<4, 2>(a, stream) : launch_q<4, 1>(a, stream);
     return nmat == 2 ? launch_q<2, 2>(a, stream) : launch_q<2, 1>(a, stream);
 }

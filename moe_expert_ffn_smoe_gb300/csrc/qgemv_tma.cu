@@ -1,0 +1,519 @@
+// Decode GEMV, second design: bulk-copy staging + integer dot products.
+//
+// Computes the same operations as the S-MoE page "Metal Compute Kernels",
+// section "Fused FFN Kernels -- One Simdgroup Per Output Row":
+//     hidden[i] = SiLU(gate . x)[i] * (up . x)[i]      (NMAT = 2)
+//     out[j]    = (down . hidden)[j]                    (NMAT = 1)
+// with w = (code - Z) s / Z and the per-group fold s * (C / Z - Sx).
+// One launch covers one expert or several ("Grouped Expert Dispatch"): the
+// grid is split into equal slices of CTAs, one slice per expert.
+//
+// Memory (GB300 layout, not the page's Metal one):
+//  * A CTA owns a contiguous range of output rows of one expert and streams
+//    it as stages: R consecutive rows of every matrix (one contiguous range
+//    per matrix) plus their scales.  Every warp has its own ring of `ns`
+//    shared-memory slots which its lane 0 fills with cp.async.bulk copies
+//    completing on the slot's mbarrier.  Many threads per SM issue copies:
+//    one issuing thread per SM cannot keep HBM busy with copies of a few KB.
+//    A warp only ever waits on slots it has filled itself, so the parity of
+//    the awaited phase is unambiguous.
+//  * The first copies go out before the kernel waits on the previous one
+//    (weights are never produced by it), so weight bytes are in flight while
+//    x is staged.
+//  * x is staged once per CTA, converted to exact integer "digits" (below).
+//
+// Arithmetic (an exact integer rewrite of the inner dot):
+//  * Per group of `group` columns, x is scaled by a power of two so its
+//    largest magnitude lies in [2^21, 2^22) and rounded to an integer
+//    xq (|x - xq*q| <= q/2 with q = 2^(e-21), e = floor(log2 max|x|)).
+//  * xq is split into three balanced base-256 digits d0 + 256 d1 + 65536 d2,
+//    each a signed byte, so sum(code * xq) over a 16-byte chunk of codes is
+//    computed exactly by dp4a (four byte products + add per instruction);
+//    codes are separated into bytes with one or two logic ops per 32-bit
+//    word (Q4: even / odd nibbles; Q2: the four bit pairs).
+//  * Per chunk: C = A2*65536 + A1*256 + A0 (exact in int32), then
+//    acc1 += s*q*C and acc2 += s*(q*Sxq); the row result is acc1/Z - acc2,
+//    with Sxq the exact integer sum of xq over the chunk.
+// Error: only the rounding of x to xq (at most 2^-22 of the group's largest
+// |x| per element) and the f32 epilogue; far inside 1e-4 * sum|w x|.
+// Non-finite x makes the chunk's q NaN, so the affected outputs are NaN.
+#include "common.cuh"
+#include "internal.h"
+#include "qformat.cuh"
+
+namespace smoe {
+
+constexpr int QG_MAX_EXPERTS = 64;
+
+struct QGArgs {
+    const uint8_t *codes[2][QG_MAX_EXPERTS];
+    const float *scales[2][QG_MAX_EXPERTS];
+    const float *x[QG_MAX_EXPERTS];
+    float *y[QG_MAX_EXPERTS];
+    unsigned *status;      // device status word (bounded waits)
+    int ctas_per_expert;
+    int units;             // output rows per expert
+    int K;
+    int group;
+    int scales_tma;        // scales travel with the codes (ngroups % 4 == 0)
+    int ns;                // ring slots per warp
+    uint32_t stage_bytes;  // bytes of one slot
+    uint32_t off_info, off_gmax, off_bars, off_slots;  // shared-memory offsets
+};
+
+template <int BITS>
+struct DigitFmt;
+
+template <>
+struct DigitFmt<4> {
+    static constexpr int NCLASS = 2;     // byte classes per code word
+    static constexpr int XSTRIDE = 112;  // digit bytes per chunk (96 + 16 pad: conflict-free)
+    static constexpr int CODES_PER_CHUNK = 32;
+    static constexpr int WORD_COLS = 8;
+    static constexpr float ZINV = 1.0f / 7.5f;
+    // class 0: codes of the even columns, class 1: odd columns, one per byte
+    static __device__ __forceinline__ int cls(uint32_t w, int k)
+    {
+        return static_cast<int>((k == 0 ? w : (w >> 4)) & 0x0F0F0F0Fu);
+    }
+    // column (0..7 inside the word) whose digit goes to byte b of class k
+    static __device__ __forceinline__ int col(int k, int b) { return 2 * b + k; }
+};
+
+template <>
+struct DigitFmt<2> {
+    static constexpr int NCLASS = 4;
+    static constexpr int XSTRIDE = 208;  // 192 + 16 pad
+    static constexpr int CODES_PER_CHUNK = 64;
+    static constexpr int WORD_COLS = 16;
+    static constexpr float ZINV = 1.0f / 1.5f;
+    static __device__ __forceinline__ int cls(uint32_t w, int k)
+    {
+        return static_cast<int>((w >> (2 * k)) & 0x03030303u);
+    }
+    static __device__ __forceinline__ int col(int k, int b) { return 4 * b + k; }
+};
+
+__device__ __forceinline__ uint4 lds128u(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float4 lds128f(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// Balanced base-256 digits of v (|v| <= 2^22): v = d0 + 256 d1 + 65536 d2,
+// every digit in [-128, 127].
+__device__ __forceinline__ void digits3(int v, int &d0, int &d1, int &d2)
+{
+    d0 = static_cast<int>(static_cast<signed char>(v & 0xFF));
+    const int r = (v - d0) >> 8;
+    d1 = static_cast<int>(static_cast<signed char>(r & 0xFF));
+    d2 = (r - d1) >> 8;
+}
+
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
+{
+    return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
+           ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
+}
+
+// Stages x[0..K) as digits: chunk c occupies XSTRIDE bytes at c*XSTRIDE;
+// inside it, the uint4 at (3k + j)*16 holds digit j of byte class k for the
+// chunk's 4 code words (word v in component v).  info[c] = {q, q*Sxq, group
+// index, 0}.  Called by all threads of the block (blockDim.x % 32 == 0).
+template <int BITS>
+__device__ void stage_x_digits(const float *__restrict__ x, int K, int group, uint8_t *smem, uint32_t off_info,
+                               uint32_t off_gmax)
+{
+    using D = DigitFmt<BITS>;
+    const int nwords = K / D::WORD_COLS;
+    const int ngroups = K / group;
+    unsigned *gmax = reinterpret_cast<unsigned *>(smem + off_gmax);
+    float4 *info = reinterpret_cast<float4 *>(smem + off_info);
+    for (int g = threadIdx.x; g < ngroups; g += blockDim.x) gmax[g] = 0u;
+    __syncthreads();
+    for (int v = threadIdx.x; v < nwords; v += blockDim.x) {
+        const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < D::WORD_COLS / 4; ++i) {
+            const float4 f = p[i];
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+            if (!(isfinite(f.x) && isfinite(f.y) && isfinite(f.z) && isfinite(f.w))) m = __uint_as_float(0x7F800000u);
+        }
+        atomicMax(&gmax[(v * D::WORD_COLS) / group], __float_as_uint(m));
+    }
+    __syncthreads();
+    for (int base = 0; base < nwords; base += blockDim.x) {
+        const int v = base + threadIdx.x;
+        int S = 0;
+        float q = 1.f;
+        int g = 0;
+        if (v < nwords) {
+            g = (v * D::WORD_COLS) / group;
+            const unsigned mb = gmax[g];
+            int e = static_cast<int>(mb >> 23) - 127;
+            if (e < -105) e = -105;
+            const bool finite = mb < 0x7F800000u;
+            const float scale = finite ? __uint_as_float(static_cast<unsigned>(127 + 21 - e) << 23) : 0.f;
+            q = finite ? __uint_as_float(static_cast<unsigned>(127 + e - 21) << 23) : __uint_as_float(0x7FC00000u);
+            int xq[D::WORD_COLS];
+            const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
+#pragma unroll
+            for (int i = 0; i < D::WORD_COLS / 4; ++i) {
+                const float4 f = p[i];
+                xq[4 * i + 0] = __float2int_rn(f.x * scale);
+                xq[4 * i + 1] = __float2int_rn(f.y * scale);
+                xq[4 * i + 2] = __float2int_rn(f.z * scale);
+                xq[4 * i + 3] = __float2int_rn(f.w * scale);
+            }
+            if (!finite) {
+#pragma unroll
+                for (int i = 0; i < D::WORD_COLS; ++i) xq[i] = 0;
+            }
+            int d[3][D::WORD_COLS];
+#pragma unroll
+            for (int i = 0; i < D::WORD_COLS; ++i) {
+                digits3(xq[i], d[0][i], d[1][i], d[2][i]);
+                S += xq[i];
+            }
+            uint8_t *chunk = smem + static_cast<size_t>(v >> 2) * D::XSTRIDE + (v & 3) * 4;
+#pragma unroll
+            for (int k = 0; k < D::NCLASS; ++k)
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                    *reinterpret_cast<uint32_t *>(chunk + (3 * k + j) * 16) =
+                        pack4(d[j][D::col(k, 0)], d[j][D::col(k, 1)], d[j][D::col(k, 2)], d[j][D::col(k, 3)]);
+        }
+        S += __shfl_xor_sync(FULL_MASK, S, 1);
+        S += __shfl_xor_sync(FULL_MASK, S, 2);
+        if (v < nwords && (v & 3) == 0) info[v >> 2] = make_float4(q, static_cast<float>(S) * q, __int_as_float(g), 0.f);
+    }
+}
+
+// Every warp owns `ns` slots and streams its own stages through them: lane 0
+// issues the bulk copies of stage k into slot k % ns, the warp waits on the
+// slot's mbarrier, computes the stage's R rows (RPT per team of L lanes)
+// and, once all lanes are done with the slot, lane 0 refills it with stage
+// k + ns.
+template <int BITS, int NMAT, int L, int RPT>
+__global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGArgs a)
+{
+    using D = DigitFmt<BITS>;
+    constexpr int TEAMS = 32 / L;
+    constexpr int R = TEAMS * RPT;  // output rows per stage
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = ((raw + 127u) & ~127u) - raw;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int NW = blockDim.x >> 5;
+    const int e = blockIdx.x / a.ctas_per_expert;
+    const int bi = blockIdx.x - e * a.ctas_per_expert;
+    const int u0 = static_cast<int>(static_cast<long long>(a.units) * bi / a.ctas_per_expert);
+    const int u1 = static_cast<int>(static_cast<long long>(a.units) * (bi + 1) / a.ctas_per_expert);
+    const int nst = (u1 - u0 + R - 1) / R;
+    const int my = warp < nst ? (nst - warp + NW - 1) / NW : 0;  // stages of this warp
+    const int KC = a.K / D::CODES_PER_CHUNK;
+    const uint32_t row_bytes = static_cast<uint32_t>(KC) * 16u;
+    const int ngroups = a.K / a.group;
+    const int ns = a.ns;
+    const uint32_t bars = sbase + a.off_bars + static_cast<uint32_t>(warp * ns) * 8u;
+    const uint32_t slots = sbase + a.off_slots + static_cast<uint32_t>(warp * ns) * a.stage_bytes;
+    const uint32_t scales_off = static_cast<uint32_t>(NMAT * R) * row_bytes;
+
+    // lane 0: the bulk copies of this warp's k-th stage into slot k % ns
+    auto issue = [&](int k) {
+        const int us = u0 + (warp + k * NW) * R;
+        const int n = min(R, u1 - us);
+        const uint32_t slot = slots + static_cast<uint32_t>(k % ns) * a.stage_bytes;
+        const uint32_t bar = bars + static_cast<uint32_t>(k % ns) * 8u;
+        const uint32_t cb = static_cast<uint32_t>(n) * row_bytes;
+        const uint32_t sb = a.scales_tma ? static_cast<uint32_t>(n * ngroups) * 4u : 0u;
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(NMAT) * (cb + sb));
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m) {
+            bulk_g2s(slot + static_cast<uint32_t>(m * R) * row_bytes,
+                     a.codes[m][e] + static_cast<size_t>(us) * row_bytes, cb, bar);
+            if (sb)
+                bulk_g2s(slot + scales_off + static_cast<uint32_t>(m * R * ngroups) * 4u,
+                         a.scales[m][e] + static_cast<size_t>(us) * ngroups, sb, bar);
+        }
+    };
+
+    if (lane == 0) {
+        for (int i = 0; i < ns; ++i) mbar_init(bars + 8u * i, 1);
+        fence_mbar_init();
+        const int first = my < ns ? my : ns;
+        for (int k = 0; k < first; ++k) issue(k);
+    }
+    __syncwarp();
+
+    pdl_wait();
+    stage_x_digits<BITS>(a.x[e], a.K, a.group, smem, a.off_info, a.off_gmax);
+    __syncthreads();
+    if (threadIdx.x == 0) pdl_launch_dependents();
+
+    const int team = lane / L;
+    const int u = lane % L;
+    const uint32_t info0 = sbase + a.off_info;
+    int k = 0;
+    bool ok = true;
+    for (; k < my; ++k) {
+        ok = mbar_wait_bounded(bars + static_cast<uint32_t>(k % ns) * 8u, (k / ns) & 1, a.status, 1u);
+        ok = __all_sync(FULL_MASK, ok);
+        if (!ok) break;
+        const uint32_t slot = slots + static_cast<uint32_t>(k % ns) * a.stage_bytes;
+        const int us = u0 + (warp + k * NW) * R;
+        const int n = min(R, u1 - us);
+
+        float acc1[NMAT][RPT], acc2[NMAT][RPT];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) acc1[m][r] = acc2[m][r] = 0.f;
+
+        const uint32_t code0 = slot + static_cast<uint32_t>(team) * row_bytes + static_cast<uint32_t>(u) * 16u;
+#pragma unroll 2
+        for (int c = u; c < KC; c += L) {
+            const uint32_t coff = static_cast<uint32_t>(c - u) * 16u;
+            const float4 inf = lds128f(info0 + static_cast<uint32_t>(c) * 16u);
+            const int g = __float_as_int(inf.z);
+            const uint32_t xc = sbase + static_cast<uint32_t>(c) * D::XSTRIDE;
+            uint4 cw[NMAT][RPT];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                for (int r = 0; r < RPT; ++r)
+                    cw[m][r] = lds128u(code0 + static_cast<uint32_t>(m * R + r * TEAMS) * row_bytes + coff);
+            int A0[NMAT][RPT], A1[NMAT][RPT], A2[NMAT][RPT];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) A0[m][r] = A1[m][r] = A2[m][r] = 0;
+#pragma unroll
+            for (int cl = 0; cl < D::NCLASS; ++cl) {
+                const uint4 d0 = lds128u(xc + (3 * cl + 0) * 16);
+                const uint4 d1 = lds128u(xc + (3 * cl + 1) * 16);
+                const uint4 d2 = lds128u(xc + (3 * cl + 2) * 16);
+#pragma unroll
+                for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                    for (int r = 0; r < RPT; ++r)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int cb = D::cls(word_of(cw[m][r], v), cl);
+                            A0[m][r] = __dp4a(cb, static_cast<int>(word_of(d0, v)), A0[m][r]);
+                            A1[m][r] = __dp4a(cb, static_cast<int>(word_of(d1, v)), A1[m][r]);
+                            A2[m][r] = __dp4a(cb, static_cast<int>(word_of(d2, v)), A2[m][r]);
+                        }
+            }
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    const int ul = r * TEAMS + team;
+                    const float sc =
+                        a.scales_tma ? lds_f32(slot + scales_off + static_cast<uint32_t>((m * R + ul) * ngroups + g) * 4u)
+                                     : ldg_f32(a.scales[m][e] + static_cast<size_t>(min(us + ul, u1 - 1)) * ngroups + g);
+                    // |C| < 2^31: at most 32 codes x 15 x 2^22 (Q4), 64 x 3 x 2^22 (Q2)
+                    const int C = A2[m][r] * 65536 + A1[m][r] * 256 + A0[m][r];
+                    acc1[m][r] = fmaf(sc * inf.x, static_cast<float>(C), acc1[m][r]);
+                    acc2[m][r] = fmaf(sc, inf.y, acc2[m][r]);
+                }
+        }
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+#pragma unroll
+                for (int off = L / 2; off > 0; off >>= 1) {
+                    acc1[m][r] += __shfl_xor_sync(FULL_MASK, acc1[m][r], off);
+                    acc2[m][r] += __shfl_xor_sync(FULL_MASK, acc2[m][r], off);
+                }
+        __syncwarp();
+        if (lane == 0 && k + ns < my) {
+            fence_proxy_async_smem();
+            issue(k + ns);
+        }
+        if (u == 0) {
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const int ul = r * TEAMS + team;
+                if (ul < n) {
+                    const float y0 = acc1[0][r] * D::ZINV - acc2[0][r];
+                    float out = y0;
+                    if (NMAT == 2) out = silu_f32(y0) * (acc1[NMAT - 1][r] * D::ZINV - acc2[NMAT - 1][r]);
+                    a.y[e][us + ul] = out;
+                }
+            }
+        }
+    }
+    if (!ok && lane == 0) {
+        // A copy never completed: wait (bounded) for the ones still in
+        // flight before the CTA's shared memory is released.
+        const int last = (k + ns < my) ? k + ns : my;
+        for (int kk = k; kk < last; ++kk)
+            mbar_wait_bounded(bars + static_cast<uint32_t>(kk % ns) * 8u, (kk / ns) & 1, nullptr, 0u);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+namespace {
+
+template <int BITS, int NMAT>
+using QGKernel = void (*)(QGArgs);
+
+template <int BITS, int NMAT>
+QGKernel<BITS, NMAT> pick_kernel(int L, int rpt)
+{
+    if (rpt == 2) {
+        if (L == 32) return qgemv_tma<BITS, NMAT, 32, 2>;
+        if (L == 16) return qgemv_tma<BITS, NMAT, 16, 2>;
+        if (L == 8) return qgemv_tma<BITS, NMAT, 8, 2>;
+    } else {
+        if (L == 32) return qgemv_tma<BITS, NMAT, 32, 1>;
+        if (L == 16) return qgemv_tma<BITS, NMAT, 16, 1>;
+        if (L == 8) return qgemv_tma<BITS, NMAT, 8, 1>;
+    }
+    return nullptr;
+}
+
+uint32_t round16(uint32_t v) { return (v + 15u) & ~15u; }
+
+constexpr size_t kSmemBudget = 200 * 1024;
+
+struct TmaConfig {
+    int nw, ns, rpt;
+};
+
+// Ring shape for a row range of `max_units` rows: the largest bytes in
+// flight that fit the shared-memory budget, preferring 16 warps.
+template <int BITS, int NMAT>
+bool pick_config(const QGArgs &a, int teams, int max_units, int max_smem, TmaConfig *out, uint32_t *stage_bytes,
+                 uint32_t *off_slots, size_t *smem_out)
+{
+    using D = DigitFmt<BITS>;
+    const int KC = a.K / D::CODES_PER_CHUNK;
+    const int ngroups = a.K / a.group;
+    const uint32_t row_bytes = static_cast<uint32_t>(KC) * 16u;
+    const size_t budget = kSmemBudget < static_cast<size_t>(max_smem) ? kSmemBudget : static_cast<size_t>(max_smem);
+    size_t best_flight = 0;
+    bool found = false;
+    for (int rpt = 1; rpt <= 2; ++rpt) {
+        const int R = teams * rpt;
+        const int max_stages = (max_units + R - 1) / R;
+        const uint32_t sbytes = round16(static_cast<uint32_t>(NMAT * R) * row_bytes +
+                                        (a.scales_tma ? static_cast<uint32_t>(NMAT * R * ngroups) * 4u : 0u));
+        for (int nw = 16; nw >= 8; nw -= 4) {
+            const int per_warp = (max_stages + nw - 1) / nw;
+            for (int ns = 4; ns >= 1; --ns) {
+                if (ns > per_warp && ns > 1) continue;
+                const uint32_t offs = a.off_bars + round16(static_cast<uint32_t>(nw * ns) * 8u);
+                const size_t smem = 128 + static_cast<size_t>(offs) + static_cast<size_t>(nw) * ns * sbytes;
+                if (smem > budget) continue;
+                // bytes in flight: all of a warp's stages when its ring holds
+                // them, else the slots not being computed on
+                const size_t flight = per_warp <= ns ? static_cast<size_t>(nw) * per_warp * sbytes
+                                                     : static_cast<size_t>(nw) * (ns - 1) * sbytes;
+                if (!found || flight > best_flight) {
+                    best_flight = flight;
+                    *out = TmaConfig{nw, ns, rpt};
+                    *stage_bytes = sbytes;
+                    *off_slots = offs;
+                    *smem_out = smem;
+                    found = true;
+                }
+                break;  // larger ns for this (rpt, nw) already tried first
+            }
+        }
+    }
+    return found;
+}
+
+template <int BITS, int NMAT>
+cudaError_t launch_tma(QGArgs &a, int n_experts, cudaStream_t stream, bool *unsupported)
+{
+    using D = DigitFmt<BITS>;
+    *unsupported = false;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return cudaErrorInvalidDevice;
+    const int KC = a.K / D::CODES_PER_CHUNK;
+    int L = 0;
+    if (KC > 0 && KC % 32 == 0) L = 32;
+    else if (KC > 0 && KC % 16 == 0) L = 16;
+    else if (KC > 0 && KC % 8 == 0) L = 8;
+    if (L == 0 || n_experts < 1 || n_experts > QG_MAX_EXPERTS) {
+        *unsupported = true;
+        return cudaSuccess;
+    }
+    const int ngroups = a.K / a.group;
+    a.scales_tma = (ngroups % 4 == 0) ? 1 : 0;
+    int cpe = dev->sm_count / n_experts;
+    if (cpe < 1) cpe = 1;
+    a.ctas_per_expert = cpe;
+    const int max_units = (a.units + cpe - 1) / cpe;
+    a.off_info = static_cast<uint32_t>(KC) * D::XSTRIDE;
+    a.off_gmax = a.off_info + static_cast<uint32_t>(KC) * 16u;
+    a.off_bars = a.off_gmax + round16(static_cast<uint32_t>(ngroups) * 4u);
+    TmaConfig cfg;
+    size_t smem = 0;
+    if (!pick_config<BITS, NMAT>(a, 32 / L, max_units, dev->max_smem_optin, &cfg, &a.stage_bytes, &a.off_slots,
+                                 &smem)) {
+        *unsupported = true;
+        return cudaSuccess;
+    }
+    a.ns = cfg.ns;
+    QGKernel<BITS, NMAT> k = pick_kernel<BITS, NMAT>(L, cfg.rpt);
+    cudaError_t err = ensure_dynamic_smem(k, smem);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(k, dim3(static_cast<unsigned>(cpe * n_experts)), dim3(cfg.nw * 32), smem, stream, a);
+}
+
+}  // namespace
+
+cudaError_t launch_qgemv_experts(int bits, int nmat, int n_experts, const uint8_t *const *codes0,
+                                 const uint8_t *const *codes1, const float *const *scales0,
+                                 const float *const *scales1, const float *const *x, float *const *y,
+                                 int units, int K, int group, cudaStream_t stream, bool *unsupported)
+{
+    QGArgs a = {};
+    for (int i = 0; i < n_experts && i < QG_MAX_EXPERTS; ++i) {
+        a.codes[0][i] = codes0[i];
+        a.codes[1][i] = nmat == 2 ? codes1[i] : codes0[i];
+        a.scales[0][i] = scales0[i];
+        a.scales[1][i] = nmat == 2 ? scales1[i] : scales0[i];
+        a.x[i] = x[i];
+        a.y[i] = y[i];
+    }
+    a.status = device_status_word();
+    a.units = units;
+    a.K = K;
+    a.group = group;
+    if (bits == 4)
+        return nmat == 2 ? launch_tma<4, 2>(a, n_experts, stream, unsupported)
+                         : launch_tma<4, 1>(a, n_experts, stream, unsupported);
+    return nmat == 2 ? launch_tma<2, 2>(a, n_experts, stream, unsupported)
+                     : launch_tma<2, 1>(a, n_experts, stream, unsupported);
+}
+
+}  // namespace smoe

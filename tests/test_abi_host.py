@@ -134,3 +134,21 @@ def test_binding_raises_with_status(smoe):
     with pytest.raises(smoe.SmoeError) as ei:
         smoe.smoe_gate_up_q4(A, A, A, A, A, A, 256, 100, 64, stream=0)
     assert ei.value.status == smoe.SMOE_ERR_SHAPE
+
+
+def test_grouped_refusals(smoe):
+    L = smoe._lib
+    P = lambda vals: (ctypes.c_void_p * len(vals))(*vals)
+    g = P([A, A + 0x100000])
+    gs = P([A + 0x200000, A + 0x300000])
+    x, h = A + 0x400000, A + 0x500000
+    assert L.smoe_experts_gate_up_q4(-1, g, gs, g, gs, x, h, 256, 256, 64, None) == smoe.SMOE_ERR_SHAPE
+    assert L.smoe_experts_gate_up_q4(2, g, gs, g, gs, x, h, 256, 100, 64, None) == smoe.SMOE_ERR_SHAPE
+    assert L.smoe_experts_gate_up_q4(2, None, gs, g, gs, x, h, 256, 256, 64, None) == smoe.SMOE_ERR_NULL
+    assert L.smoe_experts_gate_up_q4(2, P([A, 0]), gs, g, gs, x, h, 256, 256, 64, None) == smoe.SMOE_ERR_NULL
+    assert L.smoe_experts_gate_up_q4(2, P([A, A + 8]), gs, g, gs, x, h, 256, 256, 64, None) == smoe.SMOE_ERR_ALIGN
+    assert L.smoe_experts_gate_up_q4(2, g, gs, g, gs, x, x + 256, 256, 256, 64, None) == smoe.SMOE_ERR_ALIAS
+    assert L.smoe_experts_gate_up_q4(2, g, gs, g, gs, x, A + 0x100000 + 1024, 256, 256, 64, None) == \
+        smoe.SMOE_ERR_ALIAS
+    assert L.smoe_experts_down_q2(2, g, gs, x, A + 0x200000, 256, 256, 64, None) == smoe.SMOE_ERR_ALIAS
+    assert L.smoe_experts_down_q4(0, None, None, None, None, 256, 256, 64, None) == smoe.SMOE_OK

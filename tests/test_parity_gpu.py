@@ -371,3 +371,74 @@ def test_graph_capture_of_8_expert_sequence_matches_eager(smoe, dev):
     g.replay()
     torch.cuda.synchronize()
     assert torch.equal(out, eager)
+
+
+# ------------------------------------------------------ grouped expert calls
+
+def _grouped(smoe, bits):
+    return ((smoe.smoe_experts_gate_up_q4, smoe.smoe_experts_down_q4) if bits == 4 else
+            (smoe.smoe_experts_gate_up_q2, smoe.smoe_experts_down_q2))
+
+
+def _run_grouped(smoe, dev, bits, experts, x, d_model, d_ff, group):
+    gu, dn = _grouped(smoe, bits)
+    tens = [{k: to_dev(v, dev) for k, v in ex.items()} for ex in experts]
+    n = len(experts)
+    hidden = torch.full((n, d_ff), float("nan"), device=dev)
+    out = torch.full((n, d_model), float("nan"), device=dev)
+    gu([t["gate_codes"] for t in tens], [t["gate_scales"] for t in tens], [t["up_codes"] for t in tens],
+       [t["up_scales"] for t in tens], to_dev(x, dev), hidden, d_ff, d_model, group)
+    dn([t["down_codes"] for t in tens], [t["down_scales"] for t in tens], hidden, out, d_model, d_ff, group)
+    torch.cuda.synchronize()
+    return hidden, out, tens
+
+
+@pytest.mark.parametrize("bits,seed", [(4, 5), (2, 6)])
+def test_grouped_8_expert_decode(smoe, dev, bits, seed):
+    """One launch for the gate/up of all 8 experts, one for their downs."""
+    d_model, d_ff, group = 4096, 1536, 64
+    experts = [inp.expert(bits, d_model, d_ff, group, seed, e) for e in range(8)]
+    x = inp.activations(d_model, seed)
+    hidden, out, tens = _run_grouped(smoe, dev, bits, experts, x, d_model, d_ff, group)
+    h, o = hidden.cpu().numpy(), out.cpu().numpy()
+    for i, ex in enumerate(experts):
+        _check_expert(bits, ex, x, h[i], o[i], d_model, d_ff, group, f"grouped Q{bits} expert {i}")
+    # the grouped launch computes every row exactly as the single-expert call does
+    gate_up, down = _fns(smoe, bits)
+    h1 = torch.empty(d_ff, device=dev)
+    o1 = torch.empty(d_model, device=dev)
+    xd = to_dev(x, dev)
+    for i in (0, 7):
+        t = tens[i]
+        gate_up(t["gate_codes"], t["gate_scales"], t["up_codes"], t["up_scales"], xd, h1, d_ff, d_model, group)
+        down(t["down_codes"], t["down_scales"], hidden[i], o1, d_model, d_ff, group)
+        torch.cuda.synchronize()
+        assert torch.equal(h1, hidden[i]) and torch.equal(o1, out[i])
+
+
+@pytest.mark.parametrize("bits,n,d_model,d_ff,group", [(4, 3, 256, 512, 64), (2, 5, 512, 256, 64),
+                                                      (4, 70, 256, 64, 64), (4, 2, 160, 96, 32)])
+def test_grouped_ragged(smoe, dev, bits, n, d_model, d_ff, group):
+    experts = [inp.expert(bits, d_model, d_ff, group, 60 + n, e) for e in range(n)]
+    x = inp.activations(d_model, 60 + n)
+    hidden, out, _ = _run_grouped(smoe, dev, bits, experts, x, d_model, d_ff, group)
+    h, o = hidden.cpu().numpy(), out.cpu().numpy()
+    for i in sorted(set([0, n // 2, n - 1])):
+        _check_expert(bits, experts[i], x, h[i], o[i], d_model, d_ff, group, f"grouped n={n} expert {i}")
+
+
+def test_grouped_zero_experts_is_a_no_op(smoe, dev):
+    smoe.smoe_experts_gate_up_q4([], [], [], [], None, None, 1536, 4096, 64)
+    smoe.smoe_experts_down_q2([], [], None, None, 4096, 1536, 64)
+
+
+def test_nan_input_gives_nan_rows(smoe, dev):
+    rows, cols, group = 64, 4096, 64
+    codes = inp.packed_codes(rows, cols, 4, 43, 1)
+    sc = inp.scales(rows, cols // group, 43, 2)
+    x = inp.activations(cols, 43)
+    x[100] = np.nan
+    y = torch.zeros(rows, device=dev)
+    smoe.smoe_down_q4(to_dev(codes, dev), to_dev(sc, dev), to_dev(x, dev), y, rows, cols, group)
+    torch.cuda.synchronize()
+    assert np.isnan(y.cpu().numpy()).all()
