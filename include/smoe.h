@@ -228,8 +228,10 @@ int ffn_batch_q4(const uint8_t *gate_codes, const float *gate_scales,
  * inside the library, which every GPU that loads the library holds until
  * the process exits.  Calls whose workspace need,
  * smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group), exceeds that size
- * are refused with SMOE_ERR_SHAPE before anything is launched (4 MiB holds
- * T * d_ff <= 1,048,576 hidden values, e.g. T = 682 at d_ff = 1536).
+ * are refused with SMOE_ERR_SHAPE before anything is launched (at
+ * d_model = 4096, d_ff = 1536 every T up to 64 fits; the workspace holds the
+ * hidden activations and, for T >= 2, the split token operands of the
+ * tensor-core path).
  * The function calls no cudaMalloc, cudaFree or other allocating routine.
  *
  * The first call on a device looks up the array's device address with

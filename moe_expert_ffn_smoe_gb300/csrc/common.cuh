@@ -142,6 +142,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return done != 0;
 }
 
+// Arrives once on an mbarrier (release, CTA scope).
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Named barrier over `nthreads` threads (a multiple of 32) of the block.
 __device__ __forceinline__ void named_barrier(uint32_t id, uint32_t nthreads)
 {

@@ -3,10 +3,12 @@
 // every row of X [T x d_model], gate/up+SiLU into H [T x d_ff] (the caller's
 // workspace), then down into Y [T x d_model].
 //
-// This file holds the CUDA-core path: a multi-token GEMV in which a warp
-// unpacks each 16-byte chunk of codes once and applies it to TT tokens whose
-// x rows are staged in shared memory.  One token goes through the decode
-// kernels instead (qgemv.cu).
+// Paths: one token goes through the decode kernels (qgemv.cu); two or more
+// tokens go to the tensor cores (ffn_batch_tc.cu) when the group size and
+// both dimensions are multiples of 64; other shapes use the CUDA-core
+// multi-token GEMV below, in which a warp unpacks each 16-byte chunk of
+// codes once and applies it to TT tokens whose x rows are staged in shared
+// memory.
 #include <mutex>
 
 #include "common.cuh"
@@ -208,9 +210,8 @@ cudaError_t launch_qgemm_tokens(int bits, int nmat, const uint8_t *const codes[2
 
 size_t ffn_batch_workspace(int T, int d_model, int d_ff, int group)
 {
-    (void)d_model;
-    (void)group;
     if (T <= 0) return 0;
+    if (T > 1 && tc_batch_supported(T, d_model, d_ff, group)) return tc_batch_workspace(T, d_model, d_ff);
     const size_t hidden = static_cast<size_t>(T) * static_cast<size_t>(d_ff) * sizeof(float);
     return (hidden + 255) & ~static_cast<size_t>(255);
 }
@@ -229,6 +230,9 @@ cudaError_t launch_ffn_batch(const uint8_t *const gu_codes[2], const float *cons
         if (e != cudaSuccess) return e;
         return launch_qgemv(4, 1, dc, ds, H, Y, d_model, d_ff, group, stream);
     }
+    if (tc_batch_supported(T, d_model, d_ff, group))
+        return launch_ffn_batch_tc(gu_codes, gu_scales, down_codes, down_scales, X, Y, T, d_model, d_ff, group,
+                                   workspace, stream);
     if (d_ff > 0)
         e = launch_qgemm_tokens(4, 2, gu_codes, gu_scales, X, H, T, d_ff, d_model, group, stream);
     if (e != cudaSuccess) return e;

@@ -46,6 +46,15 @@ cudaError_t launch_qgemm_tokens(int bits, int nmat, const uint8_t *const codes[2
                                 const float *const scales[2], const float *X, float *Y,
                                 int T, int units, int K, int group, cudaStream_t stream);
 
+// Tensor-core batch path (ffn_batch_tc.cu): shapes it takes, its workspace,
+// and the launch of its four kernels (operand preparation and GEMM for
+// gate/up, then for down).
+bool tc_batch_supported(int T, int d_model, int d_ff, int group);
+size_t tc_batch_workspace(int T, int d_model, int d_ff);
+cudaError_t launch_ffn_batch_tc(const uint8_t *const gu_codes[2], const float *const gu_scales[2],
+                                const uint8_t *down_codes, const float *down_scales, const float *X, float *Y,
+                                int T, int d_model, int d_ff, int group, void *workspace, cudaStream_t stream);
+
 // Bytes of workspace the batch FFN needs (0 for T <= 0).
 size_t ffn_batch_workspace(int T, int d_model, int d_ff, int group);
 
