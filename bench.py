@@ -17,7 +17,7 @@ rows of the hot path (Q2 decode, bf16 matvec shapes, token batch, the small
 256/256 expert) each timed the same way.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--no-rows] [--no-cpu]
+                  [--no-rows] [--no-cpu] [--rows PATTERN]
 """
 import argparse
 import hashlib
@@ -376,9 +376,10 @@ def gpu_arm(args, rank, world, local):
 
 # ------------------------------------------------------------ other rows
 
-def rows_breakdown(smoe, dev, steps):
+def rows_breakdown(smoe, dev, steps, pattern=""):
     """Each remaining row of the hot path, timed with events on its own stream
-    over `steps` launches with rotating inputs larger than L2."""
+    over `steps` launches with rotating inputs larger than L2.  `pattern`
+    keeps only the rows whose name contains it."""
     import torch
     hbm_peak, _ = peaks()
     out = {}
@@ -390,61 +391,81 @@ def rows_breakdown(smoe, dev, steps):
                 launch(i)
             return time_steps(lambda k: [launch(i) for i in range(k)], n, s)
 
-    # Q2 8-expert decode
+    if pattern in "q2_8expert_decode":
+        q2_row(smoe, dev, steps, out, hbm_peak)
+    for (rows, cols), seed in zip(inp.CONFIGS["bf16_matvec"]["shapes"], inp.CONFIGS["bf16_matvec"]["seeds"]):
+        if pattern in f"bf16_{rows}x{cols}":
+            bf16_row(smoe, dev, steps, out, hbm_peak, timed, s, rows, cols, seed)
+    for T in inp.CONFIGS["q4_token_batch"]["tokens"]:
+        if pattern in f"q4_token_batch_T{T}":
+            batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T)
+    if pattern in "q4_ffn_256":
+        small_row(smoe, dev, steps, out, timed, s)
+    return out
+
+
+def q2_row(smoe, dev, steps, out, hbm_peak):
+    """Q2 8-expert decode with the grouped calls, timed like the headline step."""
+    import torch
     n_copies = max(2, -(-4 * L2_BYTES // step_bytes(2)))
     q2 = DecodeWorkload(smoe, dev, 2, 6, n_copies, grouped=True)
     q2.capture()
     q2.run(5)
-    t = time_steps(lambda k: q2.run(k), max(50, steps // 4), q2.stream)
     n = max(50, steps // 4)
+    t = time_steps(lambda k: q2.run(k), n, q2.stream)
     sb = step_bytes(2)
     out["q2_8expert_decode"] = {"GB/s": round(sb * n / t / 1e9, 1), "us_per_step": round(t / n * 1e6, 3),
                                 "frac": round(sb * n / t / 1e9 / hbm_peak, 4), "bytes_per_step": sb}
     del q2
     torch.cuda.empty_cache()
 
-    # bf16 matvec, four shapes
-    for (rows, cols), seed in zip(inp.CONFIGS["bf16_matvec"]["shapes"], inp.CONFIGS["bf16_matvec"]["seeds"]):
-        wbytes = rows * cols * 2
-        ncp = max(1, min(8, -(-2 * L2_BYTES // wbytes)))
-        ws = [torch.from_numpy(inp.bf16_rows(rows, cols, seed, 1 + c).view(np.int16)).to(dev)
-              for c in range(ncp)]
-        x = torch.from_numpy(inp.activations(cols, seed)).to(dev)
-        y = torch.empty(rows, device=dev)
-        nl = max(20, min(steps // 4, int(2e9 // wbytes)))
-        t = timed(lambda i: smoe.matvec_bf16(ws[i % ncp], x, y, rows, cols, stream=s), nl)
-        b = wbytes + cols * 4 + rows * 4
-        out[f"bf16_{rows}x{cols}"] = {"GB/s": round(b * nl / t / 1e9, 1), "us_per_call": round(t / nl * 1e6, 3),
-                                      "frac": round(b * nl / t / 1e9 / hbm_peak, 4), "bytes_per_call": b}
-        del ws
-        torch.cuda.empty_cache()
 
-    # token batch, one Q4 expert
+def bf16_row(smoe, dev, steps, out, hbm_peak, timed, s, rows, cols, seed):
+    """One dense bf16 matvec shape."""
+    import torch
+    wbytes = rows * cols * 2
+    ncp = max(1, min(8, -(-2 * L2_BYTES // wbytes)))
+    ws = [torch.from_numpy(inp.bf16_rows(rows, cols, seed, 1 + c).view(np.int16)).to(dev) for c in range(ncp)]
+    x = torch.from_numpy(inp.activations(cols, seed)).to(dev)
+    y = torch.empty(rows, device=dev)
+    nl = max(20, min(steps // 4, int(2e9 // wbytes)))
+    t = timed(lambda i: smoe.matvec_bf16(ws[i % ncp], x, y, rows, cols, stream=s), nl)
+    b = wbytes + cols * 4 + rows * 4
+    out[f"bf16_{rows}x{cols}"] = {"GB/s": round(b * nl / t / 1e9, 1), "us_per_call": round(t / nl * 1e6, 3),
+                                  "frac": round(b * nl / t / 1e9 / hbm_peak, 4), "bytes_per_call": b}
+    del ws
+    torch.cuda.empty_cache()
+
+
+def batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T):
+    """Token-batch FFN of one Q4 expert for T tokens (16 rotating experts)."""
+    import torch
     ncp = 16
     experts = [{k: torch.from_numpy(v).to(dev) for k, v in inp.expert(4, D_MODEL, D_FF, GROUP, 7 + 1000 * c).items()}
                for c in range(ncp)]
-    for T in inp.CONFIGS["q4_token_batch"]["tokens"]:
-        X = torch.from_numpy(inp.activations((T, D_MODEL), 7)).to(dev)
-        Y = torch.empty((T, D_MODEL), device=dev)
-        need = smoe.smoe_ffn_batch_workspace_bytes(T, D_MODEL, D_FF, GROUP)
-        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    X = torch.from_numpy(inp.activations((T, D_MODEL), 7)).to(dev)
+    Y = torch.empty((T, D_MODEL), device=dev)
+    need = smoe.smoe_ffn_batch_workspace_bytes(T, D_MODEL, D_FF, GROUP)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
 
-        def launch(i, T=T, X=X, Y=Y, ws=ws, need=need):
-            e = experts[i % ncp]
-            smoe.ffn_batch_q4(e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"],
-                              e["down_codes"], e["down_scales"], X, Y, T, D_MODEL, D_FF, GROUP, ws,
-                              need, stream=s)
-        nl = max(20, min(steps // 8, 400))
-        t = timed(launch, nl)
-        b = expert_bytes(4) + 2 * T * D_MODEL * 4
-        flops = 2 * T * 3 * D_FF * D_MODEL
-        out[f"q4_token_batch_T{T}"] = {"GB/s": round(b * nl / t / 1e9, 1), "us_per_call": round(t / nl * 1e6, 3),
-                                       "frac": round(b * nl / t / 1e9 / hbm_peak, 4),
-                                       "TFLOP/s": round(flops * nl / t / 1e12, 2), "bytes_per_call": b}
+    def launch(i):
+        e = experts[i % ncp]
+        smoe.ffn_batch_q4(e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"], e["down_codes"],
+                          e["down_scales"], X, Y, T, D_MODEL, D_FF, GROUP, ws, need, stream=s)
+    nl = max(20, min(steps // 8, 400))
+    t = timed(launch, nl)
+    b = expert_bytes(4) + 2 * T * D_MODEL * 4
+    flops = 2 * T * 3 * D_FF * D_MODEL
+    out[f"q4_token_batch_T{T}"] = {"GB/s": round(b * nl / t / 1e9, 1), "us_per_call": round(t / nl * 1e6, 3),
+                                   "frac": round(b * nl / t / 1e9 / hbm_peak, 4),
+                                   "TFLOP/s": round(flops * nl / t / 1e12, 2), "bytes_per_call": b}
     del experts
     torch.cuda.empty_cache()
 
-    # the small 256/256 expert (latency bound)
+
+def small_row(smoe, dev, steps, out, timed, s):
+    """The small 256/256 expert (latency bound)."""
+    import torch
     small = [{k: torch.from_numpy(v).to(dev) for k, v in inp.expert(4, 256, 256, 64, c).items()} for c in range(4)]
     xs = torch.from_numpy(inp.activations(256, 0)).to(dev)
     hs = torch.empty(256, device=dev)
@@ -458,7 +479,6 @@ def rows_breakdown(smoe, dev, steps):
     nl = max(50, min(steps // 4, 2000))
     t = timed(small_launch, nl)
     out["q4_ffn_256"] = {"us_per_ffn": round(t / nl * 1e6, 3), "bytes_per_ffn": expert_bytes(4, 256, 256, 64)}
-    return out
 
 
 # ------------------------------------------------------------ the CPU arm
@@ -551,6 +571,7 @@ def main():
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row breakdown")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--rows", default="", help="run only the breakdown rows whose name contains this")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -570,7 +591,7 @@ def main():
                                "sample": desc}
     if rank == 0 and world == 1 and not args.no_rows:
         del wl
-        res["rows"] = rows_breakdown(smoe, dev, args.steps)
+        res["rows"] = rows_breakdown(smoe, dev, args.steps, args.rows)
     if rank == 0:
         print(json.dumps(res), flush=True)
     if world > 1:
