@@ -3,7 +3,8 @@
 Each translation unit is compiled in its own nvcc process (in parallel),
 then linked into one shared library with the CUDA runtime linked
 statically, so loading the library needs no GPU and no libcudart.
-Set SMOE_PTXAS_VERBOSE=1 to print register and shared-memory use.
+Set SMOE_PTXAS_VERBOSE=1 to print register and shared-memory use, and
+SMOE_NVCC_EXTRA to pass extra nvcc flags (e.g. -D tuning macros).
 """
 import concurrent.futures as cf
 import glob
@@ -50,6 +51,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
                     "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
     if os.environ.get("SMOE_PTXAS_VERBOSE") == "1":
         flags += ["-Xptxas", "-v"]
+    flags += os.environ.get("SMOE_NVCC_EXTRA", "").split()  # extra compile flags (tuning builds)
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src) + ".o")

@@ -87,10 +87,17 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 // Opts a kernel into more than 48 KB of dynamic shared memory when needed.
+// The limit is only ever raised: one kernel serves launches of different
+// shared-memory sizes, and a launch captured earlier into a graph must stay
+// valid after a later, smaller launch of the same kernel.
 template <typename K>
 cudaError_t ensure_dynamic_smem(K kernel, size_t bytes)
 {
     if (bytes <= 48 * 1024) return cudaSuccess;
+    cudaFuncAttributes fa;
+    cudaError_t err = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(kernel));
+    if (err != cudaSuccess) return err;
+    if (static_cast<size_t>(fa.maxDynamicSharedSizeBytes) >= bytes) return cudaSuccess;
     return cudaFuncSetAttribute(reinterpret_cast<const void *>(kernel),
                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 static_cast<int>(bytes));

@@ -1,0 +1,252 @@
+// Decode GEMV with the token's digits held in registers.
+//
+// Same operations and the same exact integer arithmetic as qgemv_tma.cu
+// (S-MoE page "Metal Compute Kernels", section "Fused FFN Kernels -- One
+// Simdgroup Per Output Row"; w = (code - Z) s / Z, folded per group), for
+// row lengths where every lane of a team can keep the x digits of all the
+// chunks it ever touches in registers:
+//  * A team of L lanes covers one row; lane u always handles the chunks
+//    c = u + j L (j < CPL), so its 3 * NCLASS digit words per chunk, the
+//    chunk's q / Z and q * Sxq and its scale offset are loaded from shared
+//    memory once, after x has been staged, and kept for the whole kernel.
+//    The inner loop then reads only the weight codes and one scale per
+//    chunk from shared memory: the scales of a stage travel with its codes
+//    (the kernel is used only when a row's scales are a multiple of 16
+//    bytes, i.e. groups per row % 4 == 0).
+//  * The fold keeps one accumulator per row:  y += s * (C q / Z - q Sxq)
+//    per chunk, with C the chunk's exact integer dot product.
+//  * The bulk copies of a stage are issued by up to four lanes at once
+//    (codes and scales of each matrix) rather than by one.
+// Streaming is as in qgemv_tma.cu: every warp owns a ring of `ns`
+// shared-memory slots filled by cp.async.bulk and waits only on its own.
+#include "qgemv_tma.cuh"
+
+namespace smoe {
+
+namespace {
+
+template <int BITS, int NMAT, int L, int CPL, int RPT>
+__global__ void __launch_bounds__(384, 1) qgemv_reg(const __grid_constant__ QGArgs a)
+{
+    using D = DigitFmt<BITS>;
+    constexpr int TEAMS = 32 / L;
+    constexpr int R = TEAMS * RPT;             // rows of each matrix per stage
+    constexpr int KC = L * CPL;                // 16-byte code chunks per row
+    constexpr uint32_t ROW_BYTES = KC * 16u;
+    constexpr int ND = 3 * D::NCLASS;          // digit words (uint4) per chunk
+
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = ((raw + 127u) & ~127u) - raw;
+    uint8_t *smem = smem_raw + pad;
+    const uint32_t sbase = raw + pad;
+
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int NW = blockDim.x >> 5;
+    const int e = blockIdx.x / a.ctas_per_expert;
+    const int bi = blockIdx.x - e * a.ctas_per_expert;
+    const int u0 = static_cast<int>(static_cast<long long>(a.units) * bi / a.ctas_per_expert);
+    const int u1 = static_cast<int>(static_cast<long long>(a.units) * (bi + 1) / a.ctas_per_expert);
+    const int nst = (u1 - u0 + R - 1) / R;
+    const int my = warp < nst ? (nst - warp + NW - 1) / NW : 0;  // stages of this warp
+    const int ngroups = a.K / a.group;
+    const int ns = a.ns;
+    const uint32_t bars = sbase + a.off_bars + static_cast<uint32_t>(warp * ns) * 8u;
+    const uint32_t slots = sbase + a.off_slots + static_cast<uint32_t>(warp * ns) * a.stage_bytes;
+    const uint32_t scales_off = static_cast<uint32_t>(NMAT * R) * ROW_BYTES;
+    const uint32_t sbytes_row = static_cast<uint32_t>(ngroups) * 4u;  // scales travel with the codes
+
+    // Copy roles: lanes 0..NMAT-1 the codes of matrix `lane`, lanes
+    // NMAT..2 NMAT-1 the scales of matrix `lane - NMAT`.  src0 is this lane's source for the warp's first
+    // stage; each later stage of the warp is NW * R rows further on.
+    const int role_m = lane < NMAT ? lane : lane - NMAT;
+    const bool role_codes = lane < NMAT;
+    const bool role_any = lane < 2 * NMAT;
+    const uint8_t *src0 = nullptr;
+    size_t src_step = 0;
+    uint32_t row_b = 0, dst_off = 0;
+    if (role_any) {
+        const int m = role_m < NMAT ? role_m : 0;
+        const size_t first_row = static_cast<size_t>(u0) + static_cast<size_t>(warp) * R;
+        if (role_codes) {
+            const uint8_t *c = (NMAT == 2 && m == 1) ? a.codes[1][e] : a.codes[0][e];
+            src0 = c + first_row * ROW_BYTES;
+            row_b = ROW_BYTES;
+            dst_off = static_cast<uint32_t>(m * R) * ROW_BYTES;
+        } else {
+            const float *sc = (NMAT == 2 && m == 1) ? a.scales[1][e] : a.scales[0][e];
+            src0 = reinterpret_cast<const uint8_t *>(sc + first_row * ngroups);
+            row_b = sbytes_row;
+            dst_off = scales_off + static_cast<uint32_t>(m * R) * sbytes_row;
+        }
+        src_step = static_cast<size_t>(NW) * R * row_b;
+    }
+
+    // The whole warp: the copies of its k-th stage into slot `si`.
+    auto issue = [&](int k, int si) {
+        const int us = u0 + (warp + k * NW) * R;
+        const uint32_t n = static_cast<uint32_t>(min(R, u1 - us));
+        const uint32_t slot = slots + static_cast<uint32_t>(si) * a.stage_bytes;
+        const uint32_t bar = bars + static_cast<uint32_t>(si) * 8u;
+        if (lane == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(NMAT) * n * (ROW_BYTES + sbytes_row));
+        __syncwarp();
+        if (role_any) bulk_g2s(slot + dst_off, src0 + static_cast<size_t>(k) * src_step, n * row_b, bar);
+    };
+
+    if (lane == 0) {
+        for (int i = 0; i < ns; ++i) mbar_init(bars + 8u * i, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    {
+        const int first = my < ns ? my : ns;
+        for (int k = 0; k < first; ++k) issue(k, k);
+    }
+
+    pdl_wait();
+    stage_x_digits<BITS>(a.x[e], a.K, a.group, smem, a.off_info, a.off_gmax);
+    __syncthreads();
+    if (threadIdx.x == 0) pdl_launch_dependents();
+
+    const int team = lane / L;
+    const int u = lane % L;
+
+    // This lane's digits, q / Z, q * Sxq and scale offsets, for good.
+    uint4 dg[CPL][ND];
+    float qz[CPL], qs[CPL];
+    uint32_t soff[CPL];
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+        const int c = u + j * L;
+        const uint32_t xc = sbase + static_cast<uint32_t>(c) * D::XSTRIDE;
+#pragma unroll
+        for (int t = 0; t < ND; ++t) dg[j][t] = lds128u(xc + static_cast<uint32_t>(t) * 16u);
+        const float4 inf = lds128f(sbase + a.off_info + static_cast<uint32_t>(c) * 16u);
+        qz[j] = inf.x * D::ZINV;
+        qs[j] = inf.y;
+        soff[j] = static_cast<uint32_t>(__float_as_int(inf.z)) * 4u;
+    }
+
+    int k = 0, si = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (; k < my; ++k) {
+        ok = mbar_wait_bounded(bars + static_cast<uint32_t>(si) * 8u, phase, a.status, 1u);
+        ok = __all_sync(FULL_MASK, ok);
+        if (!ok) break;
+        const uint32_t slot = slots + static_cast<uint32_t>(si) * a.stage_bytes;
+        const int us = u0 + (warp + k * NW) * R;
+        const uint32_t code_lane = slot + static_cast<uint32_t>(team) * ROW_BYTES + static_cast<uint32_t>(u) * 16u;
+        const uint32_t scale_lane = slot + scales_off + static_cast<uint32_t>(team) * sbytes_row;
+
+        float acc[NMAT][RPT];
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) acc[m][r] = 0.f;
+
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+                for (int r = 0; r < RPT; ++r) {
+                    // row m R + r TEAMS + team, chunk u + j L
+                    const uint4 cw = lds128u(code_lane + static_cast<uint32_t>((m * R + r * TEAMS) * ROW_BYTES +
+                                                                               j * L * 16));
+                    int A0 = 0, A1 = 0, A2 = 0;
+#pragma unroll
+                    for (int cl = 0; cl < D::NCLASS; ++cl)
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const uint32_t cb = D::cls(word_of(cw, v), cl);
+                            A0 = dp4a_us(cb, word_of(dg[j][3 * cl + 0], v), A0);
+                            A1 = dp4a_us(cb, word_of(dg[j][3 * cl + 1], v), A1);
+                            A2 = dp4a_us(cb, word_of(dg[j][3 * cl + 2], v), A2);
+                        }
+                    // |C| < 2^31: at most 32 codes x 15 x 2^22 (Q4), 64 x 3 x 2^22 (Q2)
+                    const int C = A2 * 65536 + A1 * 256 + A0;
+                    const float sc =
+                        lds_f32(scale_lane + static_cast<uint32_t>(m * R + r * TEAMS) * sbytes_row + soff[j]);
+                    acc[m][r] = fmaf(sc, fmaf(static_cast<float>(C), qz[j], -qs[j]), acc[m][r]);
+                }
+        }
+#pragma unroll
+        for (int m = 0; m < NMAT; ++m)
+#pragma unroll
+            for (int r = 0; r < RPT; ++r)
+#pragma unroll
+                for (int off = L / 2; off > 0; off >>= 1) acc[m][r] += __shfl_xor_sync(FULL_MASK, acc[m][r], off);
+        __syncwarp();
+        if (k + ns < my) {
+            fence_proxy_async_smem();
+            issue(k + ns, si);
+        }
+        if (u == 0) {
+#pragma unroll
+            for (int r = 0; r < RPT; ++r) {
+                const int ul = r * TEAMS + team;
+                if (us + ul < u1) {
+                    float out = acc[0][r];
+                    if (NMAT == 2) out = silu_f32(acc[0][r]) * acc[NMAT - 1][r];
+                    a.y[e][us + ul] = out;
+                }
+            }
+        }
+        if (++si == ns) {
+            si = 0;
+            phase ^= 1u;
+        }
+    }
+    if (!ok && lane == 0) {
+        // A copy never completed: wait (bounded) for the ones still in
+        // flight (stages k .. min(k + ns, my) - 1, in ring order from si)
+        // before the CTA's shared memory is released.
+        const int last = (k + ns < my) ? k + ns : my;
+        for (int kk = k; kk < last; ++kk) {
+            mbar_wait_bounded(bars + static_cast<uint32_t>(si) * 8u, phase, nullptr, 0u);
+            if (++si == ns) {
+                si = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+}
+
+template <int BITS, int NMAT, int L, int RPT>
+QGKernelFn pick_cpl(int cpl)
+{
+    switch (cpl) {
+    case 1: return qgemv_reg<BITS, NMAT, L, 1, RPT>;
+    case 2: return qgemv_reg<BITS, NMAT, L, 2, RPT>;
+    case 3: return BITS == 4 ? qgemv_reg<BITS, NMAT, L, (BITS == 4 ? 3 : 1), RPT> : nullptr;
+    case 4: return BITS == 4 ? qgemv_reg<BITS, NMAT, L, (BITS == 4 ? 4 : 1), RPT> : nullptr;
+    default: return nullptr;
+    }
+}
+
+template <int BITS, int NMAT, int RPT>
+QGKernelFn pick_l(int L, int cpl)
+{
+    if (L == 32) return pick_cpl<BITS, NMAT, 32, RPT>(cpl);
+    if (L == 16) return pick_cpl<BITS, NMAT, 16, RPT>(cpl);
+    if (L == 8) return pick_cpl<BITS, NMAT, 8, RPT>(cpl);
+    return nullptr;
+}
+
+}  // namespace
+
+QGKernelFn qgemv_reg_kernel(int bits, int nmat, int L, int cpl, int rpt)
+{
+    // gate/up (two matrices) always streams one row per team and stage
+    if (nmat == 2) {
+        if (rpt != 1) return nullptr;
+        return bits == 4 ? pick_l<4, 2, 1>(L, cpl) : pick_l<2, 2, 1>(L, cpl);
+    }
+    if (rpt == 1) return bits == 4 ? pick_l<4, 1, 1>(L, cpl) : pick_l<2, 1, 1>(L, cpl);
+    if (rpt == 2) return bits == 4 ? pick_l<4, 1, 2>(L, cpl) : pick_l<2, 1, 2>(L, cpl);
+    return nullptr;
+}
+
+}  // namespace smoe

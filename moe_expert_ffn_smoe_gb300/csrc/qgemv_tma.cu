@@ -37,173 +37,9 @@
 // Error: only the rounding of x to xq (at most 2^-22 of the group's largest
 // |x| per element) and the f32 epilogue; far inside 1e-4 * sum|w x|.
 // Non-finite x makes the chunk's q NaN, so the affected outputs are NaN.
-#include "common.cuh"
-#include "internal.h"
-#include "qformat.cuh"
+#include "qgemv_tma.cuh"
 
 namespace smoe {
-
-constexpr int QG_MAX_EXPERTS = 64;
-
-struct QGArgs {
-    const uint8_t *codes[2][QG_MAX_EXPERTS];
-    const float *scales[2][QG_MAX_EXPERTS];
-    const float *x[QG_MAX_EXPERTS];
-    float *y[QG_MAX_EXPERTS];
-    unsigned *status;      // device status word (bounded waits)
-    int ctas_per_expert;
-    int units;             // output rows per expert
-    int K;
-    int group;
-    int scales_tma;        // scales travel with the codes (ngroups % 4 == 0)
-    int ns;                // ring slots per warp
-    uint32_t stage_bytes;  // bytes of one slot
-    uint32_t off_info, off_gmax, off_bars, off_slots;  // shared-memory offsets
-};
-
-template <int BITS>
-struct DigitFmt;
-
-template <>
-struct DigitFmt<4> {
-    static constexpr int NCLASS = 2;     // byte classes per code word
-    static constexpr int XSTRIDE = 112;  // digit bytes per chunk (96 + 16 pad: conflict-free)
-    static constexpr int CODES_PER_CHUNK = 32;
-    static constexpr int WORD_COLS = 8;
-    static constexpr float ZINV = 1.0f / 7.5f;
-    // class 0: codes of the even columns, class 1: odd columns, one per byte
-    static __device__ __forceinline__ int cls(uint32_t w, int k)
-    {
-        return static_cast<int>((k == 0 ? w : (w >> 4)) & 0x0F0F0F0Fu);
-    }
-    // column (0..7 inside the word) whose digit goes to byte b of class k
-    static __device__ __forceinline__ int col(int k, int b) { return 2 * b + k; }
-};
-
-template <>
-struct DigitFmt<2> {
-    static constexpr int NCLASS = 4;
-    static constexpr int XSTRIDE = 208;  // 192 + 16 pad
-    static constexpr int CODES_PER_CHUNK = 64;
-    static constexpr int WORD_COLS = 16;
-    static constexpr float ZINV = 1.0f / 1.5f;
-    static __device__ __forceinline__ int cls(uint32_t w, int k)
-    {
-        return static_cast<int>((w >> (2 * k)) & 0x03030303u);
-    }
-    static __device__ __forceinline__ int col(int k, int b) { return 4 * b + k; }
-};
-
-__device__ __forceinline__ uint4 lds128u(uint32_t addr)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ float4 lds128f(uint32_t addr)
-{
-    float4 v;
-    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
-    return v;
-}
-
-__device__ __forceinline__ float lds_f32(uint32_t addr)
-{
-    float v;
-    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
-    return v;
-}
-
-// Balanced base-256 digits of v (|v| <= 2^22): v = d0 + 256 d1 + 65536 d2,
-// every digit in [-128, 127].
-__device__ __forceinline__ void digits3(int v, int &d0, int &d1, int &d2)
-{
-    d0 = static_cast<int>(static_cast<signed char>(v & 0xFF));
-    const int r = (v - d0) >> 8;
-    d1 = static_cast<int>(static_cast<signed char>(r & 0xFF));
-    d2 = (r - d1) >> 8;
-}
-
-__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
-{
-    return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
-           ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
-}
-
-// Stages x[0..K) as digits: chunk c occupies XSTRIDE bytes at c*XSTRIDE;
-// inside it, the uint4 at (3k + j)*16 holds digit j of byte class k for the
-// chunk's 4 code words (word v in component v).  info[c] = {q, q*Sxq, group
-// index, 0}.  Called by all threads of the block (blockDim.x % 32 == 0).
-template <int BITS>
-__device__ void stage_x_digits(const float *__restrict__ x, int K, int group, uint8_t *smem, uint32_t off_info,
-                               uint32_t off_gmax)
-{
-    using D = DigitFmt<BITS>;
-    const int nwords = K / D::WORD_COLS;
-    const int ngroups = K / group;
-    unsigned *gmax = reinterpret_cast<unsigned *>(smem + off_gmax);
-    float4 *info = reinterpret_cast<float4 *>(smem + off_info);
-    for (int g = threadIdx.x; g < ngroups; g += blockDim.x) gmax[g] = 0u;
-    __syncthreads();
-    for (int v = threadIdx.x; v < nwords; v += blockDim.x) {
-        const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
-        float m = 0.f;
-#pragma unroll
-        for (int i = 0; i < D::WORD_COLS / 4; ++i) {
-            const float4 f = p[i];
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
-            if (!(isfinite(f.x) && isfinite(f.y) && isfinite(f.z) && isfinite(f.w))) m = __uint_as_float(0x7F800000u);
-        }
-        atomicMax(&gmax[(v * D::WORD_COLS) / group], __float_as_uint(m));
-    }
-    __syncthreads();
-    for (int base = 0; base < nwords; base += blockDim.x) {
-        const int v = base + threadIdx.x;
-        int S = 0;
-        float q = 1.f;
-        int g = 0;
-        if (v < nwords) {
-            g = (v * D::WORD_COLS) / group;
-            const unsigned mb = gmax[g];
-            int e = static_cast<int>(mb >> 23) - 127;
-            if (e < -105) e = -105;
-            const bool finite = mb < 0x7F800000u;
-            const float scale = finite ? __uint_as_float(static_cast<unsigned>(127 + 21 - e) << 23) : 0.f;
-            q = finite ? __uint_as_float(static_cast<unsigned>(127 + e - 21) << 23) : __uint_as_float(0x7FC00000u);
-            int xq[D::WORD_COLS];
-            const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
-#pragma unroll
-            for (int i = 0; i < D::WORD_COLS / 4; ++i) {
-                const float4 f = p[i];
-                xq[4 * i + 0] = __float2int_rn(f.x * scale);
-                xq[4 * i + 1] = __float2int_rn(f.y * scale);
-                xq[4 * i + 2] = __float2int_rn(f.z * scale);
-                xq[4 * i + 3] = __float2int_rn(f.w * scale);
-            }
-            if (!finite) {
-#pragma unroll
-                for (int i = 0; i < D::WORD_COLS; ++i) xq[i] = 0;
-            }
-            int d[3][D::WORD_COLS];
-#pragma unroll
-            for (int i = 0; i < D::WORD_COLS; ++i) {
-                digits3(xq[i], d[0][i], d[1][i], d[2][i]);
-                S += xq[i];
-            }
-            uint8_t *chunk = smem + static_cast<size_t>(v >> 2) * D::XSTRIDE + (v & 3) * 4;
-#pragma unroll
-            for (int k = 0; k < D::NCLASS; ++k)
-#pragma unroll
-                for (int j = 0; j < 3; ++j)
-                    *reinterpret_cast<uint32_t *>(chunk + (3 * k + j) * 16) =
-                        pack4(d[j][D::col(k, 0)], d[j][D::col(k, 1)], d[j][D::col(k, 2)], d[j][D::col(k, 3)]);
-        }
-        S += __shfl_xor_sync(FULL_MASK, S, 1);
-        S += __shfl_xor_sync(FULL_MASK, S, 2);
-        if (v < nwords && (v & 3) == 0) info[v >> 2] = make_float4(q, static_cast<float>(S) * q, __int_as_float(g), 0.f);
-    }
-}
 
 // Every warp owns `ns` slots and streams its own stages through them: lane 0
 // issues the bulk copies of stage k into slot k % ns, the warp waits on the
@@ -320,10 +156,10 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
                     for (int r = 0; r < RPT; ++r)
 #pragma unroll
                         for (int v = 0; v < 4; ++v) {
-                            const int cb = D::cls(word_of(cw[m][r], v), cl);
-                            A0[m][r] = __dp4a(cb, static_cast<int>(word_of(d0, v)), A0[m][r]);
-                            A1[m][r] = __dp4a(cb, static_cast<int>(word_of(d1, v)), A1[m][r]);
-                            A2[m][r] = __dp4a(cb, static_cast<int>(word_of(d2, v)), A2[m][r]);
+                            const uint32_t cb = D::cls(word_of(cw[m][r], v), cl);
+                            A0[m][r] = dp4a_us(cb, word_of(d0, v), A0[m][r]);
+                            A1[m][r] = dp4a_us(cb, word_of(d1, v), A1[m][r]);
+                            A2[m][r] = dp4a_us(cb, word_of(d2, v), A2[m][r]);
                         }
             }
 #pragma unroll
@@ -409,8 +245,8 @@ struct TmaConfig {
 // Ring shape for a row range of `max_units` rows: the largest bytes in
 // flight that fit the shared-memory budget, preferring 16 warps.
 template <int BITS, int NMAT>
-bool pick_config(const QGArgs &a, int teams, int max_units, int max_smem, TmaConfig *out, uint32_t *stage_bytes,
-                 uint32_t *off_slots, size_t *smem_out)
+bool pick_config(const QGArgs &a, int teams, int max_units, int max_smem, int max_nw, int max_rpt, TmaConfig *out,
+                 uint32_t *stage_bytes, uint32_t *off_slots, size_t *smem_out)
 {
     using D = DigitFmt<BITS>;
     const int KC = a.K / D::CODES_PER_CHUNK;
@@ -419,12 +255,12 @@ bool pick_config(const QGArgs &a, int teams, int max_units, int max_smem, TmaCon
     const size_t budget = kSmemBudget < static_cast<size_t>(max_smem) ? kSmemBudget : static_cast<size_t>(max_smem);
     size_t best_flight = 0;
     bool found = false;
-    for (int rpt = 1; rpt <= 2; ++rpt) {
+    for (int rpt = 1; rpt <= max_rpt; ++rpt) {
         const int R = teams * rpt;
         const int max_stages = (max_units + R - 1) / R;
         const uint32_t sbytes = round16(static_cast<uint32_t>(NMAT * R) * row_bytes +
                                         (a.scales_tma ? static_cast<uint32_t>(NMAT * R * ngroups) * 4u : 0u));
-        for (int nw = 16; nw >= 8; nw -= 4) {
+        for (int nw = max_nw; nw >= 8; nw -= 4) {
             const int per_warp = (max_stages + nw - 1) / nw;
             for (int ns = 4; ns >= 1; --ns) {
                 if (ns > per_warp && ns > 1) continue;
@@ -477,8 +313,26 @@ cudaError_t launch_tma(QGArgs &a, int n_experts, cudaStream_t stream, bool *unsu
     a.off_bars = a.off_gmax + round16(static_cast<uint32_t>(ngroups) * 4u);
     TmaConfig cfg;
     size_t smem = 0;
-    if (!pick_config<BITS, NMAT>(a, 32 / L, max_units, dev->max_smem_optin, &cfg, &a.stage_bytes, &a.off_slots,
-                                 &smem)) {
+    // Register-digit kernel when a lane's share of the row is at most
+    // reg_kernel_max_cpl(BITS) chunks: the largest team (L) that divides KC.
+    int rl = 0;
+    for (int l = 32; l >= 8; l >>= 1)
+        if (KC % l == 0 && KC / l <= reg_kernel_max_cpl(BITS)) {
+            rl = l;
+            break;
+        }
+    if (rl != 0 && a.scales_tma && pick_config<BITS, NMAT>(a, 32 / rl, max_units, dev->max_smem_optin, 12, NMAT == 2 ? 1 : 2, &cfg,
+                                           &a.stage_bytes, &a.off_slots, &smem)) {
+        QGKernelFn rk = qgemv_reg_kernel(BITS, NMAT, rl, KC / rl, cfg.rpt);
+        if (rk) {
+            a.ns = cfg.ns;
+            cudaError_t err = ensure_dynamic_smem(rk, smem);
+            if (err != cudaSuccess) return err;
+            return launch_pdl(rk, dim3(static_cast<unsigned>(cpe * n_experts)), dim3(cfg.nw * 32), smem, stream, a);
+        }
+    }
+    if (!pick_config<BITS, NMAT>(a, 32 / L, max_units, dev->max_smem_optin, 16, 2, &cfg, &a.stage_bytes,
+                                 &a.off_slots, &smem)) {
         *unsupported = true;
         return cudaSuccess;
     }

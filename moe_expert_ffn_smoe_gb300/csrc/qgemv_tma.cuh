@@ -1,0 +1,205 @@
+// Shared pieces of the two decode kernels (qgemv_tma.cu: x digits read from
+// shared memory; qgemv_reg.cu: x digits held in registers): the launch
+// arguments, the per-format digit layout and the staging of x as exact
+// integer digits.  The arithmetic is described at the top of qgemv_tma.cu.
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+#include "qformat.cuh"
+
+namespace smoe {
+
+constexpr int QG_MAX_EXPERTS = 64;
+
+struct QGArgs {
+    const uint8_t *codes[2][QG_MAX_EXPERTS];
+    const float *scales[2][QG_MAX_EXPERTS];
+    const float *x[QG_MAX_EXPERTS];
+    float *y[QG_MAX_EXPERTS];
+    unsigned *status;      // device status word (bounded waits)
+    int ctas_per_expert;
+    int units;             // output rows per expert
+    int K;
+    int group;
+    int scales_tma;        // scales travel with the codes (ngroups % 4 == 0)
+    int ns;                // ring slots per warp
+    uint32_t stage_bytes;  // bytes of one slot
+    uint32_t off_info, off_gmax, off_bars, off_slots;  // shared-memory offsets
+};
+
+template <int BITS>
+struct DigitFmt;
+
+template <>
+struct DigitFmt<4> {
+    static constexpr int NCLASS = 2;     // byte classes per code word
+    static constexpr int XSTRIDE = 112;  // digit bytes per chunk (96 + 16 pad: conflict-free)
+    static constexpr int CODES_PER_CHUNK = 32;
+    static constexpr int WORD_COLS = 8;
+    static constexpr float ZINV = 1.0f / 7.5f;
+    // class 0: codes of the even columns, class 1: 16 x the codes of the odd
+    // columns (the high nibbles, masked in place), one per byte.  The digits
+    // of class k are those of x scaled by 2^-SHIFT(k), so the byte products
+    // carry the same weight in both classes.
+    static __device__ __forceinline__ uint32_t cls(uint32_t w, int k)
+    {
+        return w & (k == 0 ? 0x0F0F0F0Fu : 0xF0F0F0F0u);
+    }
+    static constexpr int SHIFT(int k) { return 4 * k; }
+    // column (0..7 inside the word) whose digit goes to byte b of class k
+    static __device__ __forceinline__ int col(int k, int b) { return 2 * b + k; }
+};
+
+template <>
+struct DigitFmt<2> {
+    static constexpr int NCLASS = 4;
+    static constexpr int XSTRIDE = 208;  // 192 + 16 pad
+    static constexpr int CODES_PER_CHUNK = 64;
+    static constexpr int WORD_COLS = 16;
+    static constexpr float ZINV = 1.0f / 1.5f;
+    static __device__ __forceinline__ uint32_t cls(uint32_t w, int k)
+    {
+        return (w >> (2 * k)) & 0x03030303u;
+    }
+    static constexpr int SHIFT(int) { return 0; }
+    static __device__ __forceinline__ int col(int k, int b) { return 4 * b + k; }
+};
+
+__device__ __forceinline__ uint4 lds128u(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float4 lds128f(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr)
+{
+    float v;
+    asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// c + sum of the four byte products a_i * b_i, a's bytes unsigned (codes,
+// possibly shifted into the high nibble), b's bytes signed (x digits).
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// Balanced base-256 digits of v (|v| <= 2^22): v = d0 + 256 d1 + 65536 d2,
+// every digit in [-128, 127].
+__device__ __forceinline__ void digits3(int v, int &d0, int &d1, int &d2)
+{
+    d0 = static_cast<int>(static_cast<signed char>(v & 0xFF));
+    const int r = (v - d0) >> 8;
+    d1 = static_cast<int>(static_cast<signed char>(r & 0xFF));
+    d2 = (r - d1) >> 8;
+}
+
+__device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
+{
+    return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
+           ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
+}
+
+// Stages x[0..K) as digits: chunk c occupies XSTRIDE bytes at c*XSTRIDE;
+// inside it, the uint4 at (3k + j)*16 holds digit j of byte class k for the
+// chunk's 4 code words (word v in component v).  info[c] = {q, q*Sxq, group
+// index, 0}.  Called by all threads of the block (blockDim.x % 32 == 0).
+template <int BITS>
+__device__ void stage_x_digits(const float *__restrict__ x, int K, int group, uint8_t *smem, uint32_t off_info,
+                               uint32_t off_gmax)
+{
+    using D = DigitFmt<BITS>;
+    const int nwords = K / D::WORD_COLS;
+    const int ngroups = K / group;
+    unsigned *gmax = reinterpret_cast<unsigned *>(smem + off_gmax);
+    float4 *info = reinterpret_cast<float4 *>(smem + off_info);
+    for (int g = threadIdx.x; g < ngroups; g += blockDim.x) gmax[g] = 0u;
+    __syncthreads();
+    for (int v = threadIdx.x; v < nwords; v += blockDim.x) {
+        const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
+        float m = 0.f;
+#pragma unroll
+        for (int i = 0; i < D::WORD_COLS / 4; ++i) {
+            const float4 f = p[i];
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
+            if (!(isfinite(f.x) && isfinite(f.y) && isfinite(f.z) && isfinite(f.w))) m = __uint_as_float(0x7F800000u);
+        }
+        atomicMax(&gmax[(v * D::WORD_COLS) / group], __float_as_uint(m));
+    }
+    __syncthreads();
+    for (int base = 0; base < nwords; base += blockDim.x) {
+        const int v = base + threadIdx.x;
+        int S = 0;
+        float q = 1.f;
+        int g = 0;
+        if (v < nwords) {
+            g = (v * D::WORD_COLS) / group;
+            const unsigned mb = gmax[g];
+            int e = static_cast<int>(mb >> 23) - 127;
+            if (e < -105) e = -105;
+            const bool finite = mb < 0x7F800000u;
+            const float scale = finite ? __uint_as_float(static_cast<unsigned>(127 + 21 - e) << 23) : 0.f;
+            q = finite ? __uint_as_float(static_cast<unsigned>(127 + e - 21) << 23) : __uint_as_float(0x7FC00000u);
+            int xq[D::WORD_COLS];
+            const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
+            // column i of the word is in byte class i % NCLASS; class k is
+            // rounded at 2^SHIFT(k) times the step q
+#pragma unroll
+            for (int i = 0; i < D::WORD_COLS / 4; ++i) {
+                const float4 f = p[i];
+                const float fv[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int col = 4 * i + t;
+                    const float sk = scale * __uint_as_float(static_cast<unsigned>(127 - D::SHIFT(col % D::NCLASS)) << 23);
+                    xq[col] = __float2int_rn(fv[t] * sk);
+                }
+            }
+            if (!finite) {
+#pragma unroll
+                for (int i = 0; i < D::WORD_COLS; ++i) xq[i] = 0;
+            }
+            int d[3][D::WORD_COLS];
+#pragma unroll
+            for (int i = 0; i < D::WORD_COLS; ++i) {
+                digits3(xq[i], d[0][i], d[1][i], d[2][i]);
+                S += xq[i] * (1 << D::SHIFT(i % D::NCLASS));
+            }
+            uint8_t *chunk = smem + static_cast<size_t>(v >> 2) * D::XSTRIDE + (v & 3) * 4;
+#pragma unroll
+            for (int k = 0; k < D::NCLASS; ++k)
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+                    *reinterpret_cast<uint32_t *>(chunk + (3 * k + j) * 16) =
+                        pack4(d[j][D::col(k, 0)], d[j][D::col(k, 1)], d[j][D::col(k, 2)], d[j][D::col(k, 3)]);
+        }
+        S += __shfl_xor_sync(FULL_MASK, S, 1);
+        S += __shfl_xor_sync(FULL_MASK, S, 2);
+        if (v < nwords && (v & 3) == 0) info[v >> 2] = make_float4(q, static_cast<float>(S) * q, __int_as_float(g), 0.f);
+    }
+}
+
+
+using QGKernelFn = void (*)(QGArgs);
+
+// The register-digit kernel for (bits, nmat, L lanes per row, cpl chunks
+// per lane, rpt rows per team), or nullptr when none is built for them.
+QGKernelFn qgemv_reg_kernel(int bits, int nmat, int L, int cpl, int rpt);
+
+// Chunks per lane the register-digit kernel takes at most: its digits use
+// cpl * 12 * NCLASS registers per thread.
+constexpr int reg_kernel_max_cpl(int bits) { return bits == 4 ? 4 : 2; }
+
+}  // namespace smoe
