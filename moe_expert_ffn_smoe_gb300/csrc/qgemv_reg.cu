@@ -99,15 +99,17 @@ __global__ void __launch_bounds__(384, 1) qgemv_reg(const __grid_constant__ QGAr
         fence_mbar_init();
     }
     __syncwarp();
-    {
-        const int first = my < ns ? my : ns;
-        for (int k = 0; k < first; ++k) issue(k, k);
-    }
+    // Weights never depend on an earlier kernel: the first stage goes out
+    // before waiting for it.  The rest of the first wave follows the staging
+    // of x, whose loads would otherwise queue behind it.
+    const int first = my < ns ? my : ns;
+    if (first > 0) issue(0, 0);
 
     pdl_wait();
     stage_x_digits<BITS>(a.x[e], a.K, a.group, smem, a.off_info, a.off_gmax);
     __syncthreads();
     if (threadIdx.x == 0) pdl_launch_dependents();
+    for (int k = 1; k < first; ++k) issue(k, k);
 
     const int team = lane / L;
     const int u = lane % L;

@@ -95,11 +95,14 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
         }
     };
 
+    // Weights never depend on an earlier kernel: the first stage goes out
+    // before waiting for it; the rest of the first wave follows the staging
+    // of x, whose loads would otherwise queue behind it.
+    const int first = my < ns ? my : ns;
     if (lane == 0) {
         for (int i = 0; i < ns; ++i) mbar_init(bars + 8u * i, 1);
         fence_mbar_init();
-        const int first = my < ns ? my : ns;
-        for (int k = 0; k < first; ++k) issue(k);
+        if (first > 0) issue(0);
     }
     __syncwarp();
 
@@ -107,6 +110,9 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
     stage_x_digits<BITS>(a.x[e], a.K, a.group, smem, a.off_info, a.off_gmax);
     __syncthreads();
     if (threadIdx.x == 0) pdl_launch_dependents();
+    if (lane == 0)
+        for (int k = 1; k < first; ++k) issue(k);
+    __syncwarp();
 
     const int team = lane / L;
     const int u = lane % L;

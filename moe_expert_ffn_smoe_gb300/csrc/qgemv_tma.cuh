@@ -115,61 +115,94 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
 // Stages x[0..K) as digits: chunk c occupies XSTRIDE bytes at c*XSTRIDE;
 // inside it, the uint4 at (3k + j)*16 holds digit j of byte class k for the
 // chunk's 4 code words (word v in component v).  info[c] = {q, q*Sxq, group
-// index, 0}.  Called by all threads of the block (blockDim.x % 32 == 0).
+// index, 0}.  Called by all threads of the block (blockDim.x % 32 == 0); the
+// caller synchronises the block before reading the result.
+// Thread t of each pass handles word t of x.  When a group spans a power of
+// two of at most 32 words, its words lie in consecutive lanes of one warp and
+// the group maximum is a shuffle reduction over values already in registers
+// (one read of x, no block barrier); otherwise a first pass gathers the group
+// maxima in shared memory with atomics.
 template <int BITS>
 __device__ void stage_x_digits(const float *__restrict__ x, int K, int group, uint8_t *smem, uint32_t off_info,
                                uint32_t off_gmax)
 {
     using D = DigitFmt<BITS>;
     const int nwords = K / D::WORD_COLS;
-    const int ngroups = K / group;
+    const int gw = group / D::WORD_COLS;  // words per group
+    const bool in_warp = gw <= 32 && (gw & (gw - 1)) == 0;
     unsigned *gmax = reinterpret_cast<unsigned *>(smem + off_gmax);
     float4 *info = reinterpret_cast<float4 *>(smem + off_info);
-    for (int g = threadIdx.x; g < ngroups; g += blockDim.x) gmax[g] = 0u;
-    __syncthreads();
-    for (int v = threadIdx.x; v < nwords; v += blockDim.x) {
-        const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
+
+    // largest |x| of a word, +inf when any entry is not finite
+    auto word_max = [](const float (&f)[D::WORD_COLS]) {
         float m = 0.f;
+        bool finite = true;
+#pragma unroll
+        for (int i = 0; i < D::WORD_COLS; ++i) {
+            m = fmaxf(m, fabsf(f[i]));
+            finite = finite && isfinite(f[i]);
+        }
+        return finite ? m : __uint_as_float(0x7F800000u);
+    };
+    auto load_word = [&](int v, float (&f)[D::WORD_COLS]) {
+        const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
 #pragma unroll
         for (int i = 0; i < D::WORD_COLS / 4; ++i) {
-            const float4 f = p[i];
-            m = fmaxf(m, fmaxf(fmaxf(fabsf(f.x), fabsf(f.y)), fmaxf(fabsf(f.z), fabsf(f.w))));
-            if (!(isfinite(f.x) && isfinite(f.y) && isfinite(f.z) && isfinite(f.w))) m = __uint_as_float(0x7F800000u);
+            const float4 q = p[i];
+            f[4 * i + 0] = q.x;
+            f[4 * i + 1] = q.y;
+            f[4 * i + 2] = q.z;
+            f[4 * i + 3] = q.w;
         }
-        atomicMax(&gmax[(v * D::WORD_COLS) / group], __float_as_uint(m));
+    };
+
+    if (!in_warp) {
+        const int ngroups = K / group;
+        for (int g = threadIdx.x; g < ngroups; g += blockDim.x) gmax[g] = 0u;
+        __syncthreads();
+        for (int v = threadIdx.x; v < nwords; v += blockDim.x) {
+            float f[D::WORD_COLS];
+            load_word(v, f);
+            atomicMax(&gmax[(v * D::WORD_COLS) / group], __float_as_uint(word_max(f)));
+        }
+        __syncthreads();
     }
-    __syncthreads();
     for (int base = 0; base < nwords; base += blockDim.x) {
         const int v = base + threadIdx.x;
+        const bool valid = v < nwords;
+        float f[D::WORD_COLS];
+        if (valid) {
+            load_word(v, f);
+        } else {
+#pragma unroll
+            for (int i = 0; i < D::WORD_COLS; ++i) f[i] = 0.f;
+        }
+        const int g = valid ? (v * D::WORD_COLS) / group : 0;
+        unsigned mb;
+        if (in_warp) {
+            // a group's gw words are gw consecutive lanes (base is a
+            // multiple of 32 and groups are aligned to gw words)
+            float m = word_max(f);
+            for (int off = 1; off < gw; off <<= 1) m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, off));
+            mb = __float_as_uint(m);
+        } else {
+            mb = valid ? gmax[g] : 0u;
+        }
         int S = 0;
         float q = 1.f;
-        int g = 0;
-        if (v < nwords) {
-            g = (v * D::WORD_COLS) / group;
-            const unsigned mb = gmax[g];
+        if (valid) {
             int e = static_cast<int>(mb >> 23) - 127;
             if (e < -105) e = -105;
             const bool finite = mb < 0x7F800000u;
             const float scale = finite ? __uint_as_float(static_cast<unsigned>(127 + 21 - e) << 23) : 0.f;
             q = finite ? __uint_as_float(static_cast<unsigned>(127 + e - 21) << 23) : __uint_as_float(0x7FC00000u);
-            int xq[D::WORD_COLS];
-            const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
             // column i of the word is in byte class i % NCLASS; class k is
             // rounded at 2^SHIFT(k) times the step q
+            int xq[D::WORD_COLS];
 #pragma unroll
-            for (int i = 0; i < D::WORD_COLS / 4; ++i) {
-                const float4 f = p[i];
-                const float fv[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const int col = 4 * i + t;
-                    const float sk = scale * __uint_as_float(static_cast<unsigned>(127 - D::SHIFT(col % D::NCLASS)) << 23);
-                    xq[col] = __float2int_rn(fv[t] * sk);
-                }
-            }
-            if (!finite) {
-#pragma unroll
-                for (int i = 0; i < D::WORD_COLS; ++i) xq[i] = 0;
+            for (int i = 0; i < D::WORD_COLS; ++i) {
+                const float sk = scale * __uint_as_float(static_cast<unsigned>(127 - D::SHIFT(i % D::NCLASS)) << 23);
+                xq[i] = finite ? __float2int_rn(f[i] * sk) : 0;
             }
             int d[3][D::WORD_COLS];
 #pragma unroll
@@ -187,7 +220,7 @@ __device__ void stage_x_digits(const float *__restrict__ x, int K, int group, ui
         }
         S += __shfl_xor_sync(FULL_MASK, S, 1);
         S += __shfl_xor_sync(FULL_MASK, S, 2);
-        if (v < nwords && (v & 3) == 0) info[v >> 2] = make_float4(q, static_cast<float>(S) * q, __int_as_float(g), 0.f);
+        if (valid && (v & 3) == 0) info[v >> 2] = make_float4(q, static_cast<float>(S) * q, __int_as_float(g), 0.f);
     }
 }
 
