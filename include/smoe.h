@@ -169,6 +169,63 @@ int smoe_experts_down_q2(int n_experts, const uint8_t *const *down_codes,
                          float *out, int d_model, int d_ff, int group, void *stream);
 
 /*
+ * Bytes of device workspace smoe_experts_ffn_q4/q2 needs: SMOE_FFN_SYNC_BYTES
+ * of hand-off counters followed by the hidden activations of up to 64
+ * experts (f32 [min(n_experts, 64) x d_ff]), rounded up to 256.  Returns 0
+ * for n_experts <= 0 and (size_t)-1 for d_ff < 0.
+ */
+#define SMOE_FFN_SYNC_BYTES 512u
+size_t smoe_experts_ffn_workspace_bytes(int n_experts, int d_ff);
+
+/*
+ * The whole routed-expert FFN of one token over n_experts experts ("Fused
+ * FFN Kernels -- One Simdgroup Per Output Row" for each expert, batched as
+ * in "Grouped Expert Dispatch"):
+ *
+ *   hidden_e  = SiLU(gate_e . x) * (up_e . x)
+ *   out[e][j] = (down_e . hidden_e)[j],  e in [0, n_experts).
+ *
+ * gate_codes ... down_scales: HOST arrays of n_experts DEVICE pointers,
+ * expert e's tensors laid out as for smoe_gate_up_q4/q2 and smoe_down_q4/q2
+ * (all experts share d_model, d_ff and group).  x: f32 [d_model], shared.
+ * out: f32 [n_experts x d_model] (expert-major), written; no router
+ * weighting or sum over experts is applied.
+ * workspace: device memory of at least
+ * smoe_experts_ffn_workspace_bytes(n_experts, d_ff) bytes, 16-byte aligned,
+ * owned by the caller.  Its first SMOE_FFN_SYNC_BYTES must be zero before
+ * the first call (one cudaMemset); every call that completes leaves them
+ * zero again.  The rest holds hidden between the two halves of the call.
+ * One launch covers up to 64 experts: the CTAs of an expert compute its
+ * hidden rows, meet on a counter in the workspace (a bounded wait), then
+ * compute its down rows, while the down weights already stream during the
+ * first half.  The launch occupies one CTA per SM and assumes its CTAs run
+ * together; if a wait gives up (about two seconds, e.g. when other streams
+ * hold SMs for that long) the outputs are unspecified,
+ * smoe_last_device_status reports SMOE_ERR_TIMEOUT and the counters must be
+ * zeroed again.  Shapes the one-launch kernel does not take run as
+ * smoe_experts_gate_up (into the workspace) followed by smoe_experts_down.
+ * Calls that share a workspace must not overlap on the GPU.
+ * Returns SMOE_ERR_WORKSPACE for a missing or short workspace and
+ * SMOE_ERR_ALIAS when out, x, the workspace or any weight overlap.
+ */
+int smoe_experts_ffn_q4(int n_experts, const uint8_t *const *gate_codes,
+                        const float *const *gate_scales,
+                        const uint8_t *const *up_codes,
+                        const float *const *up_scales,
+                        const uint8_t *const *down_codes,
+                        const float *const *down_scales, const float *x,
+                        float *out, int d_model, int d_ff, int group,
+                        void *workspace, size_t workspace_bytes, void *stream);
+int smoe_experts_ffn_q2(int n_experts, const uint8_t *const *gate_codes,
+                        const float *const *gate_scales,
+                        const uint8_t *const *up_codes,
+                        const float *const *up_scales,
+                        const uint8_t *const *down_codes,
+                        const float *const *down_scales, const float *x,
+                        float *out, int d_model, int d_ff, int group,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Dense bf16 matvec ("Coalesced Dense Matvec -- the Same Contract for bf16"):
  *
  *   y[r] = sum_k bf16(w[r][k]) * x[k],  r in [0, rows).

@@ -35,6 +35,7 @@ SMOE_ERR_TIMEOUT = 6
 SMOE_ERR_ALIAS = 7
 SMOE_MAX_COLS = 32768
 SMOE_NOALLOC_SCRATCH_BYTES = 4 << 20
+SMOE_FFN_SYNC_BYTES = 512
 
 _P = ctypes.c_void_p
 _I = ctypes.c_int
@@ -52,6 +53,9 @@ _SIGS = {
     "smoe_experts_gate_up_q2": ([_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P], _I),
     "smoe_experts_down_q4": ([_I, _P, _P, _P, _P, _I, _I, _I, _P], _I),
     "smoe_experts_down_q2": ([_I, _P, _P, _P, _P, _I, _I, _I, _P], _I),
+    "smoe_experts_ffn_workspace_bytes": ([_I, _I], _SZ),
+    "smoe_experts_ffn_q4": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
+    "smoe_experts_ffn_q2": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
     "smoe_ffn_batch_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "ffn_batch_q4": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "ffn_batch_q4_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
@@ -174,6 +178,36 @@ def smoe_experts_down_q4(down_codes, down_scales, hidden, out, d_model, d_ff, gr
 def smoe_experts_down_q2(down_codes, down_scales, hidden, out, d_model, d_ff, group, stream=None):
     _experts_down(_lib.smoe_experts_down_q2, "smoe_experts_down_q2", down_codes, down_scales, hidden, out,
                   d_model, d_ff, group, stream)
+
+
+def smoe_experts_ffn_workspace_bytes(n_experts, d_ff):
+    return _lib.smoe_experts_ffn_workspace_bytes(n_experts, d_ff)
+
+
+def _experts_ffn(fn, name, gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, x, out,
+                 d_model, d_ff, group, workspace, workspace_bytes, stream):
+    lists = (gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales)
+    n = len(gate_codes)
+    if any(len(a) != n for a in lists):
+        raise ValueError(f"{name}: per-expert lists differ in length")
+    arrs = [_ptr_array(a) for a in lists]
+    _check(fn(n, *arrs, _ptr(x), _ptr(out), d_model, d_ff, group, _ptr(workspace), workspace_bytes,
+              _stream(stream)), name)
+
+
+def smoe_experts_ffn_q4(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, x, out,
+                        d_model, d_ff, group, workspace, workspace_bytes, stream=None):
+    """Per-expert lists of tensors; out [n_experts, d_model]; workspace of
+    smoe_experts_ffn_workspace_bytes(n_experts, d_ff) bytes whose first
+    SMOE_FFN_SYNC_BYTES are zero before the first call."""
+    _experts_ffn(_lib.smoe_experts_ffn_q4, "smoe_experts_ffn_q4", gate_codes, gate_scales, up_codes, up_scales,
+                 down_codes, down_scales, x, out, d_model, d_ff, group, workspace, workspace_bytes, stream)
+
+
+def smoe_experts_ffn_q2(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, x, out,
+                        d_model, d_ff, group, workspace, workspace_bytes, stream=None):
+    _experts_ffn(_lib.smoe_experts_ffn_q2, "smoe_experts_ffn_q2", gate_codes, gate_scales, up_codes, up_scales,
+                 down_codes, down_scales, x, out, d_model, d_ff, group, workspace, workspace_bytes, stream)
 
 
 def matvec_bf16(w, x, y, rows, cols, stream=None):

@@ -137,6 +137,10 @@ int down_impl(int bits, const uint8_t *dc, const float *ds, const float *hidden,
 
 constexpr int kExpertsPerLaunch = 64;
 
+int launch_grouped(int bits, int nmat, int n, const uint8_t *const *c0, const float *const *s0,
+                   const uint8_t *const *c1, const float *const *s1, const float *x, float *y, int units, int K,
+                   int group, cudaStream_t s);
+
 // Grouped calls: per-expert checks, then launches of up to 64 experts each
 // (experts of one launch share the grid; a shape the grouped kernel does not
 // take is run expert by expert with the single-expert launcher).
@@ -170,7 +174,15 @@ int experts_impl(int bits, int nmat, int n, const uint8_t *const *c0, const floa
             }
         }
     }
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return launch_grouped(bits, nmat, n, c0, s0, c1, s1, x, y, units, K, group, static_cast<cudaStream_t>(stream));
+}
+
+// The launches of a grouped call whose arguments have been checked.
+int launch_grouped(int bits, int nmat, int n, const uint8_t *const *c0, const float *const *s0,
+                   const uint8_t *const *c1, const float *const *s1, const float *x, float *y, int units, int K,
+                   int group, cudaStream_t s)
+{
+    if (n == 0 || units == 0) return SMOE_OK;
     const float *xs[kExpertsPerLaunch];
     float *ys[kExpertsPerLaunch];
     for (int e0 = 0; e0 < n; e0 += kExpertsPerLaunch) {
@@ -198,9 +210,97 @@ int experts_impl(int bits, int nmat, int n, const uint8_t *const *c0, const floa
     return SMOE_OK;
 }
 
+size_t ffn_workspace_bytes(int n, int d_ff)
+{
+    if (d_ff < 0) return static_cast<size_t>(-1);
+    if (n <= 0) return 0;
+    const size_t e = static_cast<size_t>(n < kExpertsPerLaunch ? n : kExpertsPerLaunch);
+    const size_t b = SMOE_FFN_SYNC_BYTES + e * static_cast<size_t>(d_ff) * sizeof(float);
+    return (b + 255u) & ~static_cast<size_t>(255u);
+}
+
+// smoe_experts_ffn_q4/q2: checks, then per 64 experts the one-launch
+// kernel, or gate/up into the workspace followed by down.
+int experts_ffn_impl(int bits, int n, const uint8_t *const *gc, const float *const *gs, const uint8_t *const *uc,
+                     const float *const *us, const uint8_t *const *dc, const float *const *ds, const float *x,
+                     float *out, int d_model, int d_ff, int group, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (n < 0) return SMOE_ERR_SHAPE;
+    int st = check_q_shape(bits, d_ff, d_model, group);
+    if (st != SMOE_OK) return st;
+    st = check_q_shape(bits, d_model, d_ff, group);
+    if (st != SMOE_OK) return st;
+    if (n == 0 || d_model == 0) return SMOE_OK;
+    if (!gc || !gs || !uc || !us || !dc || !ds || !x || !out) return SMOE_ERR_NULL;
+    if (!aligned16(x) || !aligned16(out)) return SMOE_ERR_ALIGN;
+    const size_t need = ffn_workspace_bytes(n, d_ff);
+    if (!workspace || ws_bytes < need) return SMOE_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SMOE_ERR_ALIGN;
+    const Span o = {out, static_cast<size_t>(n) * static_cast<size_t>(d_model) * sizeof(float)};
+    const Span w = {workspace, need};
+    const Span xi = {x, static_cast<size_t>(d_model) * sizeof(float)};
+    if (overlap(o, xi) || overlap(o, w) || overlap(w, xi)) return SMOE_ERR_ALIAS;
+    for (int e = 0; e < n; ++e) {
+        const void *ptrs[6] = {gc[e], gs[e], uc[e], us[e], dc[e], ds[e]};
+        for (const void *p : ptrs) {
+            if (!p) return SMOE_ERR_NULL;
+            if (!aligned16(p)) return SMOE_ERR_ALIGN;
+        }
+        const Span ins[6] = {{gc[e], q_bytes(bits, d_ff, d_model)}, {gs[e], scale_bytes(d_ff, d_model, group)},
+                             {uc[e], q_bytes(bits, d_ff, d_model)}, {us[e], scale_bytes(d_ff, d_model, group)},
+                             {dc[e], q_bytes(bits, d_model, d_ff)}, {ds[e], scale_bytes(d_model, d_ff, group)}};
+        for (const Span &in : ins)
+            if (overlap(o, in) || overlap(w, in)) return SMOE_ERR_ALIAS;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    unsigned *sync = static_cast<unsigned *>(workspace);
+    float *hidden = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + SMOE_FFN_SYNC_BYTES);
+    for (int e0 = 0; e0 < n; e0 += kExpertsPerLaunch) {
+        const int cnt = (n - e0) < kExpertsPerLaunch ? (n - e0) : kExpertsPerLaunch;
+        float *o0 = out + static_cast<size_t>(e0) * d_model;
+        bool unsupported = true;
+        cudaError_t err = cudaSuccess;
+        if (d_ff > 0)
+            err = smoe::launch_expert_ffn(bits, cnt, gc + e0, gs + e0, uc + e0, us + e0, dc + e0, ds + e0, x,
+                                          hidden, o0, sync, d_model, d_ff, group, s, &unsupported);
+        if (err != cudaSuccess) return SMOE_ERR_LAUNCH;
+        if (unsupported) {
+            st = launch_grouped(bits, 2, cnt, gc + e0, gs + e0, uc + e0, us + e0, x, hidden, d_ff, d_model, group,
+                                s);
+            if (st != SMOE_OK) return st;
+            st = launch_grouped(bits, 1, cnt, dc + e0, ds + e0, nullptr, nullptr, hidden, o0, d_model, d_ff, group,
+                                s);
+            if (st != SMOE_OK) return st;
+        }
+    }
+    return SMOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+size_t smoe_experts_ffn_workspace_bytes(int n_experts, int d_ff) { return ffn_workspace_bytes(n_experts, d_ff); }
+
+int smoe_experts_ffn_q4(int n_experts, const uint8_t *const *gate_codes, const float *const *gate_scales,
+                        const uint8_t *const *up_codes, const float *const *up_scales,
+                        const uint8_t *const *down_codes, const float *const *down_scales, const float *x,
+                        float *out, int d_model, int d_ff, int group, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    return experts_ffn_impl(4, n_experts, gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales,
+                            x, out, d_model, d_ff, group, workspace, workspace_bytes, stream);
+}
+
+int smoe_experts_ffn_q2(int n_experts, const uint8_t *const *gate_codes, const float *const *gate_scales,
+                        const uint8_t *const *up_codes, const float *const *up_scales,
+                        const uint8_t *const *down_codes, const float *const *down_scales, const float *x,
+                        float *out, int d_model, int d_ff, int group, void *workspace, size_t workspace_bytes,
+                        void *stream)
+{
+    return experts_ffn_impl(2, n_experts, gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales,
+                            x, out, d_model, d_ff, group, workspace, workspace_bytes, stream);
+}
 
 int smoe_experts_gate_up_q4(int n_experts, const uint8_t *const *gate_codes, const float *const *gate_scales,
                             const uint8_t *const *up_codes, const float *const *up_scales, const float *x,

@@ -33,6 +33,16 @@ cudaError_t launch_qgemv_experts(int bits, int nmat, int n_experts, const uint8_
                                  const float *const *scales1, const float *const *x, float *const *y,
                                  int units, int K, int group, cudaStream_t stream, bool *unsupported);
 
+// The fused routed-expert FFN over n <= 64 experts in one launch
+// (expert_ffn.cu): hidden [n x d_ff] and the hand-off counters `sync`
+// (2 x 64 words, zero on entry, zero again on completion) live in the
+// caller's workspace.  Sets *unsupported (and launches nothing) for shapes
+// the fused kernel does not take.
+cudaError_t launch_expert_ffn(int bits, int n, const uint8_t *const *gc, const float *const *gs,
+                              const uint8_t *const *uc, const float *const *us, const uint8_t *const *dc,
+                              const float *const *ds, const float *x, float *hidden, float *out, unsigned *sync,
+                              int d_model, int d_ff, int group, cudaStream_t stream, bool *unsupported);
+
 // Device address of the library's device status word on the current device.
 unsigned *device_status_word();
 

@@ -4,22 +4,15 @@
 // (S-MoE page "Metal Compute Kernels", section "Fused FFN Kernels -- One
 // Simdgroup Per Output Row"; w = (code - Z) s / Z, folded per group), for
 // row lengths where every lane of a team can keep the x digits of all the
-// chunks it ever touches in registers:
-//  * A team of L lanes covers one row; lane u always handles the chunks
-//    c = u + j L (j < CPL), so its 3 * NCLASS digit words per chunk, the
-//    chunk's q / Z and q * Sxq and its scale offset are loaded from shared
-//    memory once, after x has been staged, and kept for the whole kernel.
-//    The inner loop then reads only the weight codes and one scale per
-//    chunk from shared memory: the scales of a stage travel with its codes
-//    (the kernel is used only when a row's scales are a multiple of 16
-//    bytes, i.e. groups per row % 4 == 0).
-//  * The fold keeps one accumulator per row:  y += s * (C q / Z - q Sxq)
-//    per chunk, with C the chunk's exact integer dot product.
-//  * The bulk copies of a stage are issued by up to four lanes at once
-//    (codes and scales of each matrix) rather than by one.
+// chunks it ever touches in registers (regdot.cuh).  The inner loop reads
+// only codes and one scale per chunk from shared memory: the scales of a
+// stage travel with its codes (the kernel is used only when a row's scales
+// are a multiple of 16 bytes, i.e. groups per row % 4 == 0).
 // Streaming is as in qgemv_tma.cu: every warp owns a ring of `ns`
 // shared-memory slots filled by cp.async.bulk and waits only on its own.
-#include "qgemv_tma.cuh"
+// The bulk copies of a stage are issued by up to four lanes at once (codes
+// and scales of each matrix).
+#include "regdot.cuh"
 
 namespace smoe {
 
@@ -28,12 +21,10 @@ namespace {
 template <int BITS, int NMAT, int L, int CPL, int RPT>
 __global__ void __launch_bounds__(384, 1) qgemv_reg(const __grid_constant__ QGArgs a)
 {
-    using D = DigitFmt<BITS>;
-    constexpr int TEAMS = 32 / L;
-    constexpr int R = TEAMS * RPT;             // rows of each matrix per stage
-    constexpr int KC = L * CPL;                // 16-byte code chunks per row
-    constexpr uint32_t ROW_BYTES = KC * 16u;
-    constexpr int ND = 3 * D::NCLASS;          // digit words (uint4) per chunk
+    using RD = RegDot<BITS, NMAT, L, CPL, RPT>;
+    constexpr int TEAMS = RD::TEAMS;
+    constexpr int R = RD::R;                   // rows of each matrix per stage
+    constexpr uint32_t ROW_BYTES = RD::ROW_BYTES;
 
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -115,20 +106,8 @@ __global__ void __launch_bounds__(384, 1) qgemv_reg(const __grid_constant__ QGAr
     const int u = lane % L;
 
     // This lane's digits, q / Z, q * Sxq and scale offsets, for good.
-    uint4 dg[CPL][ND];
-    float qz[CPL], qs[CPL];
-    uint32_t soff[CPL];
-#pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-        const int c = u + j * L;
-        const uint32_t xc = sbase + static_cast<uint32_t>(c) * D::XSTRIDE;
-#pragma unroll
-        for (int t = 0; t < ND; ++t) dg[j][t] = lds128u(xc + static_cast<uint32_t>(t) * 16u);
-        const float4 inf = lds128f(sbase + a.off_info + static_cast<uint32_t>(c) * 16u);
-        qz[j] = inf.x * D::ZINV;
-        qs[j] = inf.y;
-        soff[j] = static_cast<uint32_t>(__float_as_int(inf.z)) * 4u;
-    }
+    RD rd;
+    rd.load(sbase, a.off_info, u);
 
     int k = 0, si = 0;
     uint32_t phase = 0;
@@ -139,47 +118,8 @@ __global__ void __launch_bounds__(384, 1) qgemv_reg(const __grid_constant__ QGAr
         if (!ok) break;
         const uint32_t slot = slots + static_cast<uint32_t>(si) * a.stage_bytes;
         const int us = u0 + (warp + k * NW) * R;
-        const uint32_t code_lane = slot + static_cast<uint32_t>(team) * ROW_BYTES + static_cast<uint32_t>(u) * 16u;
-        const uint32_t scale_lane = slot + scales_off + static_cast<uint32_t>(team) * sbytes_row;
-
         float acc[NMAT][RPT];
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-            for (int r = 0; r < RPT; ++r) acc[m][r] = 0.f;
-
-#pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-#pragma unroll
-            for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-                for (int r = 0; r < RPT; ++r) {
-                    // row m R + r TEAMS + team, chunk u + j L
-                    const uint4 cw = lds128u(code_lane + static_cast<uint32_t>((m * R + r * TEAMS) * ROW_BYTES +
-                                                                               j * L * 16));
-                    int A0 = 0, A1 = 0, A2 = 0;
-#pragma unroll
-                    for (int cl = 0; cl < D::NCLASS; ++cl)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const uint32_t cb = D::cls(word_of(cw, v), cl);
-                            A0 = dp4a_us(cb, word_of(dg[j][3 * cl + 0], v), A0);
-                            A1 = dp4a_us(cb, word_of(dg[j][3 * cl + 1], v), A1);
-                            A2 = dp4a_us(cb, word_of(dg[j][3 * cl + 2], v), A2);
-                        }
-                    // |C| < 2^31: at most 32 codes x 15 x 2^22 (Q4), 64 x 3 x 2^22 (Q2)
-                    const int C = A2 * 65536 + A1 * 256 + A0;
-                    const float sc =
-                        lds_f32(scale_lane + static_cast<uint32_t>(m * R + r * TEAMS) * sbytes_row + soff[j]);
-                    acc[m][r] = fmaf(sc, fmaf(static_cast<float>(C), qz[j], -qs[j]), acc[m][r]);
-                }
-        }
-#pragma unroll
-        for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-            for (int r = 0; r < RPT; ++r)
-#pragma unroll
-                for (int off = L / 2; off > 0; off >>= 1) acc[m][r] += __shfl_xor_sync(FULL_MASK, acc[m][r], off);
+        rd.stage(slot, team, u, sbytes_row, acc);
         __syncwarp();
         if (k + ns < my) {
             fence_proxy_async_smem();

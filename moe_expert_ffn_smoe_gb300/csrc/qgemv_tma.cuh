@@ -122,7 +122,9 @@ __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
 // the group maximum is a shuffle reduction over values already in registers
 // (one read of x, no block barrier); otherwise a first pass gathers the group
 // maxima in shared memory with atomics.
-template <int BITS>
+// COHERENT: x was written by other CTAs of the running grid (read through L2
+// only, never through the read-only path).
+template <int BITS, bool COHERENT = false>
 __device__ void stage_x_digits(const float *__restrict__ x, int K, int group, uint8_t *smem, uint32_t off_info,
                                uint32_t off_gmax)
 {
@@ -148,7 +150,7 @@ __device__ void stage_x_digits(const float *__restrict__ x, int K, int group, ui
         const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
 #pragma unroll
         for (int i = 0; i < D::WORD_COLS / 4; ++i) {
-            const float4 q = p[i];
+            const float4 q = COHERENT ? __ldcg(p + i) : p[i];
             f[4 * i + 0] = q.x;
             f[4 * i + 1] = q.y;
             f[4 * i + 2] = q.z;

@@ -152,3 +152,30 @@ def test_grouped_refusals(smoe):
         smoe.SMOE_ERR_ALIAS
     assert L.smoe_experts_down_q2(2, g, gs, x, A + 0x200000, 256, 256, 64, None) == smoe.SMOE_ERR_ALIAS
     assert L.smoe_experts_down_q4(0, None, None, None, None, 256, 256, 64, None) == smoe.SMOE_OK
+
+
+def test_experts_ffn_workspace_and_refusals(smoe):
+    L = smoe._lib
+    assert L.smoe_experts_ffn_workspace_bytes(0, 1536) == 0
+    assert L.smoe_experts_ffn_workspace_bytes(8, 1536) == 512 + 8 * 1536 * 4
+    assert L.smoe_experts_ffn_workspace_bytes(100, 1536) == 512 + 64 * 1536 * 4
+    assert L.smoe_experts_ffn_workspace_bytes(3, 100) % 256 == 0
+    assert L.smoe_experts_ffn_workspace_bytes(3, -1) == ctypes.c_size_t(-1).value
+    P = lambda vals: (ctypes.c_void_p * len(vals))(*vals)
+    w = [P([A + 0x1000000 * (6 * e + k) for e in range(2)]) for k in range(6)]
+    x, out = A + 0x40000000, A + 0x41000000
+    ws = A + 0x42000000
+    need = L.smoe_experts_ffn_workspace_bytes(2, 1536)
+    f = L.smoe_experts_ffn_q4
+    args = lambda n=2, wsp=ws, wsb=need, o=out, dm=4096, df=1536, g=64: (n, *w, x, o, dm, df, g, wsp, wsb, None)
+    assert f(*args(wsb=need - 4)) == smoe.SMOE_ERR_WORKSPACE
+    assert f(*args(wsp=None)) == smoe.SMOE_ERR_WORKSPACE
+    assert f(*args(wsp=ws + 8)) == smoe.SMOE_ERR_ALIGN
+    assert f(*args(n=-1)) == smoe.SMOE_ERR_SHAPE
+    assert f(*args(df=1000)) == smoe.SMOE_ERR_SHAPE          # d_ff not a multiple of the group
+    assert f(*args(o=ws + 1024)) == smoe.SMOE_ERR_ALIAS      # out inside the workspace
+    assert f(*args(wsp=x - 256)) == smoe.SMOE_ERR_ALIAS      # workspace over x
+    assert f(*args(o=A + 0x1000000 * 4 + 64)) == smoe.SMOE_ERR_ALIAS  # out over expert 0's down codes
+    assert f(*args(n=0)) == smoe.SMOE_OK
+    bad = [P([A, A + 8])] + w[1:]
+    assert f(2, *bad, x, out, 4096, 1536, 64, ws, need, None) == smoe.SMOE_ERR_ALIGN
