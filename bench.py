@@ -160,9 +160,10 @@ class DecodeWorkload:
     """n_copies independent sets of 8 experts (bits = 4 or 2) resident on the
     device, one captured graph per copy, plus the token and outputs."""
 
-    def __init__(self, smoe, dev, bits, seed, n_copies, grouped=False):
+    def __init__(self, smoe, dev, bits, seed, n_copies, grouped=False, fused=False):
         import torch
-        self.smoe, self.dev, self.bits, self.grouped = smoe, dev, bits, grouped
+        self.smoe, self.dev, self.bits, self.grouped, self.fused = smoe, dev, bits, grouped, fused
+        self.ffn = smoe.smoe_experts_ffn_q4 if bits == 4 else smoe.smoe_experts_ffn_q2
         self.gate_up = smoe.smoe_gate_up_q4 if bits == 4 else smoe.smoe_gate_up_q2
         self.down = smoe.smoe_down_q4 if bits == 4 else smoe.smoe_down_q2
         self.g_gate_up = smoe.smoe_experts_gate_up_q4 if bits == 4 else smoe.smoe_experts_gate_up_q2
@@ -177,10 +178,19 @@ class DecodeWorkload:
         self.x = torch.from_numpy(inp.activations(D_MODEL, seed)).to(dev)
         self.hidden = torch.empty((N_EXPERTS, D_FF), device=dev)
         self.out = torch.empty((N_EXPERTS, D_MODEL), device=dev)
+        # workspace of the one-call path: counters (zero) + hidden
+        self.ws_bytes = smoe.smoe_experts_ffn_workspace_bytes(N_EXPERTS, D_FF)
+        self.ws = torch.zeros(self.ws_bytes, dtype=torch.uint8, device=dev)
         self.stream = torch.cuda.Stream(device=dev)
         self.graphs = []
 
     def calls(self, c, stream):
+        if self.fused:
+            ex = self.copies[c]
+            self.ffn(*[[t[k] for t in ex] for k in ("gate_codes", "gate_scales", "up_codes", "up_scales",
+                                                    "down_codes", "down_scales")],
+                     self.x, self.out, D_MODEL, D_FF, GROUP, self.ws, self.ws_bytes, stream=stream)
+            return
         if self.grouped:
             ex = self.copies[c]
             self.g_gate_up([t["gate_codes"] for t in ex], [t["gate_scales"] for t in ex],
@@ -292,6 +302,13 @@ def gpu_arm(args, rank, world, local):
     calls.capture()
     calls.run(max(3, args.warmup))
     calls.stream.synchronize()
+    # the same step as one call (smoe_experts_ffn_q4: one launch)
+    one = DecodeWorkload(smoe, dev, 4, 5, 0, fused=True)
+    one.copies = wl.copies
+    one.x, one.out = wl.x, wl.out
+    one.capture()
+    one.run(max(3, args.warmup))
+    one.stream.synchronize()
 
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     barrier(world)
@@ -304,6 +321,8 @@ def gpu_arm(args, rank, world, local):
     t = max_over_ranks(t, world, dev)
     t_calls = time_steps(lambda k: calls.run(k), args.steps, calls.stream)
     t_calls = max_over_ranks(t_calls, world, dev)
+    t_one = time_steps(lambda k: one.run(k), args.steps, one.stream)
+    t_one = max_over_ranks(t_one, world, dev)
 
     sb = step_bytes(4)
     value = sb * args.steps * world / t / 1e9
@@ -323,7 +342,7 @@ def gpu_arm(args, rank, world, local):
     kernel_alone_seconds(gu_launch, nlaunch, wl.stream)  # warm
     t_gu = kernel_alone_seconds(gu_launch, nlaunch, wl.stream)
     achieved = gu_bytes / t_gu / 1e9
-    roof = {"kernel": "qgemv_tma<Q4,gate_up> (smoe_experts_gate_up_q4, 8 experts x 1536x4096)",
+    roof = {"kernel": "qgemv_reg<Q4,gate_up> (smoe_experts_gate_up_q4, 8 experts x 1536x4096)",
             "bound": "hbm",
             "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
             "frac": round(achieved / hbm_peak, 4), "traffic": roofline_traffic("gate_up_q4"),
@@ -363,6 +382,10 @@ def gpu_arm(args, rank, world, local):
                              "programmatic dependent launch between kernels",
                    "parallelism": f"replicas x{world} (experts are independent; no collective)"},
         "us_per_8expert_ffn": round(ms * 1e3, 3),
+        "one_call": {"GB/s": round(sb * args.steps * world / t_one / 1e9, 2),
+                     "us_per_8expert_ffn": round(t_one / args.steps * 1e6, 3),
+                     "launch": "1 C-ABI call per step (smoe_experts_ffn_q4: one launch for gate/up and "
+                               "down of the 8 experts) in a CUDA graph"},
         "per_expert_calls": {"GB/s": round(sb * args.steps * world / t_calls / 1e9, 2),
                              "us_per_8expert_ffn": round(t_calls / args.steps * 1e6, 3),
                              "launch": "16 single-expert calls (8 x smoe_gate_up_q4 + smoe_down_q4) per "
