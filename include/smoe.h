@@ -270,7 +270,7 @@ int ffn_batch_q4(const uint8_t *gate_codes, const float *gate_scales,
                  void *workspace, size_t workspace_bytes, void *stream);
 
 /* Size of the device array ffn_batch_q4_noalloc uses as its workspace. */
-#define SMOE_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define SMOE_NOALLOC_SCRATCH_BYTES (32u << 20)
 
 /*
  * ffn_batch_q4 for callers that must not allocate device memory: a host
@@ -286,9 +286,10 @@ int ffn_batch_q4(const uint8_t *gate_codes, const float *gate_scales,
  * the process exits.  Calls whose workspace need,
  * smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group), exceeds that size
  * are refused with SMOE_ERR_SHAPE before anything is launched (at
- * d_model = 4096, d_ff = 1536 every T up to 64 fits; the workspace holds the
- * hidden activations and, for T >= 2, the split token operands of the
- * tensor-core path).
+ * d_model = 4096, d_ff = 1536 every T up to 256 fits; for T >= 2 the
+ * workspace holds the split token operands of the tensor-core path, the
+ * hidden activations in the down projection's operand form and the split-K
+ * partial sums).
  * The function calls no cudaMalloc, cudaFree or other allocating routine.
  *
  * The first call on a device looks up the array's device address with

@@ -34,7 +34,7 @@ SMOE_ERR_LAUNCH = 5
 SMOE_ERR_TIMEOUT = 6
 SMOE_ERR_ALIAS = 7
 SMOE_MAX_COLS = 32768
-SMOE_NOALLOC_SCRATCH_BYTES = 4 << 20
+SMOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 SMOE_FFN_SYNC_BYTES = 512
 
 _P = ctypes.c_void_p

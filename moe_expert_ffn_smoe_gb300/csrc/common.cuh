@@ -127,14 +127,16 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
-// Tests phase `parity` of an mbarrier (the hardware may hold the thread for
-// a short, system-defined time while the phase is still incomplete).
+// Tests phase `parity` of an mbarrier.  While the phase is incomplete the
+// hardware may suspend the thread for up to about 20 us (the suspend-time
+// hint) and wakes it when the phase completes, so waiting warps leave the
+// issue slots and the shared-memory pipe to the warps that have work.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, 20000;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
         : "r"(bar), "r"(parity)

@@ -5,30 +5,45 @@
 //
 // Exactness plan (the scale varies per (row, group), so it cannot be folded
 // into an operand):
-//  * A (weights, M x 64 per group slice) holds each code c as the bf16 value
-//    1 + c/16, which is exact.  The affine fold then reads, per 64-column
-//    tile of one group, D = sum (1 + c/16) x = Sx + C/16 and
-//        sum w x = s (C/Z - Sx) = s (A D - (A + 1) Sx),   A = 16/Z.
-//  * B (tokens, N x 64) holds x split into two bf16 halves, hi = bf16(x) and
-//    lo = bf16(x - hi); two MMAs accumulate D over hi and lo into the same
-//    TMEM accumulator (x represented to about 2^-17 relative), and Sx is the
-//    f32 sum of hi + lo over the tile, so D and Sx see the same x.
-//  * Each 64-column tile's accumulator is read back from TMEM and folded
-//    into per-thread f32 sums with the tile's scale (double-buffered, so the
-//    next tile's MMAs run while the epilogue reads this one).
+//  * A (weights, 128 rows x 64 columns per K tile, one group slice) holds
+//    each code c as the bf16 value (c - Z)/16 = (2c - 15)/32, which is exact
+//    (an odd numerator of at most 4 bits).  It is made from the exact bf16
+//    1 + c/16 (a bit pattern) minus 1 + Z/16 = 1.46875, a subtraction whose
+//    exact result is representable.  Per 64-column tile of one group the
+//    accumulator is then D = sum (c - Z) x / 16 and
+//        sum w x = s sum (c - Z) x / Z = s (16/Z) D.
+//  * B (tokens, NT x 64) holds x split into two bf16 halves, hi = bf16(x) and
+//    lo = bf16(x - hi), stored as one operand of 2 NT rows (hi rows, then
+//    lo rows), so one MMA of N = 2 NT computes both halves; the epilogue
+//    adds the hi and lo columns (x represented to about 2^-17 relative).
+//  * Each 64-column tile's accumulator is read back from TMEM and added to
+//    per-thread f32 sums with the tile's scale.  TMEM holds up to 16 tiles'
+//    accumulators (512 columns), so the MMAs run ahead of the epilogue.
 //
-// CTA roles (288 threads): warps 0-3 epilogue (TMEM lane quarters 0-3 =
-// rows 0-127), warps 4-7 operand preparation (unpack codes to bf16 in the
-// canonical no-swizzle K-major layout, bulk-copy the pre-split token block),
-// warp 8 MMA issue and TMEM allocation.  Stages of shared memory hand tiles
-// from the preparation warps to the MMA thread ("full" barriers) and back
-// ("empty", signalled by tcgen05.commit); two TMEM buffers hand accumulators
-// to the epilogue and back.  Every barrier has one in-order waiter, so the
-// parity of each awaited phase is unambiguous; every wait is bounded.
-//
-// Grid: (matrix x 128-row tile, token tile, K split).  With a K split the
-// partial sums are added into a zero-initialised output with f32 atomics.
+// Three launches per call, chained with programmatic dependent launch:
+//  1. prep_tokens: X -> B blocks (hi, lo per (token tile, K tile)) and
+//     zeroed split-K counters.
+//  2. tc_ffn<NT, gate/up>: a CTA tile is 64 gate rows + the same 64 up rows
+//     (128 accumulator rows) over one K range.  The last CTA of a tile's K
+//     splits adds the partial sums in a fixed order, forms SiLU(g) * u and
+//     writes it directly as the B block of the down projection's K tile
+//     (64 hidden columns = one down K tile).
+//  3. tc_ffn<NT, down>: 128 down rows over one K range; the last split
+//     writes Y.
+// Inside a GEMM CTA (608 threads): warps 0-7 epilogue (warp w reads TMEM
+// lane quarter w % 4 = 32 tile rows, columns of half w / 4), warps 8-15
+// convert codes to A tiles (thread = half a tile row: 4 of its 8 code
+// words), warp 16 issues the MMAs, warp 17 streams code chunks with 2-D
+// tensor copies (TMA, 128-byte swizzle: 4 K tiles x 128 rows per chunk),
+// warp 18 streams the token B blocks with bulk copies.  Two converter and
+// two epilogue warps per SM sub-partition keep those dependent chains
+// overlapped.  Every hand-off is an mbarrier with one
+// in-order waiter per role, so each awaited phase parity is unambiguous;
+// every wait is bounded.
+#include <cuda.h>
 #include <cuda_bf16.h>
+
+#include <mutex>
 
 #include "common.cuh"
 #include "internal.h"
@@ -36,21 +51,40 @@
 namespace smoe {
 namespace {
 
-constexpr int KT = 64;   // columns per K tile (one group slice)
-constexpr int MT = 128;  // rows per CTA tile
-constexpr int STAGES = 4;
-constexpr int EPI_WARPS = 4;
-constexpr int PREP_WARPS = 4;
-constexpr int TC_THREADS = (EPI_WARPS + PREP_WARPS + 1) * 32;
+constexpr int KT = 64;                        // columns per K tile (one group slice)
+constexpr int MT = 128;                       // accumulator rows per CTA tile
+constexpr int CHUNK_KT = 4;                   // K tiles per code chunk
+constexpr uint32_t CHUNK_BYTES = MT * 128u;   // 128 rows x 128 bytes of Q4 codes
+constexpr int CODE_SLOTS = 3;
+constexpr int EPI_WARPS = 8;
+constexpr int CONV_WARPS = 8;
+constexpr int CONV_WARP0 = 8;
+constexpr int MMA_WARP = 16;
+constexpr int CODE_WARP = 17;
+constexpr int BPROD_WARP = 18;
+constexpr int TC_THREADS = 19 * 32;
 constexpr uint32_t A_BYTES = MT * KT * 2;
-constexpr float FOLD_A = 16.0f / 7.5f;
+constexpr float FOLD = 16.0f / 7.5f;  // 16/Z
+constexpr size_t kTcSmemBudget = 200 * 1024;
 
-__host__ __device__ constexpr uint32_t b_bytes(int nt) { return static_cast<uint32_t>(nt) * KT * 2u * 2u; }
-__host__ __device__ constexpr uint32_t stage_bytes(int nt) { return A_BYTES + b_bytes(nt); }
+// B block of one (token tile, K tile): hi [NT x 64] bf16, then lo.
+__host__ __device__ constexpr uint32_t b_bytes(int nt) { return static_cast<uint32_t>(nt) * 256u; }
+__host__ __device__ constexpr uint32_t round1024(uint32_t v) { return (v + 1023u) & ~1023u; }
+__host__ __device__ constexpr uint32_t stage_bytes(int nt) { return round1024(A_BYTES + b_bytes(nt)); }
+__host__ __device__ constexpr int stages_for(int nt)
+{
+    return static_cast<int>((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / stage_bytes(nt)) < 8
+               ? static_cast<int>((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / stage_bytes(nt))
+               : 8;
+}
+// TMEM accumulator buffers: as many 2 NT-column buffers as fit in 512
+// columns (at most 16), so the MMAs of later K tiles rarely wait for the
+// epilogue.
+__host__ __device__ constexpr int accbufs_for(int nt) { return 256 / nt < 16 ? 256 / nt : 16; }
 
 // Byte offset of (row, 8-column block k8) in a [rows x 64] bf16 tile laid out
 // as 8x8 core matrices: core (row/8, k8) at ((row/8)*8 + k8)*128, row%8 at 16*(row%8).
-__device__ __forceinline__ uint32_t core_off(int row, int k8)
+__host__ __device__ __forceinline__ uint32_t core_off(int row, int k8)
 {
     return static_cast<uint32_t>(((row >> 3) * 8 + k8) * 128 + (row & 7) * 16);
 }
@@ -95,31 +129,65 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 16 consecutive f32 columns of this warp's 32 TMEM lanes.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16])
+// 8 consecutive f32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v)
 {
-    uint32_t r[16];
+    uint32_t r[8];
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 32 consecutive f32 columns of this warp's 32 TMEM lanes.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v)
+{
+    uint32_t r[32];
     asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// N (a multiple of 8) consecutive f32 columns of this warp's 32 TMEM lanes.
+template <int N>
+__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[N])
+{
+#pragma unroll
+    for (int c = 0; c + 32 <= N; c += 32) tmem_ld32(taddr + c, v + c);
+#pragma unroll
+    for (int c = N / 32 * 32; c < N; c += 8) tmem_ld8(taddr + c, v + c);
 }
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+// bf16x2 a - b (round to nearest; exact here: the difference is representable).
+__device__ __forceinline__ uint32_t bf16x2_sub(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // One 32-bit word of Q4 codes (columns 0..7) as 8 exact bf16 values
-// 1 + c/16, in the order 0,4,1,5,2,6,3,7.
+// (c - 7.5)/16, in the order 0,4,1,5,2,6,3,7: the bit pattern of 1 + c/16
+// (exponent 0, c in the top four mantissa bits) minus 1 + 7.5/16.
 __device__ __forceinline__ uint4 q4_word_to_bf16(uint32_t w)
 {
-    const uint32_t mag = 0x3F803F80u;
+    const uint32_t mag = 0x3F803F80u;  // 1.0, 1.0
+    const uint32_t off = 0x3FBC3FBCu;  // 1.46875, 1.46875
     uint4 r;
-    r.x = ((w << 3) & 0x00780078u) | mag;  // columns 0 and 4
-    r.y = ((w >> 1) & 0x00780078u) | mag;  // 1 and 5
-    r.z = ((w >> 5) & 0x00780078u) | mag;  // 2 and 6
-    r.w = ((w >> 9) & 0x00780078u) | mag;  // 3 and 7
+    r.x = bf16x2_sub(((w << 3) & 0x00780078u) | mag, off);  // columns 0 and 4
+    r.y = bf16x2_sub(((w >> 1) & 0x00780078u) | mag, off);  // 1 and 5
+    r.z = bf16x2_sub(((w >> 5) & 0x00780078u) | mag, off);  // 2 and 6
+    r.w = bf16x2_sub(((w >> 9) & 0x00780078u) | mag, off);  // 3 and 7
     return r;
 }
 
@@ -129,142 +197,154 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
                  : "memory");
 }
 
-__device__ __forceinline__ uint4 ldg_u4(const void *p)
+__device__ __forceinline__ uint4 lds128v(uint32_t addr)
 {
     uint4 v;
-    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
     return v;
 }
 
-// ---------------------------------------------------------------- B prep
+// 2-D tensor copy global -> shared of one box at (x bytes, y rows),
+// completing on the mbarrier.  x must be a multiple of 16.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+            "r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// Splits 8 values into bf16 hi/lo (hi = bf16(v), lo = bf16(v - hi)) packed
+// in pairs.
+__device__ __forceinline__ void split8(const float (&v)[8], uint32_t (&hi)[4], uint32_t (&lo)[4])
+{
+#pragma unroll
+    for (int p = 0; p < 8; p += 2) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[p]);
+        const __nv_bfloat16 h1 = __float2bfloat16_rn(v[p + 1]);
+        const __nv_bfloat16 l0 = __float2bfloat16_rn(v[p] - __bfloat162float(h0));
+        const __nv_bfloat16 l1 = __float2bfloat16_rn(v[p + 1] - __bfloat162float(h1));
+        hi[p / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+        lo[p / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+                    (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+    }
+}
+
+// ---------------------------------------------------------------- token prep
 
 struct PrepArgs {
-    const float *X;  // mode 0: [T x K]
-    const float *G;  // mode 1: [T x K] pre-activation gate sums
-    const float *U;  //         [T x K] up sums
-    uint8_t *Bblk;   // [T/nt][K/64] blocks of b_bytes(nt): hi then lo
-    float *Sx;       // [K/64][Tpad]
-    int T, Tpad, K, nt, mode;
+    const float *X;  // [T x K]
+    uint8_t *Bblk;   // [ntiles][K/64] blocks of b_bytes(nt)
+    unsigned *count; // split-K counters of both GEMMs, zeroed here
+    int ncount;
+    int T, K, nt, ntiles;
 };
 
-// One thread per (token, 8-column block): the token's 8 values (or SiLU(g)*u)
-// split into bf16 hi/lo in the tile layout, plus the per-tile sums of hi+lo.
-__global__ void __launch_bounds__(256) prep_b(PrepArgs a)
+// One thread per (token, 8-column block): the token's 8 values split into
+// bf16 hi/lo in the tile layout.  Tokens past T (padding of the last tile)
+// are zeros.
+__global__ void __launch_bounds__(256) prep_tokens(PrepArgs a)
 {
     pdl_wait();
     const int kb_per_t = a.K / 8;
     const int nkt = a.K / KT;
-    const long long total = static_cast<long long>(a.Tpad) * kb_per_t;  // multiple of 8
+    const long long total = static_cast<long long>(a.ntiles) * a.nt * kb_per_t;  // multiple of 8
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    const long long first = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (first < a.ncount) a.count[first] = 0u;
     const long long rounds = (total + stride - 1) / stride;
     for (long long rd = 0; rd < rounds; ++rd) {
-        const long long idx = rd * stride + static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-        float part = 0.f;
-        int t = 0, kt = 0;
-        const bool live = idx < total;
-        if (live) {
-            t = static_cast<int>(idx / kb_per_t);
-            const int kb = static_cast<int>(idx % kb_per_t);
-            kt = kb / 8;
-            const int k8 = kb % 8;
-            float v[8];
-            if (t < a.T) {
-                const size_t base = static_cast<size_t>(t) * a.K + static_cast<size_t>(kb) * 8;
-                float raw[8];
-                if (a.mode == 0) {
-                    const float4 p0 = reinterpret_cast<const float4 *>(a.X + base)[0];
-                    const float4 p1 = reinterpret_cast<const float4 *>(a.X + base)[1];
-                    raw[0] = p0.x; raw[1] = p0.y; raw[2] = p0.z; raw[3] = p0.w;
-                    raw[4] = p1.x; raw[5] = p1.y; raw[6] = p1.z; raw[7] = p1.w;
-                } else {
+        const long long idx = rd * stride + first;
+        if (idx >= total) break;
+        const int t = static_cast<int>(idx / kb_per_t);
+        const int kb = static_cast<int>(idx % kb_per_t);
+        const int kt = kb / 8;
+        const int k8 = kb % 8;
+        float v[8];
+        if (t < a.T) {
+            const float *src = a.X + static_cast<size_t>(t) * a.K + static_cast<size_t>(kb) * 8;
+            const float4 p0 = reinterpret_cast<const float4 *>(src)[0];
+            const float4 p1 = reinterpret_cast<const float4 *>(src)[1];
+            const float raw[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) raw[i] = silu_f32(a.G[base + i]) * a.U[base + i];
-                }
+            for (int p = 0; p < 8; ++p) v[p] = raw[perm8(p)];
+        } else {
 #pragma unroll
-                for (int p = 0; p < 8; ++p) v[p] = raw[perm8(p)];
-            } else {
-#pragma unroll
-                for (int p = 0; p < 8; ++p) v[p] = 0.f;
-            }
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int p = 0; p < 8; p += 2) {
-                const __nv_bfloat16 h0 = __float2bfloat16_rn(v[p]);
-                const __nv_bfloat16 h1 = __float2bfloat16_rn(v[p + 1]);
-                const float r0 = v[p] - __bfloat162float(h0);
-                const float r1 = v[p + 1] - __bfloat162float(h1);
-                const __nv_bfloat16 l0 = __float2bfloat16_rn(r0);
-                const __nv_bfloat16 l1 = __float2bfloat16_rn(r1);
-                part += (__bfloat162float(h0) + __bfloat162float(l0)) + (__bfloat162float(h1) + __bfloat162float(l1));
-                hi[p / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-                            (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-                lo[p / 2] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
-                            (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
-            }
-            uint8_t *blk = a.Bblk + (static_cast<size_t>(t / a.nt) * nkt + kt) * b_bytes(a.nt);
-            const uint32_t off = core_off(t % a.nt, k8);
-            *reinterpret_cast<uint4 *>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-            *reinterpret_cast<uint4 *>(blk + static_cast<size_t>(a.nt) * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+            for (int p = 0; p < 8; ++p) v[p] = 0.f;
         }
-        // the 8 blocks of one (token, K tile) are 8 consecutive threads
-        part += __shfl_xor_sync(FULL_MASK, part, 1);
-        part += __shfl_xor_sync(FULL_MASK, part, 2);
-        part += __shfl_xor_sync(FULL_MASK, part, 4);
-        if (live && (idx % 8) == 0) a.Sx[static_cast<size_t>(kt) * a.Tpad + t] = part;
+        uint32_t hi[4], lo[4];
+        split8(v, hi, lo);
+        uint8_t *blk = a.Bblk + (static_cast<size_t>(t / a.nt) * nkt + kt) * b_bytes(a.nt);
+        const uint32_t off = core_off(t % a.nt, k8);
+        *reinterpret_cast<uint4 *>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(blk + static_cast<size_t>(a.nt) * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
     pdl_launch_dependents();
 }
 
 // ---------------------------------------------------------------- GEMM
 
-struct TcArgs {
-    const uint8_t *codes[2];
+struct alignas(64) TcArgs {
+    CUtensorMap tmap[2];    // codes: gate and up rows (gate/up) or down rows (tmap[0])
     const float *scales[2];
-    float *out[2];  // [T x M] per matrix
-    const uint8_t *Bblk;
-    const float *Sx;
+    const uint8_t *B;       // token operand blocks [ntiles][K/64]
+    float *partial;         // split-K partial sums [mtiles][ntiles][nsplit][NT][MT]
+    unsigned *count;        // [mtiles][ntiles] arrivals of the K splits
+    float *Y;               // down: [T x M]
+    uint8_t *Hb;            // gate/up: down-operand blocks [ntiles][M/64]
     unsigned *status;
-    int M, K, group, T, Tpad;
-    int mtiles;        // 128-row tiles per matrix
-    int kt_per_split;  // K tiles per CTA
-    int atomic;        // K split: accumulate into zeroed outputs
+    int M;                  // rows per matrix (d_ff for gate/up, d_model for down)
+    int K, group, T, ntiles, kps, nsplit;
 };
 
-template <int NT>
-__global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm(const __grid_constant__ TcArgs a)
+template <int NT, bool GU>
+__global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ TcArgs a)
 {
-    constexpr uint32_t NCOLS = (2 * NT) < 32 ? 32 : 2 * NT;  // two accumulator buffers
+    constexpr int NB = accbufs_for(NT);
+    constexpr uint32_t NCOLS = NB * 2 * NT;  // a power of two in [64, 512]
+    constexpr int S = stages_for(NT);
+    constexpr uint32_t SB = stage_bytes(NT);
     extern __shared__ uint8_t smem_raw[];
+    __shared__ int last_split;
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t bars = base + STAGES * stage_bytes(NT);
-    const uint32_t full0 = bars, empty0 = bars + 8 * STAGES, accf0 = bars + 16 * STAGES,
-                   acce0 = accf0 + 16, tslot = acce0 + 16;
+    const uint32_t codes0 = base;                              // CODE_SLOTS chunks, 1024-aligned
+    const uint32_t stage0 = base + CODE_SLOTS * CHUNK_BYTES;   // S stages of A + B
+    const uint32_t bars = stage0 + S * SB;
+    const uint32_t cfull0 = bars, cempty0 = cfull0 + 8 * CODE_SLOTS, full0 = cempty0 + 8 * CODE_SLOTS,
+                   empty0 = full0 + 8 * S, accf0 = empty0 + 8 * S, acce0 = accf0 + 8 * NB, tslot = acce0 + 8 * NB;
     uint32_t *tmem_word = reinterpret_cast<uint32_t *>(smem_raw + (tslot - raw));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m = blockIdx.x / a.mtiles;
-    const int row0 = (blockIdx.x % a.mtiles) * MT;
+    const int mtile = blockIdx.x;
     const int ntile = blockIdx.y;
+    const int split = blockIdx.z;
     const int nkt = a.K / KT;
-    const int kt0 = blockIdx.z * a.kt_per_split;
-    const int kt1 = min(nkt, kt0 + a.kt_per_split);
+    const int kt0 = split * a.kps;
+    const int kt1 = min(nkt, kt0 + a.kps);
     const int nk = kt1 > kt0 ? kt1 - kt0 : 0;
+    const int nchunks = (nk + CHUNK_KT - 1) / CHUNK_KT;
     const int ngroups = a.K / a.group;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full0 + 8 * s, PREP_WARPS + 1);
+        for (int c = 0; c < CODE_SLOTS; ++c) {
+            mbar_init(cfull0 + 8 * c, 1);
+            mbar_init(cempty0 + 8 * c, CONV_WARPS);
+        }
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full0 + 8 * s, CONV_WARPS + 1);
             mbar_init(empty0 + 8 * s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < NB; ++b) {
             mbar_init(accf0 + 8 * b, 1);
             mbar_init(acce0 + 8 * b, EPI_WARPS);
         }
         fence_mbar_init();
     }
-    if (warp == EPI_WARPS + PREP_WARPS) {
+    if (warp == MMA_WARP) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tslot), "r"(NCOLS)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
@@ -273,111 +353,188 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm(const __grid_constant__
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_word;
-    pdl_wait();
 
-    if (warp == EPI_WARPS + PREP_WARPS) {
+    if (warp == CODE_WARP) {
+        // ---- code chunks (weights never depend on an earlier kernel)
+        if (lane == 0) {
+            for (int c = 0; c < nchunks; ++c) {
+                const int slot = c % CODE_SLOTS;
+                if (c >= CODE_SLOTS &&
+                    !mbar_wait_bounded(cempty0 + 8 * slot, ((c / CODE_SLOTS) - 1) & 1, a.status, 7u))
+                    break;
+                const uint32_t dst = codes0 + slot * CHUNK_BYTES;
+                const int x = (kt0 + c * CHUNK_KT) * 32;  // byte offset along the row: multiple of 32
+                mbar_arrive_expect_tx(cfull0 + 8 * slot, CHUNK_BYTES);
+                if (GU) {
+                    tma_load_2d(dst, &a.tmap[0], x, mtile * 64, cfull0 + 8 * slot);
+                    tma_load_2d(dst + CHUNK_BYTES / 2, &a.tmap[1], x, mtile * 64, cfull0 + 8 * slot);
+                } else {
+                    tma_load_2d(dst, &a.tmap[0], x, mtile * MT, cfull0 + 8 * slot);
+                }
+            }
+        }
+    } else if (warp == BPROD_WARP) {
+        // ---- token blocks, produced by the previous kernel
+        pdl_wait();
+        if (lane == 0) {
+            const uint8_t *src = a.B + (static_cast<size_t>(ntile) * nkt + kt0) * b_bytes(NT);
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % S;
+                if (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 8u)) break;
+                mbar_arrive_expect_tx(full0 + 8 * s, b_bytes(NT));
+                bulk_g2s(stage0 + s * SB + A_BYTES, src + static_cast<size_t>(i) * b_bytes(NT), b_bytes(NT),
+                         full0 + 8 * s);
+            }
+        }
+    } else if (warp == MMA_WARP) {
         // ---- MMA issue
         if (lane == 0) {
-            const uint32_t idesc = instr_desc(MT, NT);
+            const uint32_t idesc = instr_desc(MT, 2 * NT);
             for (int i = 0; i < nk; ++i) {
-                const int s = i % STAGES;
-                const int b = i & 1;
-                if (!mbar_wait_bounded(full0 + 8 * s, (i / STAGES) & 1, a.status, 3u)) break;
-                if (i >= 2 && !mbar_wait_bounded(acce0 + 8 * b, ((i >> 1) - 1) & 1, a.status, 4u)) break;
+                const int s = i % S;
+                const int b = i % NB;
+                if (!mbar_wait_bounded(full0 + 8 * s, (i / S) & 1, a.status, 3u)) break;
+                if (i >= NB && !mbar_wait_bounded(acce0 + 8 * b, ((i / NB) - 1) & 1, a.status, 4u)) break;
                 tc_fence_after();
-                const uint32_t sa = base + s * stage_bytes(NT);
+                const uint32_t sa = stage0 + s * SB;
                 const uint32_t sb = sa + A_BYTES;
-                const uint32_t d = tmem + static_cast<uint32_t>(b * NT);
+                const uint32_t d = tmem + static_cast<uint32_t>(b * 2 * NT);
 #pragma unroll
-                for (int part = 0; part < 2; ++part)
-#pragma unroll
-                    for (int kk = 0; kk < KT / 16; ++kk)
-                        mma_bf16(d, smem_desc(sa + kk * 256), smem_desc(sb + part * NT * 128 + kk * 256), idesc,
-                                 (part | kk) != 0);
+                for (int kk = 0; kk < KT / 16; ++kk)
+                    mma_bf16(d, smem_desc(sa + kk * 256), smem_desc(sb + kk * 256), idesc, kk != 0);
                 mma_commit(empty0 + 8 * s);
                 mma_commit(accf0 + 8 * b);
             }
         }
-    } else if (warp >= EPI_WARPS) {
-        // ---- operand preparation: thread pi owns row pi of the tile
-        const int pi = threadIdx.x - EPI_WARPS * 32;
-        const int row = row0 + pi;
-        const bool rok = row < a.M;
-        const size_t row_bytes = static_cast<size_t>(a.K) / 2;
-        const uint8_t *crow = a.codes[m] + static_cast<size_t>(rok ? row : 0) * row_bytes;
-        const uint8_t *bsrc = a.Bblk + static_cast<size_t>(ntile) * nkt * b_bytes(NT);
-        uint4 c0 = make_uint4(0, 0, 0, 0), c1 = c0;
-        if (nk > 0 && rok) {
-            c0 = ldg_u4(crow + static_cast<size_t>(kt0) * 32);
-            c1 = ldg_u4(crow + static_cast<size_t>(kt0) * 32 + 16);
-        }
+    } else if (warp >= CONV_WARP0) {
+        // ---- codes -> A tiles: thread (r, hf) converts words 4 hf .. 4 hf + 3
+        // (8-column blocks k8 = 4 hf .. 4 hf + 3) of tile row r
+        const int ct = threadIdx.x - CONV_WARP0 * 32;
+        const int r = ct & (MT - 1), hf = ct >> 7;
+        const uint32_t rsw = static_cast<uint32_t>(r & 7);  // 128-byte swizzle of the chunk rows
         for (int i = 0; i < nk; ++i) {
-            const int s = i % STAGES;
-            if (i >= STAGES && !mbar_wait_bounded(empty0 + 8 * s, ((i / STAGES) - 1) & 1, a.status, 5u)) break;
-            const uint32_t sa = base + s * stage_bytes(NT);
-            if (pi == 0) {
-                mbar_arrive_expect_tx(full0 + 8 * s, b_bytes(NT));
-                bulk_g2s(sa + A_BYTES, bsrc + static_cast<size_t>(kt0 + i) * b_bytes(NT), b_bytes(NT), full0 + 8 * s);
-            }
-            const uint4 w0 = c0, w1 = c1;
-            if (i + 1 < nk && rok) {  // next tile's codes while this one is unpacked
-                c0 = ldg_u4(crow + static_cast<size_t>(kt0 + i + 1) * 32);
-                c1 = ldg_u4(crow + static_cast<size_t>(kt0 + i + 1) * 32 + 16);
-            }
-            const uint32_t words[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+            const int c = i / CHUNK_KT, sub = i % CHUNK_KT, slot = c % CODE_SLOTS;
+            if (sub == 0 && !mbar_wait_bounded(cfull0 + 8 * slot, (c / CODE_SLOTS) & 1, a.status, 5u)) break;
+            const int s = i % S;
+            if (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 5u)) break;
+            const uint32_t row = codes0 + slot * CHUNK_BYTES + static_cast<uint32_t>(r) * 128u;
+            const uint4 w = lds128v(row + (((2u * sub + static_cast<uint32_t>(hf)) ^ rsw) << 4));
+            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+            const uint32_t sa = stage0 + s * SB;
 #pragma unroll
-            for (int k8 = 0; k8 < 8; ++k8) sts128(sa + core_off(pi, k8), q4_word_to_bf16(rok ? words[k8] : 0u));
+            for (int j = 0; j < 4; ++j) sts128(sa + core_off(r, 4 * hf + j), q4_word_to_bf16(words[j]));
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(full0 + 8 * s);
+            if (lane == 0) {
+                mbar_arrive(full0 + 8 * s);
+                if (sub == CHUNK_KT - 1 || i == nk - 1) mbar_arrive(cempty0 + 8 * slot);
+            }
         }
     } else {
-        // ---- epilogue: warp q reads TMEM lanes 32q..32q+31 (= tile rows)
-        const int r = warp * 32 + lane;
-        const int row = row0 + r;
+        // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (= tile
+        // rows) and columns [h NH, (h + 1) NH) of each accumulator, h = w / 4.
+        // It writes partials, hidden blocks and Y: all after the previous
+        // kernel has completed.
+        pdl_wait();
+        constexpr int NH = NT / 2;
+        const int q = warp & 3, h = warp >> 2;
+        const int r = q * 32 + lane;
+        const int et = h * MT + r;  // 0..255 over the epilogue threads
+        const int mat = GU ? (r >> 6) : 0;
+        const int row = GU ? mtile * 64 + (r & 63) : mtile * MT + r;
         const bool rok = row < a.M;
-        float y[NT];
+        const float *srow = a.scales[mat] + static_cast<size_t>(rok ? row : 0) * ngroups;
+        float y[NH];
 #pragma unroll
-        for (int n = 0; n < NT; ++n) y[n] = 0.f;
-        const float *srow = a.scales[m] + static_cast<size_t>(rok ? row : 0) * ngroups;
+        for (int n = 0; n < NH; ++n) y[n] = 0.f;
+        float sc_next = (rok && nk > 0) ? ldg_f32(srow + (kt0 * KT) / a.group) : 0.f;
         for (int i = 0; i < nk; ++i) {
-            const int b = i & 1;
-            const int kt = kt0 + i;
-            const float sc = rok ? ldg_f32(srow + (kt * KT) / a.group) : 0.f;
-            const bool ok = mbar_wait_bounded(accf0 + 8 * b, (i >> 1) & 1, a.status, 6u);
+            const int b = i % NB;
+            const float f = sc_next * FOLD;
+            if (i + 1 < nk) sc_next = rok ? ldg_f32(srow + ((kt0 + i + 1) * KT) / a.group) : 0.f;
+            const bool ok = mbar_wait_bounded(accf0 + 8 * b, (i / NB) & 1, a.status, 6u);
             if (!__all_sync(FULL_MASK, ok)) break;
             tc_fence_after();
-            float d[NT];
+            // hi columns [c, c + CH) and the matching lo columns, CH at a time
+            constexpr int CH = NH < 16 ? NH : (NH > 32 ? 8 : 16);
+            const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * 2 * NT + h * NH);
 #pragma unroll
-            for (int c = 0; c < NT; c += 16) {
-                float v[16];
-                tmem_ld16(tmem + (static_cast<uint32_t>(warp * 32) << 16) + static_cast<uint32_t>(b * NT + c), v);
+            for (int c = 0; c < NH; c += CH) {
+                float vh[CH], vl[CH];
+                tmem_ld<CH>(tq + c, vh);
+                tmem_ld<CH>(tq + NT + c, vl);
+                tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 16; ++j) d[c + j] = v[j];
+                for (int n = 0; n < CH; ++n) y[c + n] = fmaf(f, vh[n] + vl[n], y[c + n]);
             }
-            tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce0 + 8 * b);
-            const float *sx = a.Sx + static_cast<size_t>(kt) * a.Tpad + static_cast<size_t>(ntile) * NT;
-            const float sa = sc * FOLD_A, sb = sc * (FOLD_A + 1.0f);
+        }
+
+        // ---- K splits: every split stores its partial sums; the last one to
+        // arrive adds all of them in split order and finishes the tile.
+        bool finisher = true;
+        if (a.nsplit > 1) {
+            const size_t tile = static_cast<size_t>(mtile) * a.ntiles + ntile;
+            float *mine = a.partial + (tile * a.nsplit + split) * NT * MT;
 #pragma unroll
-            for (int n = 0; n < NT; n += 4) {
-                const float4 s4 = *reinterpret_cast<const float4 *>(sx + n);
-                y[n + 0] = fmaf(sa, d[n + 0], fmaf(-sb, s4.x, y[n + 0]));
-                y[n + 1] = fmaf(sa, d[n + 1], fmaf(-sb, s4.y, y[n + 1]));
-                y[n + 2] = fmaf(sa, d[n + 2], fmaf(-sb, s4.z, y[n + 2]));
-                y[n + 3] = fmaf(sa, d[n + 3], fmaf(-sb, s4.w, y[n + 3]));
+            for (int n = 0; n < NH; ++n) mine[(h * NH + n) * MT + r] = y[n];
+            __threadfence();
+            named_barrier(1, EPI_WARPS * 32);
+            if (et == 0) last_split = atomicAdd(&a.count[tile], 1u) == static_cast<unsigned>(a.nsplit - 1);
+            named_barrier(1, EPI_WARPS * 32);
+            finisher = last_split != 0;
+            if (finisher) {
+                __threadfence();
+                const float *all = a.partial + tile * a.nsplit * NT * MT;
+#pragma unroll
+                for (int n = 0; n < NH; ++n) y[n] = 0.f;
+                for (int sp = 0; sp < a.nsplit; ++sp)
+#pragma unroll
+                    for (int n = 0; n < NH; ++n)
+                        y[n] += __ldcg(all + (static_cast<size_t>(sp) * NT + h * NH + n) * MT + r);
             }
         }
-        if (rok && nk > 0) {
-            float *o = a.out[m];
+        if (finisher) {
+            if (GU) {
+                // rows 64..127 hold up for the hidden columns of rows 0..63:
+                // exchange through shared memory (the stages are idle now),
+                // then write SiLU(g) * u as the B block of down K tile `mtile`
+                float *xch = reinterpret_cast<float *>(smem_raw + (stage0 - raw));  // [NT][64]
+                if (r >= 64) {
 #pragma unroll
-            for (int n = 0; n < NT; ++n) {
-                const int t = ntile * NT + n;
-                if (t < a.T) {
-                    if (a.atomic) atomicAdd(o + static_cast<size_t>(t) * a.M + row, y[n]);
-                    else o[static_cast<size_t>(t) * a.M + row] = y[n];
+                    for (int n = 0; n < NH; ++n) xch[(h * NH + n) * 64 + (r - 64)] = y[n];
+                }
+                named_barrier(1, EPI_WARPS * 32);
+                if (r < 64) {
+#pragma unroll
+                    for (int n = 0; n < NH; ++n) {
+                        float *p = xch + (h * NH + n) * 64 + r;
+                        *p = silu_f32(y[n]) * *p;
+                    }
+                }
+                named_barrier(1, EPI_WARPS * 32);
+                // work item: (token n, 8-column block k8), NT * 8 of them
+                uint8_t *blk = a.Hb + (static_cast<size_t>(ntile) * (a.M / KT) + mtile) * b_bytes(NT);
+                for (int it = et; it < NT * 8; it += EPI_WARPS * 32) {
+                    const int n = it >> 3, k8 = it & 7;
+                    const int t = ntile * NT + n;
+                    float v[8];
+#pragma unroll
+                    for (int p = 0; p < 8; ++p) v[p] = t < a.T ? xch[n * 64 + k8 * 8 + perm8(p)] : 0.f;
+                    uint32_t hi[4], lo[4];
+                    split8(v, hi, lo);
+                    const uint32_t off = core_off(n, k8);
+                    *reinterpret_cast<uint4 *>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(blk + static_cast<size_t>(NT) * 128 + off) =
+                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                }
+            } else if (rok) {
+#pragma unroll
+                for (int n = 0; n < NH; ++n) {
+                    const int t = ntile * NT + h * NH + n;
+                    if (t < a.T) a.Y[static_cast<size_t>(t) * a.M + row] = y[n];
                 }
             }
         }
@@ -385,76 +542,119 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_gemm(const __grid_constant__
     tc_fence_before();
     __syncthreads();
     if (threadIdx.x == 0) pdl_launch_dependents();
-    if (warp == EPI_WARPS + PREP_WARPS) {
+    if (warp == MMA_WARP) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOLS) : "memory");
     }
 }
 
-int pick_nt(int T) { return T > 32 ? 64 : (T > 16 ? 32 : 16); }
+// ---------------------------------------------------------------- host side
+
+int pick_nt(int T) { return T > 64 ? 128 : (T > 32 ? 64 : (T > 16 ? 32 : 16)); }
 
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
-struct TcLayout {
-    int nt, Tpad;
-    size_t xb, sx, g, u, hb, sh, total;
+struct GemmPlan {
+    int mtiles, kps, nsplit;
 };
 
-TcLayout tc_layout(int T, int d_model, int d_ff)
+// K splits so that mtiles * ntiles * splits fills about one wave of SMs.
+GemmPlan plan_gemm(int mtiles, int ntiles, int nkt, int sms)
+{
+    GemmPlan p = {mtiles, nkt, 1};
+    const int base = mtiles * ntiles;
+    int maxs = sms / (base > 0 ? base : 1);
+    if (maxs < 1) maxs = 1;
+    if (maxs > nkt) maxs = nkt;
+    p.kps = (nkt + maxs - 1) / maxs;
+    p.nsplit = (nkt + p.kps - 1) / p.kps;
+    return p;
+}
+
+struct TcLayout {
+    int nt, ntiles;
+    GemmPlan gu, dn;
+    size_t xb, hb, pgu, pdn, cnt, total;
+};
+
+int sizing_sms()
+{
+    const DeviceInfo *dev = device_info();
+    return dev && dev->sm_count > 0 ? dev->sm_count : 152;
+}
+
+TcLayout tc_layout(int T, int d_model, int d_ff, int sms)
 {
     TcLayout L = {};
     L.nt = pick_nt(T);
-    L.Tpad = (T + L.nt - 1) / L.nt * L.nt;
+    L.ntiles = (T + L.nt - 1) / L.nt;
+    L.gu = plan_gemm(d_ff / KT, L.ntiles, d_model / KT, sms);
+    L.dn = plan_gemm((d_model + MT - 1) / MT, L.ntiles, d_ff / KT, sms);
+    const size_t tile_f = static_cast<size_t>(L.nt) * MT * sizeof(float);
     size_t off = 0;
-    L.xb = off; off = align256(off + static_cast<size_t>(L.Tpad) * d_model * 4);
-    L.sx = off; off = align256(off + static_cast<size_t>(d_model / KT) * L.Tpad * 4);
-    L.g = off;  off = align256(off + static_cast<size_t>(T) * d_ff * 4);
-    L.u = off;  off = align256(off + static_cast<size_t>(T) * d_ff * 4);
-    L.hb = off; off = align256(off + static_cast<size_t>(L.Tpad) * d_ff * 4);
-    L.sh = off; off = align256(off + static_cast<size_t>(d_ff / KT) * L.Tpad * 4);
+    L.xb = off; off = align256(off + static_cast<size_t>(L.ntiles) * (d_model / KT) * b_bytes(L.nt));
+    L.hb = off; off = align256(off + static_cast<size_t>(L.ntiles) * (d_ff / KT) * b_bytes(L.nt));
+    L.pgu = off;
+    if (L.gu.nsplit > 1) off = align256(off + static_cast<size_t>(L.gu.mtiles) * L.ntiles * L.gu.nsplit * tile_f);
+    L.pdn = off;
+    if (L.dn.nsplit > 1) off = align256(off + static_cast<size_t>(L.dn.mtiles) * L.ntiles * L.dn.nsplit * tile_f);
+    L.cnt = off; off = align256(off + static_cast<size_t>(L.gu.mtiles + L.dn.mtiles) * L.ntiles * sizeof(unsigned));
     L.total = off;
     return L;
 }
 
-template <int NT>
-cudaError_t launch_gemm(TcArgs a, int nmat, int ntiles, int sms, cudaStream_t stream)
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encoder()
 {
-    const int nkt = a.K / KT;
-    const int base_ctas = nmat * a.mtiles * ntiles;
-    int ks = sms / (base_ctas > 0 ? base_ctas : 1);
-    if (ks < 1) ks = 1;
-    if (ks > nkt) ks = nkt;
-    a.kt_per_split = (nkt + ks - 1) / ks;
-    ks = (nkt + a.kt_per_split - 1) / a.kt_per_split;
-    a.atomic = ks > 1;
-    if (a.atomic) {
-        for (int i = 0; i < nmat; ++i) {
-            cudaError_t e = cudaMemsetAsync(a.out[i], 0, static_cast<size_t>(a.T) * a.M * sizeof(float), stream);
-            if (e != cudaSuccess) return e;
-        }
-    }
-    const size_t smem = 1024 + STAGES * stage_bytes(NT) + 256;
-    auto k = tc_gemm<NT>;
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    });
+    return fn;
+}
+
+// Tensor map of packed Q4 codes [rows x K/2 bytes]: boxes of box_rows rows x
+// 128 bytes (4 K tiles), 128-byte swizzle, zero fill outside the matrix.
+bool encode_codes(CUtensorMap *map, const uint8_t *codes, int rows, int K, int box_rows)
+{
+    EncodeTiled fn = encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int NT, bool GU>
+cudaError_t launch_gemm(const TcArgs &a, int mtiles, cudaStream_t stream)
+{
+    const size_t smem = 1024 + CODE_SLOTS * CHUNK_BYTES + static_cast<size_t>(stages_for(NT)) * stage_bytes(NT) +
+                        512;
+    auto k = tc_ffn<NT, GU>;
     cudaError_t e = ensure_dynamic_smem(k, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, dim3(nmat * a.mtiles, ntiles, ks), dim3(TC_THREADS), smem, stream, a);
+    return launch_pdl(k, dim3(mtiles, a.ntiles, a.nsplit), dim3(TC_THREADS), smem, stream, a);
 }
 
-cudaError_t launch_gemm_nt(int nt, const TcArgs &a, int nmat, int ntiles, int sms, cudaStream_t stream)
+template <bool GU>
+cudaError_t launch_gemm_nt(int nt, const TcArgs &a, int mtiles, cudaStream_t stream)
 {
-    if (nt == 64) return launch_gemm<64>(a, nmat, ntiles, sms, stream);
-    if (nt == 32) return launch_gemm<32>(a, nmat, ntiles, sms, stream);
-    return launch_gemm<16>(a, nmat, ntiles, sms, stream);
-}
-
-cudaError_t launch_prep(PrepArgs p, int sms, cudaStream_t stream)
-{
-    const long long total = static_cast<long long>(p.Tpad) * (p.K / 8);
-    long long blocks = (total + 255) / 256;
-    const long long cap = static_cast<long long>(sms) * 8;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    return launch_pdl(prep_b, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
+    if (nt == 128) return launch_gemm<128, GU>(a, mtiles, stream);
+    if (nt == 64) return launch_gemm<64, GU>(a, mtiles, stream);
+    if (nt == 32) return launch_gemm<32, GU>(a, mtiles, stream);
+    return launch_gemm<16, GU>(a, mtiles, stream);
 }
 
 }  // namespace
@@ -466,7 +666,8 @@ bool tc_batch_supported(int T, int d_model, int d_ff, int group)
 
 size_t tc_batch_workspace(int T, int d_model, int d_ff)
 {
-    return tc_layout(T, d_model, d_ff).total;
+    const int sms = sizing_sms();
+    return tc_layout(T, d_model, d_ff, sms < 152 ? 152 : sms).total;
 }
 
 cudaError_t launch_ffn_batch_tc(const uint8_t *const gu_codes[2], const float *const gu_scales[2],
@@ -475,49 +676,65 @@ cudaError_t launch_ffn_batch_tc(const uint8_t *const gu_codes[2], const float *c
 {
     const DeviceInfo *dev = device_info();
     if (!dev) return cudaErrorInvalidDevice;
-    const TcLayout L = tc_layout(T, d_model, d_ff);
+    if (!encoder()) return cudaErrorNotSupported;
+    const TcLayout L = tc_layout(T, d_model, d_ff, dev->sm_count);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    float *G = reinterpret_cast<float *>(ws + L.g);
-    float *U = reinterpret_cast<float *>(ws + L.u);
-    const int ntiles = L.Tpad / L.nt;
+    unsigned *cnt = reinterpret_cast<unsigned *>(ws + L.cnt);
+    const int ncount = (L.gu.mtiles + L.dn.mtiles) * L.ntiles;
 
-    PrepArgs p = {X, nullptr, nullptr, ws + L.xb, reinterpret_cast<float *>(ws + L.sx), T, L.Tpad, d_model, L.nt, 0};
-    cudaError_t e = launch_prep(p, dev->sm_count, stream);
-    if (e != cudaSuccess) return e;
+    PrepArgs p = {X, ws + L.xb, cnt, ncount, T, d_model, L.nt, L.ntiles};
+    {
+        const long long total = static_cast<long long>(L.ntiles) * L.nt * (d_model / 8);
+        long long blocks = (total + 255) / 256;
+        const long long cap = static_cast<long long>(dev->sm_count) * 8;
+        if (blocks > cap) blocks = cap;
+        const long long need = (ncount + 255) / 256;
+        if (blocks < need) blocks = need;
+        if (blocks < 1) blocks = 1;
+        cudaError_t e = launch_pdl(prep_tokens, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
+        if (e != cudaSuccess) return e;
+    }
 
     TcArgs a = {};
-    a.codes[0] = gu_codes[0];
-    a.codes[1] = gu_codes[1];
+    if (!encode_codes(&a.tmap[0], gu_codes[0], d_ff, d_model, 64) ||
+        !encode_codes(&a.tmap[1], gu_codes[1], d_ff, d_model, 64))
+        return cudaErrorInvalidValue;
     a.scales[0] = gu_scales[0];
     a.scales[1] = gu_scales[1];
-    a.out[0] = G;
-    a.out[1] = U;
-    a.Bblk = ws + L.xb;
-    a.Sx = reinterpret_cast<const float *>(ws + L.sx);
+    a.B = ws + L.xb;
+    a.partial = reinterpret_cast<float *>(ws + L.pgu);
+    a.count = cnt;
+    a.Y = nullptr;
+    a.Hb = ws + L.hb;
     a.status = device_status_word();
     a.M = d_ff;
     a.K = d_model;
     a.group = group;
     a.T = T;
-    a.Tpad = L.Tpad;
-    a.mtiles = (d_ff + MT - 1) / MT;
-    e = launch_gemm_nt(L.nt, a, 2, ntiles, dev->sm_count, stream);
+    a.ntiles = L.ntiles;
+    a.kps = L.gu.kps;
+    a.nsplit = L.gu.nsplit;
+    cudaError_t e = launch_gemm_nt<true>(L.nt, a, L.gu.mtiles, stream);
     if (e != cudaSuccess) return e;
 
-    PrepArgs q = {nullptr, G, U, ws + L.hb, reinterpret_cast<float *>(ws + L.sh), T, L.Tpad, d_ff, L.nt, 1};
-    e = launch_prep(q, dev->sm_count, stream);
-    if (e != cudaSuccess) return e;
-
-    TcArgs b = a;
-    b.codes[0] = b.codes[1] = down_codes;
+    TcArgs b = {};
+    if (!encode_codes(&b.tmap[0], down_codes, d_model, d_ff, MT)) return cudaErrorInvalidValue;
+    b.tmap[1] = b.tmap[0];
     b.scales[0] = b.scales[1] = down_scales;
-    b.out[0] = b.out[1] = Y;
-    b.Bblk = ws + L.hb;
-    b.Sx = reinterpret_cast<const float *>(ws + L.sh);
+    b.B = ws + L.hb;
+    b.partial = reinterpret_cast<float *>(ws + L.pdn);
+    b.count = cnt + static_cast<size_t>(L.gu.mtiles) * L.ntiles;
+    b.Y = Y;
+    b.Hb = nullptr;
+    b.status = a.status;
     b.M = d_model;
     b.K = d_ff;
-    b.mtiles = (d_model + MT - 1) / MT;
-    return launch_gemm_nt(L.nt, b, 1, ntiles, dev->sm_count, stream);
+    b.group = group;
+    b.T = T;
+    b.ntiles = L.ntiles;
+    b.kps = L.dn.kps;
+    b.nsplit = L.dn.nsplit;
+    return launch_gemm_nt<false>(L.nt, b, L.dn.mtiles, stream);
 }
 
 }  // namespace smoe
