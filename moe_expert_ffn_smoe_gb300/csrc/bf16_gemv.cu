@@ -1,12 +1,18 @@
 // Dense bf16 matvec y = W x (f32 x and y), the S-MoE page "Metal Compute
 // Kernels", section "Coalesced Dense Matvec -- the Same Contract for bf16".
 //
-// GB300 layout: one warp per output row at a time; each lane reads 16-byte
-// chunks (8 bf16) of the row, SEG chunks per lane per step, all issued before
-// any is used.  A CTA owns a contiguous range of rows and bulk-prefetches the
-// head of that range into L2 before waiting on the previous kernel.  x is
-// staged once per CTA in swizzled shared memory.  A bf16 is the upper half
-// of an f32, so widening is a shift or a mask: no conversion instruction.
+// GB300 layout: a CTA owns a contiguous block of rows (the blocks differ by
+// at most one row) and all its 512 threads work on every row together:
+// thread t reads the 16-byte chunks t, t + 512, ... (8 bf16 each) of the
+// row, so every row is one fully coalesced sweep and no warp idles while
+// others finish.  Rows are processed in groups of G (8 / chunks per
+// thread, at least 2): the loads of the next group are in flight while the
+// current group is multiplied.  x is staged in shared memory once per CTA;
+// for rows of up to 8192 columns each thread keeps the x values of its
+// chunks in registers.  A bf16 is the upper half of an f32, so widening is
+// a shift or a mask.  Per row, the 512 partial sums are reduced with warp
+// shuffles and one shared-memory step.  The CTA prefetches the head of its
+// row block into L2 before waiting on the previous kernel.
 #include "common.cuh"
 #include "internal.h"
 
@@ -18,20 +24,24 @@ struct Bf16Args {
     float *y;
     int rows;
     int K;
-    uint32_t prefetch_bytes;  // per CTA, from the start of its row range
+    uint32_t prefetch_bytes;  // per CTA, from the start of its row block
 };
 
-// float4 slot of logical float4 q of x (bijection inside aligned blocks of
-// eight float4s; lanes reading chunk = base + lane land in distinct banks).
-__device__ __forceinline__ int bx_slot(int q) { return q ^ ((q >> 3) & 7); }
+constexpr int BF_THREADS = 512;
+constexpr int BF_WARPS = BF_THREADS / 32;
+constexpr int BF_GMAX = 8;
 
-template <int SEG>
-__global__ void __launch_bounds__(512) bf16_gemv(Bf16Args a)
+// CPL: 16-byte chunks per thread per row (K <= CPL * 512 * 8).
+template <int CPL>
+__global__ void __launch_bounds__(BF_THREADS, 1) bf16_gemv(Bf16Args a)
 {
+    constexpr int BF_G = 8 / CPL > 2 ? 8 / CPL : 2;  // rows per group
+    constexpr bool XREG = CPL <= 2;                 // x of the thread's chunks in registers
     extern __shared__ __align__(16) float4 xs[];
-    const int lane = threadIdx.x & 31;
-    const int warp = threadIdx.x >> 5;
-    const int nwarps = blockDim.x >> 5;
+    __shared__ float part[2][BF_WARPS][BF_GMAX];
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    const int warp = t >> 5;
     const int KC = a.K >> 3;  // 16-byte chunks per row
     const size_t row_elems = static_cast<size_t>(a.K);
 
@@ -46,49 +56,95 @@ __global__ void __launch_bounds__(512) bf16_gemv(Bf16Args a)
 
     pdl_wait();
     const int nq = a.K >> 2;
-    for (int q = threadIdx.x; q < nq; q += blockDim.x)
-        xs[bx_slot(q)] = reinterpret_cast<const float4 *>(a.x)[q];
+    for (int q = t; q < nq; q += BF_THREADS) xs[q] = reinterpret_cast<const float4 *>(a.x)[q];
     __syncthreads();
     pdl_launch_dependents();
 
-    // chunk cc = base + lane (base a multiple of 32) covers float4s 2cc, 2cc+1;
-    // their slots are 2*base + ((2*lane + h) ^ ((lane >> 2) & 7)).
-    const uint32_t xs_base = smem_addr(xs);
-    const uint32_t xo0 = xs_base + static_cast<uint32_t>(((2 * lane) ^ ((lane >> 2) & 7)) * 16);
-    const uint32_t xo1 = xs_base + static_cast<uint32_t>(((2 * lane + 1) ^ ((lane >> 2) & 7)) * 16);
+    // this thread's x for its chunks (zero past the row)
+    auto x_of = [&](int j, float (&v)[8]) {
+        const int cc = t + BF_THREADS * j;
+        if (cc < KC) {
+            const float4 x0 = xs[2 * cc], x1 = xs[2 * cc + 1];
+            v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+            v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = 0.f;
+        }
+    };
+    float xv[XREG ? CPL : 1][8];
+#pragma unroll
+    for (int j = 0; j < (XREG ? CPL : 1); ++j) x_of(j, xv[j]);
 
-    for (int row = r0 + warp; row < r1; row += nwarps) {
-        const uint16_t *wrow = a.w + static_cast<size_t>(row) * row_elems;
-        float acc0 = 0.f, acc1 = 0.f;
-        for (int base = 0; base < KC; base += 32 * SEG) {
-            uint4 c[SEG];
+    // loads of one group: rows r .. r + G - 1 (rows past r1 read row r1 - 1)
+    auto load_group = [&](int r, uint4 (&c)[BF_G][CPL]) {
 #pragma unroll
-            for (int j = 0; j < SEG; ++j) {
-                const int cc = base + lane + 32 * j;
-                c[j] = cc < KC ? ldg_stream(wrow + static_cast<size_t>(cc) * 8) : make_uint4(0, 0, 0, 0);
-            }
+        for (int g = 0; g < BF_G; ++g) {
+            const int row = min(r + g, r1 - 1);
+            const uint16_t *wrow = a.w + static_cast<size_t>(row) * row_elems;
 #pragma unroll
-            for (int j = 0; j < SEG; ++j) {
-                const int cb = base + 32 * j;  // chunk index of lane 0
-                if (cb + lane < KC) {
-                    const uint32_t off = static_cast<uint32_t>(cb) * 32u;  // 2*cb float4s
-                    const float4 x0 = lds128(xo0 + off);
-                    const float4 x1 = lds128(xo1 + off);
-                    acc0 = fmaf(__uint_as_float(c[j].x << 16), x0.x, acc0);
-                    acc1 = fmaf(__uint_as_float(c[j].x & 0xffff0000u), x0.y, acc1);
-                    acc0 = fmaf(__uint_as_float(c[j].y << 16), x0.z, acc0);
-                    acc1 = fmaf(__uint_as_float(c[j].y & 0xffff0000u), x0.w, acc1);
-                    acc0 = fmaf(__uint_as_float(c[j].z << 16), x1.x, acc0);
-                    acc1 = fmaf(__uint_as_float(c[j].z & 0xffff0000u), x1.y, acc1);
-                    acc0 = fmaf(__uint_as_float(c[j].w << 16), x1.z, acc0);
-                    acc1 = fmaf(__uint_as_float(c[j].w & 0xffff0000u), x1.w, acc1);
-                }
+            for (int j = 0; j < CPL; ++j) {
+                const int cc = t + BF_THREADS * j;
+                c[g][j] = cc < KC ? ldg_stream(wrow + static_cast<size_t>(cc) * 8) : make_uint4(0, 0, 0, 0);
             }
         }
-        float acc = acc0 + acc1;
+    };
+
+    uint4 cur[BF_G][CPL], nxt[BF_G][CPL];
+    if (r0 < r1) load_group(r0, cur);
+    int buf = 0;
+    for (int r = r0; r < r1; r += BF_G) {
+        if (r + BF_G < r1) load_group(r + BF_G, nxt);
+        float s[BF_G];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(FULL_MASK, acc, off);
-        if (lane == 0) a.y[row] = acc;
+        for (int g = 0; g < BF_G; ++g) {
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) {
+                const uint4 c = cur[g][j];
+                float xl[8];
+                if (XREG) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) xl[k] = xv[XREG ? j : 0][k];
+                } else {
+                    x_of(j, xl);
+                }
+                a0 = fmaf(__uint_as_float(c.x << 16), xl[0], a0);
+                a1 = fmaf(__uint_as_float(c.x & 0xffff0000u), xl[1], a1);
+                a0 = fmaf(__uint_as_float(c.y << 16), xl[2], a0);
+                a1 = fmaf(__uint_as_float(c.y & 0xffff0000u), xl[3], a1);
+                a0 = fmaf(__uint_as_float(c.z << 16), xl[4], a0);
+                a1 = fmaf(__uint_as_float(c.z & 0xffff0000u), xl[5], a1);
+                a0 = fmaf(__uint_as_float(c.w << 16), xl[6], a0);
+                a1 = fmaf(__uint_as_float(c.w & 0xffff0000u), xl[7], a1);
+            }
+            s[g] = a0 + a1;
+        }
+        // warp sums of the G rows (butterfly: every lane ends with each sum);
+        // lane g keeps row g's, then one thread per row adds the 16 warps'
+#pragma unroll
+        for (int g = 0; g < BF_G; ++g)
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) s[g] += __shfl_xor_sync(FULL_MASK, s[g], off);
+        if (lane < BF_G) {
+            float v = s[0];
+#pragma unroll
+            for (int g = 1; g < BF_G; ++g)
+                if (lane == g) v = s[g];
+            part[buf][warp][lane] = v;
+        }
+        __syncthreads();
+        if (t < BF_G && r + t < r1) {
+            float v = 0.f;
+#pragma unroll
+            for (int w2 = 0; w2 < BF_WARPS; ++w2) v += part[buf][w2][t];
+            a.y[r + t] = v;
+        }
+        buf ^= 1;
+#pragma unroll
+        for (int g = 0; g < BF_G; ++g)
+#pragma unroll
+            for (int j = 0; j < CPL; ++j) cur[g][j] = nxt[g][j];
     }
 }
 
@@ -97,22 +153,31 @@ cudaError_t launch_bf16_gemv(const uint16_t *w, const float *x, float *y, int ro
 {
     const DeviceInfo *dev = device_info();
     if (!dev) return cudaErrorInvalidDevice;
-    constexpr int SEG = 8;
     Bf16Args a = {w, x, y, rows, K, 0};
-    // Shared memory rounded up to whole blocks of eight float4s (the swizzle
-    // permutes inside such blocks).
-    const size_t smem = ((static_cast<size_t>(K) / 4 + 7) / 8) * 8 * sizeof(float4);
-    const int warps = 16;
+    const int KC = K / 8;
+    int cpl = (KC + BF_THREADS - 1) / BF_THREADS;
+    if (cpl < 1) cpl = 1;  // K = 0: every chunk reads as zero, y = 0
+    const size_t smem = static_cast<size_t>(K > 0 ? K : 4) * sizeof(float);
     long long grid = dev->sm_count;
-    const long long by_rows = (static_cast<long long>(rows) + 3) / 4;  // >= 4 rows per CTA
-    if (by_rows < grid) grid = by_rows < 1 ? 1 : by_rows;
+    if (rows < grid) grid = rows < 1 ? 1 : rows;
     // Prefetch at most 1/4 of L2's worth across the grid.
     const size_t l2_share = static_cast<size_t>(32u << 20) / static_cast<size_t>(grid);
     a.prefetch_bytes = static_cast<uint32_t>(l2_share < (1u << 20) ? l2_share : (1u << 20));
-    auto k = bf16_gemv<SEG>;
+    void (*k)(Bf16Args) = nullptr;
+    switch (cpl) {
+    case 1: k = bf16_gemv<1>; break;
+    case 2: k = bf16_gemv<2>; break;
+    case 3: k = bf16_gemv<3>; break;
+    case 4: k = bf16_gemv<4>; break;
+    case 5: k = bf16_gemv<5>; break;
+    case 6: k = bf16_gemv<6>; break;
+    case 7: k = bf16_gemv<7>; break;
+    case 8: k = bf16_gemv<8>; break;
+    default: return cudaErrorInvalidValue;  // K > SMOE_MAX_COLS is refused earlier
+    }
     cudaError_t e = ensure_dynamic_smem(k, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, dim3(static_cast<unsigned>(grid)), dim3(warps * 32), smem, stream, a);
+    return launch_pdl(k, dim3(static_cast<unsigned>(grid)), dim3(BF_THREADS), smem, stream, a);
 }
 
 }  // namespace smoe
