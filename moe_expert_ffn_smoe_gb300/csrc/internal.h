@@ -96,14 +96,16 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
-// Opts a kernel into more than 48 KB of dynamic shared memory when needed.
-// The limit is only ever raised: one kernel serves launches of different
-// shared-memory sizes, and a launch captured earlier into a graph must stay
-// valid after a later, smaller launch of the same kernel.
+// Opts a kernel into `bytes` of dynamic shared memory.  Static shared memory
+// counts against the default 48 KB too, so the limit is raised for any
+// nonzero size it does not already cover.  It is only ever raised: one
+// kernel serves launches of different shared-memory sizes, and a launch
+// captured earlier into a graph must stay valid after a later, smaller
+// launch of the same kernel.
 template <typename K>
 cudaError_t ensure_dynamic_smem(K kernel, size_t bytes)
 {
-    if (bytes <= 48 * 1024) return cudaSuccess;
+    if (bytes == 0) return cudaSuccess;
     cudaFuncAttributes fa;
     cudaError_t err = cudaFuncGetAttributes(&fa, reinterpret_cast<const void *>(kernel));
     if (err != cudaSuccess) return err;

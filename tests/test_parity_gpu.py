@@ -191,7 +191,13 @@ def test_unpack_probes_gate_up(smoe, dev, bits):
 
 # ---------------------------------------------------------------- bf16
 
-@pytest.mark.parametrize("rows,cols,seed", [(8192, 4096, 1), (4096, 8192, 2), (512, 4096, 3)])
+@pytest.mark.parametrize("rows,cols,seed", [
+    (8192, 4096, 1), (4096, 8192, 2), (512, 4096, 3),
+    (3, 8, 11),          # one 16-byte chunk per row, fewer rows than SMs
+    (200, 32768, 12),    # the widest rows: 8 chunks per thread, x read from shared memory
+    (777, 4104, 13),     # a ragged last chunk round (513 chunks per row)
+    (100, 12288, 14),    # 3 chunks per thread
+])
 def test_bf16_full(smoe, dev, rows, cols, seed):
     w = inp.bf16_rows(rows, cols, seed, 1)
     x = inp.activations(cols, seed)
@@ -246,8 +252,10 @@ def _batch(smoe, dev, T, e, X, d_model, d_ff, group):
     return Y.cpu().numpy()[:T]
 
 
-@pytest.mark.parametrize("T", [1, 3, 16, 64, 256])
+@pytest.mark.parametrize("T", [1, 3, 16, 32, 64, 100, 200, 256])
 def test_token_batch(smoe, dev, T):
+    """Token tiles of 16, 32, 64 and 128 tokens; 100 and 200 leave a
+    partly padded last tile."""
     d_model, d_ff, group = 4096, 1536, 64
     e = inp.expert(4, d_model, d_ff, group, seed=7)
     X = inp.activations((T, d_model), 7)
@@ -270,6 +278,20 @@ def test_token_batch_small_shape_all_tokens(smoe, dev):
             e["down_codes"], e["down_scales"])
     _, ref, a = oracle.ffn_batch(*args, T, d_model, d_ff, group, X.astype(np.float64))
     check(Y, ref, a, "batch 256/512 T=13")
+
+
+@pytest.mark.parametrize("d_model,d_ff,group,T", [
+    (320, 192, 64, 20),    # code chunks and the last down row tile run past the matrix
+    (512, 256, 128, 70),   # groups of 128 columns: one scale per two K tiles
+])
+def test_token_batch_ragged_shapes(smoe, dev, d_model, d_ff, group, T):
+    e = inp.expert(4, d_model, d_ff, group, seed=31)
+    X = inp.activations((T, d_model), 31)
+    Y = _batch(smoe, dev, T, e, X, d_model, d_ff, group)
+    args = (4, e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"],
+            e["down_codes"], e["down_scales"])
+    _, ref, a = oracle.ffn_batch(*args, T, d_model, d_ff, group, X.astype(np.float64))
+    check(Y, ref, a, f"batch {d_model}/{d_ff} g{group} T={T}")
 
 
 # ------------------------------------------------------ ragged and edge cases
