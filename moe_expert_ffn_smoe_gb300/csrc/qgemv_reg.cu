@@ -12,15 +12,24 @@
 // shared-memory slots filled by cp.async.bulk and waits only on its own.
 // The bulk copies of a stage are issued by up to four lanes at once (codes
 // and scales of each matrix).
+//
+// Row split (H > 1): every row is cut into H parts of K / H columns; part h
+// of row i is "virtual row" i H + h, so a matrix reads as H times as many
+// rows of K / H columns with the same bytes in the same places.  Warp w
+// only ever streams virtual rows with h = w % H (one row per stage, NW a
+// multiple of H), so its lanes hold the digits of 1 / H of x: the CTA runs
+// 16 warps instead of 12.  Parts of a row are summed in shared memory after
+// the last stage, then SiLU(gate) * up is applied.
 #include "regdot.cuh"
 
 namespace smoe {
 
 namespace {
 
-template <int BITS, int NMAT, int L, int CPL, int RPT>
-__global__ void __launch_bounds__(384, 1) qgemv_reg(const __grid_constant__ QGArgs a)
+template <int BITS, int NMAT, int L, int CPL, int RPT, int H>
+__global__ void __launch_bounds__(H == 1 ? 384 : 512, 1) qgemv_reg(const __grid_constant__ QGArgs a)
 {
+    static_assert(H == 1 || (L == 32 && RPT == 1), "row split streams one row per stage");
     using RD = RegDot<BITS, NMAT, L, CPL, RPT>;
     constexpr int TEAMS = RD::TEAMS;
     constexpr int R = RD::R;                   // rows of each matrix per stage
@@ -37,16 +46,18 @@ __global__ void __launch_bounds__(384, 1) qgemv_reg(const __grid_constant__ QGAr
     const int NW = blockDim.x >> 5;
     const int e = blockIdx.x / a.ctas_per_expert;
     const int bi = blockIdx.x - e * a.ctas_per_expert;
-    const int u0 = static_cast<int>(static_cast<long long>(a.units) * bi / a.ctas_per_expert);
-    const int u1 = static_cast<int>(static_cast<long long>(a.units) * (bi + 1) / a.ctas_per_expert);
+    const int r0 = static_cast<int>(static_cast<long long>(a.units) * bi / a.ctas_per_expert);
+    const int r1 = static_cast<int>(static_cast<long long>(a.units) * (bi + 1) / a.ctas_per_expert);
+    const int u0 = r0 * H, u1 = r1 * H;  // virtual rows (H == 1: the rows)
     const int nst = (u1 - u0 + R - 1) / R;
     const int my = warp < nst ? (nst - warp + NW - 1) / NW : 0;  // stages of this warp
-    const int ngroups = a.K / a.group;
+    const int ngroups = a.K / a.group / H;  // groups of a virtual row
     const int ns = a.ns;
     const uint32_t bars = sbase + a.off_bars + static_cast<uint32_t>(warp * ns) * 8u;
     const uint32_t slots = sbase + a.off_slots + static_cast<uint32_t>(warp * ns) * a.stage_bytes;
     const uint32_t scales_off = static_cast<uint32_t>(NMAT * R) * ROW_BYTES;
     const uint32_t sbytes_row = static_cast<uint32_t>(ngroups) * 4u;  // scales travel with the codes
+    float *part = reinterpret_cast<float *>(smem + a.off_part);    // H > 1: [u1 - u0][NMAT]
 
     // Copy roles: lanes 0..NMAT-1 the codes of matrix `lane`, lanes
     // NMAT..2 NMAT-1 the scales of matrix `lane - NMAT`.  src0 is this lane's source for the warp's first
@@ -107,7 +118,8 @@ __global__ void __launch_bounds__(384, 1) qgemv_reg(const __grid_constant__ QGAr
 
     // This lane's digits, q / Z, q * Sxq and scale offsets, for good.
     RD rd;
-    rd.load(sbase, a.off_info, u);
+    const int h = H == 1 ? 0 : warp % H;
+    rd.load(sbase, a.off_info, u, h * RD::KC, h * ngroups);
 
     int k = 0, si = 0;
     uint32_t phase = 0;
@@ -130,9 +142,14 @@ __global__ void __launch_bounds__(384, 1) qgemv_reg(const __grid_constant__ QGAr
             for (int r = 0; r < RPT; ++r) {
                 const int ul = r * TEAMS + team;
                 if (us + ul < u1) {
-                    float out = acc[0][r];
-                    if (NMAT == 2) out = silu_f32(acc[0][r]) * acc[NMAT - 1][r];
-                    a.y[e][us + ul] = out;
+                    if (H > 1) {
+#pragma unroll
+                        for (int m = 0; m < NMAT; ++m) part[(us + ul - u0) * NMAT + m] = acc[m][r];
+                    } else {
+                        float out = acc[0][r];
+                        if (NMAT == 2) out = silu_f32(acc[0][r]) * acc[NMAT - 1][r];
+                        a.y[e][us + ul] = out;
+                    }
                 }
             }
         }
@@ -154,16 +171,31 @@ __global__ void __launch_bounds__(384, 1) qgemv_reg(const __grid_constant__ QGAr
             }
         }
     }
+    if (H > 1) {
+        // every warp has stored its parts (a warp that gave up left garbage
+        // and recorded the failure): add the parts of each row
+        __syncthreads();
+        for (int i = threadIdx.x; i < r1 - r0; i += blockDim.x) {
+            float v[NMAT];
+#pragma unroll
+            for (int m = 0; m < NMAT; ++m) {
+                v[m] = 0.f;
+#pragma unroll
+                for (int p = 0; p < H; ++p) v[m] += part[(i * H + p) * NMAT + m];
+            }
+            a.y[e][r0 + i] = NMAT == 2 ? silu_f32(v[0]) * v[NMAT - 1] : v[0];
+        }
+    }
 }
 
 template <int BITS, int NMAT, int L, int RPT>
 QGKernelFn pick_cpl(int cpl)
 {
     switch (cpl) {
-    case 1: return qgemv_reg<BITS, NMAT, L, 1, RPT>;
-    case 2: return qgemv_reg<BITS, NMAT, L, 2, RPT>;
-    case 3: return BITS == 4 ? qgemv_reg<BITS, NMAT, L, (BITS == 4 ? 3 : 1), RPT> : nullptr;
-    case 4: return BITS == 4 ? qgemv_reg<BITS, NMAT, L, (BITS == 4 ? 4 : 1), RPT> : nullptr;
+    case 1: return qgemv_reg<BITS, NMAT, L, 1, RPT, 1>;
+    case 2: return qgemv_reg<BITS, NMAT, L, 2, RPT, 1>;
+    case 3: return BITS == 4 ? qgemv_reg<BITS, NMAT, L, (BITS == 4 ? 3 : 1), RPT, 1> : nullptr;
+    case 4: return BITS == 4 ? qgemv_reg<BITS, NMAT, L, (BITS == 4 ? 4 : 1), RPT, 1> : nullptr;
     default: return nullptr;
     }
 }
@@ -178,6 +210,19 @@ QGKernelFn pick_l(int L, int cpl)
 }
 
 }  // namespace
+
+QGKernelFn qgemv_reg_split_kernel(int bits, int nmat, int cpl, int h)
+{
+    // built for gate/up: Q4 with 1 or 2 chunks per lane, Q2 with 1
+    if (nmat != 2 || (h != 2 && h != 4)) return nullptr;
+    if (bits == 4) {
+        if (cpl == 1) return h == 2 ? qgemv_reg<4, 2, 32, 1, 1, 2> : qgemv_reg<4, 2, 32, 1, 1, 4>;
+        if (cpl == 2) return h == 2 ? qgemv_reg<4, 2, 32, 2, 1, 2> : qgemv_reg<4, 2, 32, 2, 1, 4>;
+        return nullptr;
+    }
+    if (cpl == 1) return h == 2 ? qgemv_reg<2, 2, 32, 1, 1, 2> : qgemv_reg<2, 2, 32, 1, 1, 4>;
+    return nullptr;
+}
 
 QGKernelFn qgemv_reg_kernel(int bits, int nmat, int L, int cpl, int rpt)
 {

@@ -244,6 +244,11 @@ uint32_t round16(uint32_t v) { return (v + 15u) & ~15u; }
 
 constexpr size_t kSmemBudget = 200 * 1024;
 
+// Row-split gate/up kernel: parts per row, used when a CTA would hold fewer
+// than kSplitBelow rows (too few stages to keep 12 warps busy).
+constexpr int kRowSplit = 2;
+constexpr int kSplitBelow = 24;
+
 struct TmaConfig {
     int nw, ns, rpt;
 };
@@ -319,6 +324,26 @@ cudaError_t launch_tma(QGArgs &a, int n_experts, cudaStream_t stream, bool *unsu
     a.off_bars = a.off_gmax + round16(static_cast<uint32_t>(ngroups) * 4u);
     TmaConfig cfg;
     size_t smem = 0;
+    // Row split (gate/up over few rows per CTA): each lane holds the digits
+    // of KC / (32 H) chunks, so 16 warps fit and share H times as many
+    // stages; the parts of a row meet in shared memory.
+    constexpr int H = kRowSplit;
+    if (NMAT == 2 && max_units < kSplitBelow && KC % (32 * H) == 0 && KC / (32 * H) <= 2 &&
+        ngroups % (4 * H) == 0) {
+        QGArgs av = a;
+        av.K = a.K / H;  // the ring carries virtual rows of K / H columns
+        const size_t part_bytes = round16(static_cast<uint32_t>(max_units * H * NMAT) * 4u);
+        QGKernelFn sk = qgemv_reg_split_kernel(BITS, NMAT, KC / (32 * H), H);
+        if (sk && pick_config<BITS, NMAT>(av, 1, max_units * H, dev->max_smem_optin - static_cast<int>(part_bytes),
+                                          16, 1, &cfg, &a.stage_bytes, &a.off_slots, &smem)) {
+            a.ns = cfg.ns;
+            a.off_part = static_cast<uint32_t>(smem - 128);
+            smem += part_bytes;
+            cudaError_t err = ensure_dynamic_smem(sk, smem);
+            if (err != cudaSuccess) return err;
+            return launch_pdl(sk, dim3(static_cast<unsigned>(cpe * n_experts)), dim3(cfg.nw * 32), smem, stream, a);
+        }
+    }
     // Register-digit kernel when a lane's share of the row is at most
     // reg_kernel_max_cpl(BITS) chunks: the largest team (L) that divides KC.
     int rl = 0;

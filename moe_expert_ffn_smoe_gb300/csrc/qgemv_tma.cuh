@@ -26,6 +26,7 @@ struct QGArgs {
     int ns;                // ring slots per warp
     uint32_t stage_bytes;  // bytes of one slot
     uint32_t off_info, off_gmax, off_bars, off_slots;  // shared-memory offsets
+    uint32_t off_part;     // row-split kernel: partial row sums
 };
 
 template <int BITS>
@@ -232,6 +233,10 @@ using QGKernelFn = void (*)(QGArgs);
 // The register-digit kernel for (bits, nmat, L lanes per row, cpl chunks
 // per lane, rpt rows per team), or nullptr when none is built for them.
 QGKernelFn qgemv_reg_kernel(int bits, int nmat, int L, int cpl, int rpt);
+
+// The register-digit kernel with every row split into h parts over as many
+// classes of warps (512 threads; L = 32, one row per stage), or nullptr.
+QGKernelFn qgemv_reg_split_kernel(int bits, int nmat, int cpl, int h);
 
 // Chunks per lane the register-digit kernel takes at most: its digits use
 // cpl * 12 * NCLASS registers per thread.

@@ -32,19 +32,21 @@ struct RegDot {
     uint32_t soff[CPL];
 
     // Lane u's digits, q / Z, q * Sxq and scale byte offsets from x staged at
-    // sbase (digits) and sbase + off_info (chunk info).
-    __device__ __forceinline__ void load(uint32_t sbase, uint32_t off_info, int u)
+    // sbase (digits) and sbase + off_info (chunk info).  The rows streamed
+    // may be a part of x's length: chunks chunk0 .. chunk0 + KC - 1 of x,
+    // whose scales start at group `group0` of the full row.
+    __device__ __forceinline__ void load(uint32_t sbase, uint32_t off_info, int u, int chunk0 = 0, int group0 = 0)
     {
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            const int c = u + j * L;
+            const int c = chunk0 + u + j * L;
             const uint32_t xc = sbase + static_cast<uint32_t>(c) * D::XSTRIDE;
 #pragma unroll
             for (int t = 0; t < ND; ++t) dg[j][t] = lds128u(xc + static_cast<uint32_t>(t) * 16u);
             const float4 inf = lds128f(sbase + off_info + static_cast<uint32_t>(c) * 16u);
             qz[j] = inf.x * D::ZINV;
             qs[j] = inf.y;
-            soff[j] = static_cast<uint32_t>(__float_as_int(inf.z)) * 4u;
+            soff[j] = static_cast<uint32_t>(__float_as_int(inf.z) - group0) * 4u;
         }
     }
 

@@ -4,8 +4,10 @@ with the f64 oracle, through the C ABI.
 The call computes hidden_e = SiLU(gate_e x) * (up_e x) and
 out_e = down_e hidden_e for every expert in one launch (per 64 experts);
 shapes the one-launch kernel does not take run as the two grouped calls.
-Besides the oracle tolerance, the one-launch result must equal the grouped
-two-call result bit for bit (both use the same per-row arithmetic), and the
+The one-launch result and the grouped two-call result are both held to the
+oracle tolerance (they may sum a row's parts in different orders: the
+grouped gate/up splits rows over more warps when a CTA has few of them),
+repeated calls must reproduce their own result bit for bit, and the
 hand-off counters must be zero again after every call.
 """
 import numpy as np
@@ -68,13 +70,15 @@ def _grouped(smoe, bits, tens, xd, d_model, d_ff, group, dev):
     return hidden, out
 
 
-def _check_against_oracle(bits, ex, x, hidden, out, d_model, d_ff, group, tag):
+def _check_against_oracle(bits, ex, x, hiddens, outs, d_model, d_ff, group, tag):
+    """hiddens / outs: lists of (result, label) for this expert."""
     r = oracle.gate_up(bits, ex["gate_codes"], ex["gate_scales"], ex["up_codes"], ex["up_scales"],
                        d_ff, d_model, group, x.astype(np.float64))
-    if hidden is not None:
-        check(hidden, r["hidden"], hidden_bound_absdot(r), f"{tag} hidden")
+    for h, lab in hiddens:
+        check(h, r["hidden"], hidden_bound_absdot(r), f"{tag} {lab} hidden")
     y, a = oracle.qgemv(bits, ex["down_codes"], ex["down_scales"], d_model, d_ff, group, r["hidden"])
-    check(out, y, a, f"{tag} out")
+    for o, lab in outs:
+        check(o, y, a, f"{tag} {lab} out")
 
 
 def _setup(bits, n, d_model, d_ff, group, seed, dev):
@@ -95,12 +99,13 @@ def test_experts_ffn_8_expert_decode(smoe, dev, bits, seed):
     assert smoe.smoe_last_device_status() == 0
     assert int(ws[:SYNC_WORDS].abs().sum()) == 0, "hand-off counters not reset"
     h, o = _hidden(ws, n, d_ff).cpu().numpy(), out.cpu().numpy()
-    for i, ex in enumerate(experts):
-        _check_against_oracle(bits, ex, x, h[i], o[i], d_model, d_ff, group, f"ffn Q{bits} expert {i}")
     gh, go = _grouped(smoe, bits, tens, xd, d_model, d_ff, group, dev)
     torch.cuda.synchronize()
-    assert torch.equal(gh, _hidden(ws, n, d_ff)), "hidden differs from the grouped calls"
-    assert torch.equal(go, out), "out differs from the grouped calls"
+    gh, go = gh.cpu().numpy(), go.cpu().numpy()
+    for i, ex in enumerate(experts):
+        _check_against_oracle(bits, ex, x, [(h[i], "one call"), (gh[i], "grouped")],
+                              [(o[i], "one call"), (go[i], "grouped")], d_model, d_ff, group,
+                              f"ffn Q{bits} expert {i}")
 
 
 def test_experts_ffn_repeated_calls_and_graph(smoe, dev):
@@ -153,11 +158,12 @@ def test_experts_ffn_shapes(smoe, dev, bits, n, d_model, d_ff, group):
     assert smoe.smoe_last_device_status() == 0
     assert int(ws[:SYNC_WORDS].abs().sum()) == 0
     o = out.cpu().numpy()
-    for i in sorted({0, n // 2, n - 1}):
-        _check_against_oracle(bits, experts[i], x, None, o[i], d_model, d_ff, group, f"ffn n={n} expert {i}")
     _, go = _grouped(smoe, bits, tens, xd, d_model, d_ff, group, dev)
     torch.cuda.synchronize()
-    assert torch.equal(go, out)
+    go = go.cpu().numpy()
+    for i in sorted({0, n // 2, n - 1}):
+        _check_against_oracle(bits, experts[i], x, [], [(o[i], "one call"), (go[i], "grouped")], d_model, d_ff,
+                              group, f"ffn n={n} expert {i}")
 
 
 def test_experts_ffn_empty_hidden_writes_zeros(smoe, dev):
