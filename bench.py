@@ -463,6 +463,8 @@ def rows_breakdown(smoe, dev, steps, pattern=""):
     for (rows, cols), seed in zip(inp.CONFIGS["bf16_matvec"]["shapes"], inp.CONFIGS["bf16_matvec"]["seeds"]):
         if pattern in f"bf16_{rows}x{cols}":
             bf16_row(smoe, dev, steps, out, hbm_peak, timed, s, rows, cols, seed)
+    if pattern in "bf16_batch_8x512x4096":
+        bf16_batch_row(smoe, dev, steps, out, hbm_peak, timed, s)
     for T in inp.CONFIGS["q4_token_batch"]["tokens"]:
         if pattern in f"q4_token_batch_T{T}":
             batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T)
@@ -500,6 +502,33 @@ def bf16_row(smoe, dev, steps, out, hbm_peak, timed, s, rows, cols, seed):
     b = wbytes + cols * 4 + rows * 4
     out[f"bf16_{rows}x{cols}"] = {"GB/s": round(b * nl / t / 1e9, 1), "us_per_call": round(t / nl * 1e6, 3),
                                   "frac": round(b * nl / t / 1e9 / hbm_peak, 4), "bytes_per_call": b}
+    del ws
+    torch.cuda.empty_cache()
+
+
+def bf16_batch_row(smoe, dev, steps, out, hbm_peak, timed, s, n=8, rows=512, cols=4096, seed=3):
+    """n small bf16 matvecs in one matvec_bf16_batch submission, against the
+    same matvecs as n matvec_bf16 calls."""
+    import torch
+    wbytes = n * rows * cols * 2
+    ncp = max(2, -(-4 * L2_BYTES // wbytes))
+    ws = [[torch.from_numpy(inp.bf16_rows(rows, cols, seed, 1 + 100 * c + i).view(np.int16)).to(dev)
+           for i in range(n)] for c in range(ncp)]
+    xs = [torch.from_numpy(inp.activations(cols, seed + i)).to(dev) for i in range(n)]
+    ys = [torch.empty(rows, device=dev) for _ in range(n)]
+    nl = max(20, min(steps // 4, 400))
+    t_b = timed(lambda i: smoe.matvec_bf16_batch(ws[i % ncp], xs, ys, [rows] * n, [cols] * n, stream=s), nl)
+
+    def singles(i):
+        for j in range(n):
+            smoe.matvec_bf16(ws[i % ncp][j], xs[j], ys[j], rows, cols, stream=s)
+
+    t_s = timed(singles, nl)
+    b = n * (rows * cols * 2 + cols * 4 + rows * 4)
+    out[f"bf16_batch_{n}x{rows}x{cols}"] = {
+        "GB/s": round(b * nl / t_b / 1e9, 1), "us_per_call": round(t_b / nl * 1e6, 3),
+        "frac": round(b * nl / t_b / 1e9 / hbm_peak, 4), "bytes_per_call": b,
+        "single_calls_us": round(t_s / nl * 1e6, 3)}
     del ws
     torch.cuda.empty_cache()
 

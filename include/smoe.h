@@ -238,6 +238,24 @@ int matvec_bf16(const uint16_t *w, const float *x, float *y,
                 int rows, int cols, void *stream);
 
 /*
+ * n independent dense bf16 matvecs in one submission ("Batched Scout
+ * Matvec"):
+ *
+ *   y[i][r] = sum_k bf16(w[i][r][k]) * x[i][k],  i in [0, n), r in [0, rows[i]).
+ *
+ * w, x, y: host arrays of n device pointers; rows, cols: host arrays of n
+ * sizes.  Every entry follows matvec_bf16's contract (cols[i] a multiple of 8
+ * and at most SMOE_MAX_COLS, 16-byte alignment); an entry with rows[i] == 0
+ * is skipped and may hold null pointers.  No output may overlap any input or
+ * another output (SMOE_ERR_ALIAS).  The matvecs share one grid (one launch
+ * per 64 entries of equal row-length class, usually one in all), so many
+ * small matvecs pay one launch ramp.  n == 0 is a no-op.
+ */
+int matvec_bf16_batch(int n, const uint16_t *const *w, const float *const *x,
+                      float *const *y, const int *rows, const int *cols,
+                      void *stream);
+
+/*
  * Bytes of device workspace ffn_batch_q4 needs for these sizes (the hidden
  * activations [T x d_ff] f32 and any partial sums), rounded up to 256.
  * Returns 0 for T <= 0 and (size_t)-1 for sizes the call would refuse.

@@ -49,6 +49,7 @@ _SIGS = {
     "smoe_down_q4": ([_P, _P, _P, _P, _I, _I, _I, _P], _I),
     "smoe_down_q2": ([_P, _P, _P, _P, _I, _I, _I, _P], _I),
     "matvec_bf16": ([_P, _P, _P, _I, _I, _P], _I),
+    "matvec_bf16_batch": ([_I, _P, _P, _P, _P, _P, _P], _I),
     "smoe_experts_gate_up_q4": ([_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P], _I),
     "smoe_experts_gate_up_q2": ([_I, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P], _I),
     "smoe_experts_down_q4": ([_I, _P, _P, _P, _P, _I, _I, _I, _P], _I),
@@ -212,6 +213,17 @@ def smoe_experts_ffn_q2(gate_codes, gate_scales, up_codes, up_scales, down_codes
 
 def matvec_bf16(w, x, y, rows, cols, stream=None):
     _check(_lib.matvec_bf16(_ptr(w), _ptr(x), _ptr(y), rows, cols, _stream(stream)), "matvec_bf16")
+
+
+def matvec_bf16_batch(ws, xs, ys, rows, cols, stream=None):
+    """Lists of n tensors (or device addresses) and n sizes; one submission."""
+    n = len(ws)
+    if not (len(xs) == len(ys) == len(rows) == len(cols) == n):
+        raise ValueError("matvec_bf16_batch: lists differ in length")
+    arrs = [_ptr_array(a) for a in (ws, xs, ys)]
+    r = (ctypes.c_int * max(1, n))(*rows)
+    c = (ctypes.c_int * max(1, n))(*cols)
+    _check(_lib.matvec_bf16_batch(n, *arrs, r, c, _stream(stream)), "matvec_bf16_batch")
 
 
 def smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group):

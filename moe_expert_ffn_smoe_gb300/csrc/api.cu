@@ -394,6 +394,38 @@ int matvec_bf16(const uint16_t *w, const float *x, float *y, int rows, int cols,
     return to_status(smoe::launch_bf16_gemv(w, x, y, rows, cols, static_cast<cudaStream_t>(stream)));
 }
 
+int matvec_bf16_batch(int n, const uint16_t *const *w, const float *const *x, float *const *y,
+                      const int *rows, const int *cols, void *stream)
+{
+    if (n < 0) return SMOE_ERR_SHAPE;
+    if (n == 0) return SMOE_OK;
+    if (!w || !x || !y || !rows || !cols) return SMOE_ERR_NULL;
+    for (int i = 0; i < n; ++i) {
+        if (rows[i] < 0 || cols[i] < 0 || cols[i] > SMOE_MAX_COLS || cols[i] % 8 != 0) return SMOE_ERR_SHAPE;
+        if (rows[i] == 0) continue;
+        if (!y[i]) return SMOE_ERR_NULL;
+        if (!aligned16(y[i])) return SMOE_ERR_ALIGN;
+        if (cols[i] > 0) {
+            if (!w[i] || !x[i]) return SMOE_ERR_NULL;
+            if (!aligned16(w[i]) || !aligned16(x[i])) return SMOE_ERR_ALIGN;
+        }
+    }
+    // every output against every input and every other output
+    for (int i = 0; i < n; ++i) {
+        if (rows[i] == 0) continue;
+        const Span o = {y[i], static_cast<size_t>(rows[i]) * sizeof(float)};
+        for (int j = 0; j < n; ++j) {
+            if (rows[j] == 0) continue;
+            if (j > i && overlap(o, Span{y[j], static_cast<size_t>(rows[j]) * sizeof(float)})) return SMOE_ERR_ALIAS;
+            if (cols[j] == 0) continue;
+            if (overlap(o, Span{w[j], static_cast<size_t>(rows[j]) * static_cast<size_t>(cols[j]) * 2}) ||
+                overlap(o, Span{x[j], static_cast<size_t>(cols[j]) * sizeof(float)}))
+                return SMOE_ERR_ALIAS;
+        }
+    }
+    return to_status(smoe::launch_bf16_gemv_batch(n, w, x, y, rows, cols, static_cast<cudaStream_t>(stream)));
+}
+
 size_t smoe_ffn_batch_workspace_bytes(int T, int d_model, int d_ff, int group)
 {
     if (T <= 0) return 0;

@@ -13,6 +13,11 @@
 // a shift or a mask.  Per row, the 512 partial sums are reduced with warp
 // shuffles and one shared-memory step.  The CTA prefetches the head of its
 // row block into L2 before waiting on the previous kernel.
+//
+// Batched form (section "Batched Scout Matvec": N independent matvecs in one
+// submission): one grid of about one CTA per SM is shared by the matvecs in
+// proportion to their weight bytes, each CTA running the same row-block
+// sweep on its matvec, so many small matvecs cost one launch ramp.
 #include "common.cuh"
 #include "internal.h"
 
@@ -27,36 +32,51 @@ struct Bf16Args {
     uint32_t prefetch_bytes;  // per CTA, from the start of its row block
 };
 
+// N independent matvecs in one grid ("Batched Scout Matvec"): matvec i owns
+// CTAs [cta0[i], cta0[i + 1]), each a contiguous block of its rows.  All
+// matvecs of one launch take the same chunks per thread (CPL).
+constexpr int BF_BATCH_MAX = 64;
+
+struct Bf16BatchArgs {
+    const uint16_t *w[BF_BATCH_MAX];
+    const float *x[BF_BATCH_MAX];
+    float *y[BF_BATCH_MAX];
+    int rows[BF_BATCH_MAX];
+    int K[BF_BATCH_MAX];
+    int cta0[BF_BATCH_MAX + 1];
+    int n;
+    uint32_t prefetch_bytes;
+};
+
 constexpr int BF_THREADS = 512;
 constexpr int BF_WARPS = BF_THREADS / 32;
 constexpr int BF_GMAX = 8;
 
-// CPL: 16-byte chunks per thread per row (K <= CPL * 512 * 8).
+// Rows [r0, r1) of y = W x by the whole CTA.  CPL: 16-byte chunks per
+// thread per row (K <= CPL * 512 * 8).  xs: K floats of dynamic shared
+// memory; part: the per-warp row sums.
 template <int CPL>
-__global__ void __launch_bounds__(BF_THREADS, 1) bf16_gemv(Bf16Args a)
+__device__ __forceinline__ void bf16_rows(const uint16_t *__restrict__ w, const float *__restrict__ x,
+                                          float *__restrict__ y, int r0, int r1, int K, uint32_t prefetch_bytes,
+                                          float4 *xs, float (&part)[2][BF_WARPS][BF_GMAX])
 {
     constexpr int BF_G = 8 / CPL > 2 ? 8 / CPL : 2;  // rows per group
     constexpr bool XREG = CPL <= 2;                 // x of the thread's chunks in registers
-    extern __shared__ __align__(16) float4 xs[];
-    __shared__ float part[2][BF_WARPS][BF_GMAX];
     const int t = threadIdx.x;
     const int lane = t & 31;
     const int warp = t >> 5;
-    const int KC = a.K >> 3;  // 16-byte chunks per row
-    const size_t row_elems = static_cast<size_t>(a.K);
+    const int KC = K >> 3;  // 16-byte chunks per row
+    const size_t row_elems = static_cast<size_t>(K);
 
-    const int r0 = static_cast<int>(static_cast<long long>(a.rows) * blockIdx.x / gridDim.x);
-    const int r1 = static_cast<int>(static_cast<long long>(a.rows) * (blockIdx.x + 1) / gridDim.x);
-
-    if (a.prefetch_bytes && r1 > r0) {
+    if (prefetch_bytes && r1 > r0) {
         size_t range = static_cast<size_t>(r1 - r0) * row_elems * 2;
-        if (range > a.prefetch_bytes) range = a.prefetch_bytes;
-        prefetch_range_l2(a.w + static_cast<size_t>(r0) * row_elems, range, 16384);
+        if (range > prefetch_bytes) range = prefetch_bytes;
+        prefetch_range_l2(w + static_cast<size_t>(r0) * row_elems, range, 16384);
     }
 
     pdl_wait();
-    const int nq = a.K >> 2;
-    for (int q = t; q < nq; q += BF_THREADS) xs[q] = reinterpret_cast<const float4 *>(a.x)[q];
+    const int nq = K >> 2;
+    for (int q = t; q < nq; q += BF_THREADS) xs[q] = reinterpret_cast<const float4 *>(x)[q];
     __syncthreads();
     pdl_launch_dependents();
 
@@ -81,7 +101,7 @@ __global__ void __launch_bounds__(BF_THREADS, 1) bf16_gemv(Bf16Args a)
 #pragma unroll
         for (int g = 0; g < BF_G; ++g) {
             const int row = min(r + g, r1 - 1);
-            const uint16_t *wrow = a.w + static_cast<size_t>(row) * row_elems;
+            const uint16_t *wrow = w + static_cast<size_t>(row) * row_elems;
 #pragma unroll
             for (int j = 0; j < CPL; ++j) {
                 const int cc = t + BF_THREADS * j;
@@ -138,7 +158,7 @@ __global__ void __launch_bounds__(BF_THREADS, 1) bf16_gemv(Bf16Args a)
             float v = 0.f;
 #pragma unroll
             for (int w2 = 0; w2 < BF_WARPS; ++w2) v += part[buf][w2][t];
-            a.y[r + t] = v;
+            y[r + t] = v;
         }
         buf ^= 1;
 #pragma unroll
@@ -146,6 +166,36 @@ __global__ void __launch_bounds__(BF_THREADS, 1) bf16_gemv(Bf16Args a)
 #pragma unroll
             for (int j = 0; j < CPL; ++j) cur[g][j] = nxt[g][j];
     }
+}
+
+template <int CPL>
+__global__ void __launch_bounds__(BF_THREADS, 1) bf16_gemv(Bf16Args a)
+{
+    extern __shared__ __align__(16) float4 xs[];
+    __shared__ float part[2][BF_WARPS][BF_GMAX];
+    const int r0 = static_cast<int>(static_cast<long long>(a.rows) * blockIdx.x / gridDim.x);
+    const int r1 = static_cast<int>(static_cast<long long>(a.rows) * (blockIdx.x + 1) / gridDim.x);
+    bf16_rows<CPL>(a.w, a.x, a.y, r0, r1, a.K, a.prefetch_bytes, xs, part);
+}
+
+template <int CPL>
+__global__ void __launch_bounds__(BF_THREADS, 1) bf16_gemv_batch(const __grid_constant__ Bf16BatchArgs a)
+{
+    extern __shared__ __align__(16) float4 xs[];
+    __shared__ float part[2][BF_WARPS][BF_GMAX];
+    // the matvec this CTA belongs to: the last i with cta0[i] <= blockIdx.x
+    int lo = 0, hi = a.n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.cta0[mid] <= static_cast<int>(blockIdx.x)) lo = mid;
+        else hi = mid - 1;
+    }
+    const int i = lo;
+    const int nb = a.cta0[i + 1] - a.cta0[i];
+    const int b = static_cast<int>(blockIdx.x) - a.cta0[i];
+    const int r0 = static_cast<int>(static_cast<long long>(a.rows[i]) * b / nb);
+    const int r1 = static_cast<int>(static_cast<long long>(a.rows[i]) * (b + 1) / nb);
+    bf16_rows<CPL>(a.w[i], a.x[i], a.y[i], r0, r1, a.K[i], a.prefetch_bytes, xs, part);
 }
 
 cudaError_t launch_bf16_gemv(const uint16_t *w, const float *x, float *y, int rows, int K,
@@ -178,6 +228,99 @@ cudaError_t launch_bf16_gemv(const uint16_t *w, const float *x, float *y, int ro
     cudaError_t e = ensure_dynamic_smem(k, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, dim3(static_cast<unsigned>(grid)), dim3(BF_THREADS), smem, stream, a);
+}
+
+namespace {
+
+int bf16_cpl(int K)
+{
+    const int cpl = (K / 8 + BF_THREADS - 1) / BF_THREADS;
+    return cpl < 1 ? 1 : cpl;
+}
+
+using BatchKernel = void (*)(Bf16BatchArgs);
+
+BatchKernel batch_kernel(int cpl)
+{
+    switch (cpl) {
+    case 1: return bf16_gemv_batch<1>;
+    case 2: return bf16_gemv_batch<2>;
+    case 3: return bf16_gemv_batch<3>;
+    case 4: return bf16_gemv_batch<4>;
+    case 5: return bf16_gemv_batch<5>;
+    case 6: return bf16_gemv_batch<6>;
+    case 7: return bf16_gemv_batch<7>;
+    case 8: return bf16_gemv_batch<8>;
+    default: return nullptr;
+    }
+}
+
+// One launch for entries idx[0..cnt) (same CPL, rows > 0): about one CTA per
+// SM in total, split over the matvecs in proportion to their weight bytes,
+// at least one CTA each and never more CTAs than rows.
+cudaError_t launch_batch_part(const uint16_t *const *w, const float *const *x, float *const *y, const int *rows,
+                              const int *cols, const int *idx, int cnt, int cpl, int sm_count, cudaStream_t stream)
+{
+    Bf16BatchArgs a = {};
+    a.n = cnt;
+    double total = 0.0;
+    int kmax = 4;
+    for (int j = 0; j < cnt; ++j) {
+        total += static_cast<double>(rows[idx[j]]) * (cols[idx[j]] > 0 ? cols[idx[j]] : 8);
+        if (cols[idx[j]] > kmax) kmax = cols[idx[j]];
+    }
+    int next = 0;
+    for (int j = 0; j < cnt; ++j) {
+        const int i = idx[j];
+        const double share = static_cast<double>(rows[i]) * (cols[i] > 0 ? cols[i] : 8) / total;
+        long long nb = static_cast<long long>(share * sm_count + 0.5);
+        if (nb < 1) nb = 1;
+        if (nb > rows[i]) nb = rows[i];
+        a.w[j] = w[i];
+        a.x[j] = x[i];
+        a.y[j] = y[i];
+        a.rows[j] = rows[i];
+        a.K[j] = cols[i];
+        a.cta0[j] = next;
+        next += static_cast<int>(nb);
+    }
+    a.cta0[cnt] = next;
+    const size_t l2_share = static_cast<size_t>(32u << 20) / static_cast<size_t>(next);
+    a.prefetch_bytes = static_cast<uint32_t>(l2_share < (1u << 20) ? l2_share : (1u << 20));
+    BatchKernel k = batch_kernel(cpl);
+    if (!k) return cudaErrorInvalidValue;
+    const size_t smem = static_cast<size_t>(kmax) * sizeof(float);
+    cudaError_t e = ensure_dynamic_smem(k, smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(k, dim3(static_cast<unsigned>(next)), dim3(BF_THREADS), smem, stream, a);
+}
+
+}  // namespace
+
+cudaError_t launch_bf16_gemv_batch(int n, const uint16_t *const *w, const float *const *x, float *const *y,
+                                   const int *rows, const int *cols, cudaStream_t stream)
+{
+    const DeviceInfo *dev = device_info();
+    if (!dev) return cudaErrorInvalidDevice;
+    // one launch per chunks-per-thread class present, 64 matvecs at most each
+    for (int cpl = 1; cpl <= 8; ++cpl) {
+        int idx[BF_BATCH_MAX];
+        int cnt = 0;
+        for (int i = 0; i < n; ++i) {
+            if (rows[i] == 0 || bf16_cpl(cols[i]) != cpl) continue;
+            idx[cnt++] = i;
+            if (cnt == BF_BATCH_MAX) {
+                cudaError_t e = launch_batch_part(w, x, y, rows, cols, idx, cnt, cpl, dev->sm_count, stream);
+                if (e != cudaSuccess) return e;
+                cnt = 0;
+            }
+        }
+        if (cnt > 0) {
+            cudaError_t e = launch_batch_part(w, x, y, rows, cols, idx, cnt, cpl, dev->sm_count, stream);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    return cudaSuccess;
 }
 
 }  // namespace smoe

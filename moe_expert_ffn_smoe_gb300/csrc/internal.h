@@ -50,6 +50,11 @@ unsigned *device_status_word();
 cudaError_t launch_bf16_gemv(const uint16_t *w, const float *x, float *y, int rows, int K,
                              cudaStream_t stream);
 
+// n independent bf16 matvecs (host arrays of device pointers and sizes,
+// checked by the caller); entries with rows == 0 are skipped.
+cudaError_t launch_bf16_gemv_batch(int n, const uint16_t *const *w, const float *const *x, float *const *y,
+                                   const int *rows, const int *cols, cudaStream_t stream);
+
 // Token batch: Y[T x units] = W X^T for T tokens (nmat == 2: fused gate/up,
 // Y = hidden).  Shapes already validated.
 cudaError_t launch_qgemm_tokens(int bits, int nmat, const uint8_t *const codes[2],

@@ -179,3 +179,28 @@ def test_experts_ffn_workspace_and_refusals(smoe):
     assert f(*args(n=0)) == smoe.SMOE_OK
     bad = [P([A, A + 8])] + w[1:]
     assert f(2, *bad, x, out, 4096, 1536, 64, ws, need, None) == smoe.SMOE_ERR_ALIGN
+
+
+def test_bf16_batch_refusals(smoe):
+    L = smoe._lib
+    P = lambda v: (ctypes.c_void_p * len(v))(*v)
+    I = lambda v: (ctypes.c_int * len(v))(*v)
+    w = [A, A + 0x1000000, A + 0x2000000]
+    x = [A + 0x3000000, A + 0x3100000, A + 0x3200000]
+    y = [A + 0x4000000, A + 0x4100000, A + 0x4200000]
+    rows, cols = [16, 32, 8], [64, 128, 4096]
+
+    def call(n=3, w=w, x=x, y=y, rows=rows, cols=cols):
+        return L.matvec_bf16_batch(n, P(w), P(x), P(y), I(rows), I(cols), None)
+
+    assert L.matvec_bf16_batch(0, None, None, None, None, None, None) == smoe.SMOE_OK
+    assert L.matvec_bf16_batch(-1, None, None, None, None, None, None) == smoe.SMOE_ERR_SHAPE
+    assert L.matvec_bf16_batch(2, None, P(x), P(y), I(rows), I(cols), None) == smoe.SMOE_ERR_NULL
+    assert call(cols=[64, 12, 4096]) == smoe.SMOE_ERR_SHAPE                        # cols % 8
+    assert call(cols=[64, 128, smoe.SMOE_MAX_COLS + 8]) == smoe.SMOE_ERR_SHAPE
+    assert call(rows=[16, -1, 8]) == smoe.SMOE_ERR_SHAPE
+    assert call(w=[A, 0, A + 0x2000000]) == smoe.SMOE_ERR_NULL
+    assert call(y=[A + 0x4000000, A + 0x4100000, A + 0x4200004]) == smoe.SMOE_ERR_ALIGN
+    assert call(y=[A + 0x4000000, A + 0x4000000 + 32, A + 0x4200000]) == smoe.SMOE_ERR_ALIAS  # two outputs
+    assert call(y=[A + 0x4000000, A + 0x1000000 + 256, A + 0x4200000]) == smoe.SMOE_ERR_ALIAS  # y1 over w1
+    assert call(y=[A + 0x3200000, A + 0x4100000, A + 0x4200000]) == smoe.SMOE_ERR_ALIAS   # y0 over x2

@@ -238,6 +238,46 @@ def test_bf16_single_nonzero_is_exact(smoe, dev):
     assert g[17] == np.float32(3.0) * x[200] and np.count_nonzero(g) == 1
 
 
+def _bf16_batch_case(smoe, dev, shapes, seed):
+    ws, xs, ys, host = [], [], [], []
+    for i, (rows, cols) in enumerate(shapes):
+        w = inp.bf16_rows(rows, cols, seed, 1 + i)
+        x = inp.activations(cols, seed + 100 * i)
+        host.append((w, x))
+        ws.append(to_dev(w, dev) if rows * cols else None)
+        xs.append(to_dev(x, dev) if cols else None)
+        ys.append(torch.full((max(rows, 1),), float("nan"), device=dev))
+    smoe.matvec_bf16_batch(ws, xs, ys, [r for r, _ in shapes], [c for _, c in shapes])
+    torch.cuda.synchronize()
+    for i, ((rows, cols), (w, x)) in enumerate(zip(shapes, host)):
+        if rows == 0:
+            assert torch.isnan(ys[i]).all(), "an entry with no rows was written"
+            continue
+        got = ys[i].cpu().numpy()[:rows]
+        if cols == 0:
+            assert (got == 0).all()
+            continue
+        ref, a = oracle.matvec_bf16(w, rows, cols, x.astype(np.float64))
+        check(got, ref, a, f"bf16 batch entry {i} {rows}x{cols}")
+
+
+@pytest.mark.parametrize("shapes", [
+    [(512, 4096)] * 8,                                   # the small-matvec case: one launch
+    [(8192, 4096), (3, 8), (777, 4104), (1, 64), (4096, 1536)],  # mixed sizes, one chunk class
+    [(100, 12288), (512, 4096), (200, 32768), (64, 2048)],      # three chunk classes: three launches
+    [(0, 4096), (16, 0), (37, 520)],                     # an empty entry and a zero-width one
+])
+def test_bf16_batch(smoe, dev, shapes):
+    _bf16_batch_case(smoe, dev, shapes, 21)
+
+
+def test_bf16_batch_70_entries(smoe, dev):
+    """More than 64 entries: two launches of one class."""
+    rng = np.random.default_rng(22)
+    shapes = [(int(rng.integers(1, 300)), 8 * int(rng.integers(1, 600))) for _ in range(70)]
+    _bf16_batch_case(smoe, dev, shapes, 22)
+
+
 # ---------------------------------------------------------------- token batch
 
 def _batch(smoe, dev, T, e, X, d_model, d_ff, group):
