@@ -468,6 +468,9 @@ def rows_breakdown(smoe, dev, steps, pattern=""):
     for T in inp.CONFIGS["q4_token_batch"]["tokens"]:
         if pattern in f"q4_token_batch_T{T}":
             batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T)
+    for T in (16, 256):
+        if pattern in f"q2_token_batch_T{T}":
+            batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T, bits=2)
     if pattern in "q4_ffn_256":
         small_row(smoe, dev, steps, out, timed, s)
     return out
@@ -533,12 +536,14 @@ def bf16_batch_row(smoe, dev, steps, out, hbm_peak, timed, s, n=8, rows=512, col
     torch.cuda.empty_cache()
 
 
-def batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T):
-    """Token-batch FFN of one Q4 expert for T tokens (16 rotating experts)."""
+def batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T, bits=4):
+    """Token-batch FFN of one expert for T tokens (16 rotating experts)."""
     import torch
     ncp = 16
-    experts = [{k: torch.from_numpy(v).to(dev) for k, v in inp.expert(4, D_MODEL, D_FF, GROUP, 7 + 1000 * c).items()}
+    experts = [{k: torch.from_numpy(v).to(dev)
+                for k, v in inp.expert(bits, D_MODEL, D_FF, GROUP, 7 + bits % 4 + 1000 * c).items()}
                for c in range(ncp)]
+    fn = smoe.ffn_batch_q4 if bits == 4 else smoe.ffn_batch_q2
     X = torch.from_numpy(inp.activations((T, D_MODEL), 7)).to(dev)
     Y = torch.empty((T, D_MODEL), device=dev)
     need = smoe.smoe_ffn_batch_workspace_bytes(T, D_MODEL, D_FF, GROUP)
@@ -546,13 +551,13 @@ def batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T):
 
     def launch(i):
         e = experts[i % ncp]
-        smoe.ffn_batch_q4(e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"], e["down_codes"],
-                          e["down_scales"], X, Y, T, D_MODEL, D_FF, GROUP, ws, need, stream=s)
+        fn(e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"], e["down_codes"],
+           e["down_scales"], X, Y, T, D_MODEL, D_FF, GROUP, ws, need, stream=s)
     nl = max(20, min(steps // 8, 400))
     t = timed(launch, nl)
-    b = expert_bytes(4) + 2 * T * D_MODEL * 4
+    b = expert_bytes(bits) + 2 * T * D_MODEL * 4
     flops = 2 * T * 3 * D_FF * D_MODEL
-    out[f"q4_token_batch_T{T}"] = {"GB/s": round(b * nl / t / 1e9, 1), "us_per_call": round(t / nl * 1e6, 3),
+    out[f"q{bits}_token_batch_T{T}"] = {"GB/s": round(b * nl / t / 1e9, 1), "us_per_call": round(t / nl * 1e6, 3),
                                    "frac": round(b * nl / t / 1e9 / hbm_peak, 4),
                                    "TFLOP/s": round(flops * nl / t / 1e12, 2), "bytes_per_call": b}
     del experts

@@ -256,8 +256,9 @@ int matvec_bf16_batch(int n, const uint16_t *const *w, const float *const *x,
                       void *stream);
 
 /*
- * Bytes of device workspace ffn_batch_q4 needs for these sizes (the hidden
- * activations [T x d_ff] f32 and any partial sums), rounded up to 256.
+ * Bytes of device workspace ffn_batch_q4 and ffn_batch_q2 need for these
+ * sizes (the hidden activations [T x d_ff] f32 and any partial sums),
+ * rounded up to 256.
  * Returns 0 for T <= 0 and (size_t)-1 for sizes the call would refuse.
  */
 size_t smoe_ffn_batch_workspace_bytes(int T, int d_model, int d_ff, int group);
@@ -281,6 +282,21 @@ size_t smoe_ffn_batch_workspace_bytes(int T, int d_model, int d_ff, int group);
  * integers, X split into two bf16 halves, f32 accumulation).
  */
 int ffn_batch_q4(const uint8_t *gate_codes, const float *gate_scales,
+                 const uint8_t *up_codes, const float *up_scales,
+                 const uint8_t *down_codes, const float *down_scales,
+                 const float *X, float *Y,
+                 int T, int d_model, int d_ff, int group,
+                 void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The same token batch for one Q2 expert (the page names Q2 vaults as the
+ * next format of this batched path): codes packed four per byte as in
+ * smoe_gate_up_q2, Z = 1.5; d_model, d_ff and group multiples of 64 (the Q2
+ * layout contract).  Same arguments, workspace size
+ * (smoe_ffn_batch_workspace_bytes), checks and results as ffn_batch_q4;
+ * T >= 2 runs on the tensor cores with A = (code - 1.5)/4 exact in bf16.
+ */
+int ffn_batch_q2(const uint8_t *gate_codes, const float *gate_scales,
                  const uint8_t *up_codes, const float *up_scales,
                  const uint8_t *down_codes, const float *down_scales,
                  const float *X, float *Y,

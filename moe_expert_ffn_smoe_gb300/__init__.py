@@ -59,6 +59,7 @@ _SIGS = {
     "smoe_experts_ffn_q2": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
     "smoe_ffn_batch_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "ffn_batch_q4": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "ffn_batch_q2": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "ffn_batch_q4_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "smoe_last_device_status": ([_P], _I),
 }
@@ -236,6 +237,14 @@ def ffn_batch_q4(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_
                              _ptr(down_codes), _ptr(down_scales), _ptr(X), _ptr(Y), T, d_model,
                              d_ff, group, _ptr(workspace), workspace_bytes, _stream(stream)),
            "ffn_batch_q4")
+
+
+def ffn_batch_q2(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X, Y, T,
+                 d_model, d_ff, group, workspace, workspace_bytes, stream=None):
+    _check(_lib.ffn_batch_q2(_ptr(gate_codes), _ptr(gate_scales), _ptr(up_codes), _ptr(up_scales),
+                             _ptr(down_codes), _ptr(down_scales), _ptr(X), _ptr(Y), T, d_model,
+                             d_ff, group, _ptr(workspace), workspace_bytes, _stream(stream)),
+           "ffn_batch_q2")
 
 
 def ffn_batch_q4_noalloc(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X,

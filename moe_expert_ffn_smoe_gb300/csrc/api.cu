@@ -276,6 +276,49 @@ int experts_ffn_impl(int bits, int n, const uint8_t *const *gc, const float *con
     return SMOE_OK;
 }
 
+// ffn_batch_q4/q2: checks, then the token-batch launches.
+int ffn_batch_impl(int bits, const uint8_t *gate_codes, const float *gate_scales, const uint8_t *up_codes,
+                 const float *up_scales, const uint8_t *down_codes, const float *down_scales,
+                 const float *X, float *Y, int T, int d_model, int d_ff, int group,
+                 void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (T < 0) return SMOE_ERR_SHAPE;
+    int st = check_q_shape(bits, d_ff, d_model, group);
+    if (st != SMOE_OK) return st;
+    st = check_q_shape(bits, d_model, d_ff, group);
+    if (st != SMOE_OK) return st;
+    if (T == 0 || d_model == 0) return SMOE_OK;
+    if (!X || !Y) return SMOE_ERR_NULL;
+    if (!aligned16(X) || !aligned16(Y)) return SMOE_ERR_ALIGN;
+    if (d_ff > 0) {
+        if (!gate_codes || !gate_scales || !up_codes || !up_scales || !down_codes || !down_scales)
+            return SMOE_ERR_NULL;
+        if (!aligned16(gate_codes) || !aligned16(gate_scales) || !aligned16(up_codes) ||
+            !aligned16(up_scales) || !aligned16(down_codes) || !aligned16(down_scales))
+            return SMOE_ERR_ALIGN;
+    }
+    const size_t need = smoe::ffn_batch_workspace(T, d_model, d_ff, group);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return SMOE_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return SMOE_ERR_ALIGN;
+    }
+    const size_t xy = static_cast<size_t>(T) * static_cast<size_t>(d_model) * sizeof(float);
+    const Span outs[2] = {{Y, xy}, {workspace, need}};
+    const Span ins[7] = {{gate_codes, q_bytes(bits, d_ff, d_model)},
+                         {gate_scales, scale_bytes(d_ff, d_model, group)},
+                         {up_codes, q_bytes(bits, d_ff, d_model)},
+                         {up_scales, scale_bytes(d_ff, d_model, group)},
+                         {down_codes, q_bytes(bits, d_model, d_ff)},
+                         {down_scales, scale_bytes(d_model, d_ff, group)},
+                         {X, xy}};
+    if (any_alias(outs, 2, ins, 7)) return SMOE_ERR_ALIAS;
+    const uint8_t *gu_codes[2] = {gate_codes, up_codes};
+    const float *gu_scales[2] = {gate_scales, up_scales};
+    return to_status(smoe::launch_ffn_batch(bits, gu_codes, gu_scales, down_codes, down_scales, X, Y, T,
+                                            d_model, d_ff, group, workspace,
+                                            static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -440,41 +483,17 @@ int ffn_batch_q4(const uint8_t *gate_codes, const float *gate_scales, const uint
                  const float *X, float *Y, int T, int d_model, int d_ff, int group,
                  void *workspace, size_t workspace_bytes, void *stream)
 {
-    if (T < 0) return SMOE_ERR_SHAPE;
-    int st = check_q_shape(4, d_ff, d_model, group);
-    if (st != SMOE_OK) return st;
-    st = check_q_shape(4, d_model, d_ff, group);
-    if (st != SMOE_OK) return st;
-    if (T == 0 || d_model == 0) return SMOE_OK;
-    if (!X || !Y) return SMOE_ERR_NULL;
-    if (!aligned16(X) || !aligned16(Y)) return SMOE_ERR_ALIGN;
-    if (d_ff > 0) {
-        if (!gate_codes || !gate_scales || !up_codes || !up_scales || !down_codes || !down_scales)
-            return SMOE_ERR_NULL;
-        if (!aligned16(gate_codes) || !aligned16(gate_scales) || !aligned16(up_codes) ||
-            !aligned16(up_scales) || !aligned16(down_codes) || !aligned16(down_scales))
-            return SMOE_ERR_ALIGN;
-    }
-    const size_t need = smoe::ffn_batch_workspace(T, d_model, d_ff, group);
-    if (need > 0) {
-        if (!workspace || workspace_bytes < need) return SMOE_ERR_WORKSPACE;
-        if (!aligned16(workspace)) return SMOE_ERR_ALIGN;
-    }
-    const size_t xy = static_cast<size_t>(T) * static_cast<size_t>(d_model) * sizeof(float);
-    const Span outs[2] = {{Y, xy}, {workspace, need}};
-    const Span ins[7] = {{gate_codes, q_bytes(4, d_ff, d_model)},
-                         {gate_scales, scale_bytes(d_ff, d_model, group)},
-                         {up_codes, q_bytes(4, d_ff, d_model)},
-                         {up_scales, scale_bytes(d_ff, d_model, group)},
-                         {down_codes, q_bytes(4, d_model, d_ff)},
-                         {down_scales, scale_bytes(d_model, d_ff, group)},
-                         {X, xy}};
-    if (any_alias(outs, 2, ins, 7)) return SMOE_ERR_ALIAS;
-    const uint8_t *gu_codes[2] = {gate_codes, up_codes};
-    const float *gu_scales[2] = {gate_scales, up_scales};
-    return to_status(smoe::launch_ffn_batch(gu_codes, gu_scales, down_codes, down_scales, X, Y, T,
-                                            d_model, d_ff, group, workspace,
-                                            static_cast<cudaStream_t>(stream)));
+    return ffn_batch_impl(4, gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X, Y, T,
+                          d_model, d_ff, group, workspace, workspace_bytes, stream);
+}
+
+int ffn_batch_q2(const uint8_t *gate_codes, const float *gate_scales, const uint8_t *up_codes,
+                 const float *up_scales, const uint8_t *down_codes, const float *down_scales,
+                 const float *X, float *Y, int T, int d_model, int d_ff, int group,
+                 void *workspace, size_t workspace_bytes, void *stream)
+{
+    return ffn_batch_impl(2, gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X, Y, T,
+                          d_model, d_ff, group, workspace, workspace_bytes, stream);
 }
 
 int smoe_last_device_status(void *stream)

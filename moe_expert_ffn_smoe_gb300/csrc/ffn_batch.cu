@@ -216,7 +216,7 @@ size_t ffn_batch_workspace(int T, int d_model, int d_ff, int group)
     return (hidden + 255) & ~static_cast<size_t>(255);
 }
 
-cudaError_t launch_ffn_batch(const uint8_t *const gu_codes[2], const float *const gu_scales[2],
+cudaError_t launch_ffn_batch(int bits, const uint8_t *const gu_codes[2], const float *const gu_scales[2],
                              const uint8_t *down_codes, const float *down_scales, const float *X,
                              float *Y, int T, int d_model, int d_ff, int group, void *workspace,
                              cudaStream_t stream)
@@ -226,13 +226,16 @@ cudaError_t launch_ffn_batch(const uint8_t *const gu_codes[2], const float *cons
     const float *ds[2] = {down_scales, down_scales};
     cudaError_t e = cudaSuccess;
     if (T == 1) {
-        if (d_ff > 0) e = launch_qgemv(4, 2, gu_codes, gu_scales, X, H, d_ff, d_model, group, stream);
+        if (d_ff > 0) e = launch_qgemv(bits, 2, gu_codes, gu_scales, X, H, d_ff, d_model, group, stream);
         if (e != cudaSuccess) return e;
-        return launch_qgemv(4, 1, dc, ds, H, Y, d_model, d_ff, group, stream);
+        return launch_qgemv(bits, 1, dc, ds, H, Y, d_model, d_ff, group, stream);
     }
     if (tc_batch_supported(T, d_model, d_ff, group))
-        return launch_ffn_batch_tc(gu_codes, gu_scales, down_codes, down_scales, X, Y, T, d_model, d_ff, group,
-                                   workspace, stream);
+        return launch_ffn_batch_tc(bits, gu_codes, gu_scales, down_codes, down_scales, X, Y, T, d_model, d_ff,
+                                   group, workspace, stream);
+    // Q2 shapes (columns and groups multiples of 64) always take the
+    // tensor cores unless d_ff == 0, where Y = 0 and no code is read
+    if (bits != 4 && d_ff > 0) return cudaErrorInvalidValue;
     if (d_ff > 0)
         e = launch_qgemm_tokens(4, 2, gu_codes, gu_scales, X, H, T, d_ff, d_model, group, stream);
     if (e != cudaSuccess) return e;

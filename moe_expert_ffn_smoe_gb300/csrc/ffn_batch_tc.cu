@@ -53,7 +53,10 @@ namespace {
 
 constexpr int KT = 64;                        // columns per K tile (one group slice)
 constexpr int MT = 128;                       // accumulator rows per CTA tile
-constexpr int CHUNK_KT = 4;                   // K tiles per code chunk
+// K tiles per code chunk: a chunk row is 128 bytes of codes (Q4: 4 tiles
+// of 64 columns, Q2: 8).
+template <int BITS>
+constexpr int chunk_kt() { return 128 / (KT * BITS / 8); }
 constexpr uint32_t CHUNK_BYTES = MT * 128u;   // 128 rows x 128 bytes of Q4 codes
 constexpr int CODE_SLOTS = 3;
 constexpr int EPI_WARPS = 8;
@@ -64,7 +67,10 @@ constexpr int CODE_WARP = 17;
 constexpr int BPROD_WARP = 18;
 constexpr int TC_THREADS = 19 * 32;
 constexpr uint32_t A_BYTES = MT * KT * 2;
-constexpr float FOLD = 16.0f / 7.5f;  // 16/Z
+// A holds (c - Z) / DEN exactly (DEN = 16 at Q4, 4 at Q2), so per group
+// sum w x = s (DEN / Z) sum A x: FOLD = DEN / Z.
+template <int BITS>
+constexpr float fold() { return BITS == 4 ? 16.0f / 7.5f : 4.0f / 1.5f; }
 constexpr size_t kTcSmemBudget = 200 * 1024;
 
 // B block of one (token tile, K tile): hi [NT x 64] bf16, then lo.
@@ -89,10 +95,17 @@ __host__ __device__ __forceinline__ uint32_t core_off(int row, int k8)
     return static_cast<uint32_t>(((row >> 3) * 8 + k8) * 128 + (row & 7) * 16);
 }
 
-// Inside every 8-column block the K order is 0,4,1,5,2,6,3,7 (the order in
-// which a 32-bit word of Q4 codes unpacks to bf16 pairs); B uses the same
-// order, so the contraction is unchanged.
-__device__ __forceinline__ int perm8(int p) { return (p & 1) ? 4 + (p >> 1) : (p >> 1); }
+// The K order inside a tile follows the order in which a 32-bit code word
+// unpacks to bf16 pairs; B uses the same order, so the contraction is
+// unchanged.  Column of position p (0..7) of 8-column block kb of a tile:
+//  Q4: a word is 8 columns, one block, order 0,4,1,5,2,6,3,7;
+//  Q2: a word is 16 columns, two blocks, pairs (i, i + 8): block 2w holds
+//      0,8,1,9,2,10,3,11 of word w and block 2w + 1 holds 4,12,...,7,15.
+__host__ __device__ __forceinline__ int tile_col(int bits, int kb, int p)
+{
+    if (bits == 4) return 8 * kb + ((p & 1) ? 4 + (p >> 1) : (p >> 1));
+    return 16 * (kb >> 1) + 4 * (kb & 1) + (p >> 1) + 8 * (p & 1);
+}
 
 // tcgen05 shared-memory matrix descriptor, no swizzle, K-major:
 // LBO = distance between core matrices along K (128 B), SBO = between 8-row
@@ -191,6 +204,23 @@ __device__ __forceinline__ uint4 q4_word_to_bf16(uint32_t w)
     return r;
 }
 
+// One 32-bit word of Q2 codes (columns 0..15) as 16 exact bf16 values
+// (c - 1.5)/4 in pairs (i, i + 8): the bit pattern of 1 + c/4 (c in the top
+// two mantissa bits) minus 1 + 1.5/4 = 1.375.  lo: pairs 0..3, hi: 4..7.
+__device__ __forceinline__ void q2_word_to_bf16(uint32_t w, uint4 &lo, uint4 &hi)
+{
+    const uint32_t mag = 0x3F803F80u;  // 1.0, 1.0
+    const uint32_t off = 0x3FB03FB0u;  // 1.375, 1.375
+    lo.x = bf16x2_sub(((w << 5) & 0x00600060u) | mag, off);  // columns 0 and 8
+    lo.y = bf16x2_sub(((w << 3) & 0x00600060u) | mag, off);  // 1 and 9
+    lo.z = bf16x2_sub(((w << 1) & 0x00600060u) | mag, off);  // 2 and 10
+    lo.w = bf16x2_sub(((w >> 1) & 0x00600060u) | mag, off);  // 3 and 11
+    hi.x = bf16x2_sub(((w >> 3) & 0x00600060u) | mag, off);  // 4 and 12
+    hi.y = bf16x2_sub(((w >> 5) & 0x00600060u) | mag, off);  // 5 and 13
+    hi.z = bf16x2_sub(((w >> 7) & 0x00600060u) | mag, off);  // 6 and 14
+    hi.w = bf16x2_sub(((w >> 9) & 0x00600060u) | mag, off);  // 7 and 15
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
@@ -201,6 +231,13 @@ __device__ __forceinline__ uint4 lds128v(uint32_t addr)
 {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint2 lds64v(uint32_t addr)
+{
+    uint2 v;
+    asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
     return v;
 }
 
@@ -236,6 +273,7 @@ __device__ __forceinline__ void split8(const float (&v)[8], uint32_t (&hi)[4], u
 
 struct PrepArgs {
     const float *X;  // [T x K]
+    int bits;        // code width of the weights B is contracted with (K order)
     uint8_t *Bblk;   // [ntiles][K/64] blocks of b_bytes(nt)
     unsigned *count; // split-K counters of both GEMMs, zeroed here
     int ncount;
@@ -264,12 +302,23 @@ __global__ void __launch_bounds__(256) prep_tokens(PrepArgs a)
         const int k8 = kb % 8;
         float v[8];
         if (t < a.T) {
-            const float *src = a.X + static_cast<size_t>(t) * a.K + static_cast<size_t>(kb) * 8;
-            const float4 p0 = reinterpret_cast<const float4 *>(src)[0];
-            const float4 p1 = reinterpret_cast<const float4 *>(src)[1];
-            const float raw[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            const float *src = a.X + static_cast<size_t>(t) * a.K + static_cast<size_t>(kt) * KT;
+            if (a.bits == 4) {
+                // the block's 8 contiguous columns, permuted in registers
+                const float4 *q = reinterpret_cast<const float4 *>(src + 8 * k8);
+                const float4 p0 = q[0], p1 = q[1];
+                const float raw[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
 #pragma unroll
-            for (int p = 0; p < 8; ++p) v[p] = raw[perm8(p)];
+                for (int p = 0; p < 8; ++p) v[p] = raw[tile_col(4, k8, p) - 8 * k8];
+            } else {
+                // 8 of the 16 columns of the block's code word
+                const float4 *q = reinterpret_cast<const float4 *>(src + 16 * (k8 >> 1));
+                const float4 p0 = q[0], p1 = q[1], p2 = q[2], p3 = q[3];
+                const float raw[16] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w,
+                                       p2.x, p2.y, p2.z, p2.w, p3.x, p3.y, p3.z, p3.w};
+#pragma unroll
+                for (int p = 0; p < 8; ++p) v[p] = raw[tile_col(2, k8, p) - 16 * (k8 >> 1)];
+            }
         } else {
 #pragma unroll
             for (int p = 0; p < 8; ++p) v[p] = 0.f;
@@ -299,9 +348,11 @@ struct alignas(64) TcArgs {
     int K, group, T, ntiles, kps, nsplit;
 };
 
-template <int NT, bool GU>
+template <int BITS, int NT, bool GU>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ TcArgs a)
 {
+    constexpr int CHUNK_KT = chunk_kt<BITS>();
+    constexpr int TILE_BYTES = KT * BITS / 8;  // bytes of one row's codes per K tile
     constexpr int NB = accbufs_for(NT);
     constexpr uint32_t NCOLS = NB * 2 * NT;  // a power of two in [64, 512]
     constexpr int S = stages_for(NT);
@@ -363,7 +414,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
                     !mbar_wait_bounded(cempty0 + 8 * slot, ((c / CODE_SLOTS) - 1) & 1, a.status, 7u))
                     break;
                 const uint32_t dst = codes0 + slot * CHUNK_BYTES;
-                const int x = (kt0 + c * CHUNK_KT) * 32;  // byte offset along the row: multiple of 32
+                const int x = (kt0 + c * CHUNK_KT) * TILE_BYTES;  // byte offset along the row: multiple of 16
                 mbar_arrive_expect_tx(cfull0 + 8 * slot, CHUNK_BYTES);
                 if (GU) {
                     tma_load_2d(dst, &a.tmap[0], x, mtile * 64, cfull0 + 8 * slot);
@@ -418,11 +469,25 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
             const int s = i % S;
             if (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 5u)) break;
             const uint32_t row = codes0 + slot * CHUNK_BYTES + static_cast<uint32_t>(r) * 128u;
-            const uint4 w = lds128v(row + (((2u * sub + static_cast<uint32_t>(hf)) ^ rsw) << 4));
-            const uint32_t words[4] = {w.x, w.y, w.z, w.w};
             const uint32_t sa = stage0 + s * SB;
+            if (BITS == 4) {
+                // 16-byte unit 2 sub + hf of the (swizzled) chunk row: 4 words, one block each
+                const uint4 w = lds128v(row + (((2u * sub + static_cast<uint32_t>(hf)) ^ rsw) << 4));
+                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-            for (int j = 0; j < 4; ++j) sts128(sa + core_off(r, 4 * hf + j), q4_word_to_bf16(words[j]));
+                for (int j = 0; j < 4; ++j) sts128(sa + core_off(r, 4 * hf + j), q4_word_to_bf16(words[j]));
+            } else {
+                // half hf of 16-byte unit sub: 2 words, two blocks each
+                const uint2 w = lds64v(row + ((static_cast<uint32_t>(sub) ^ rsw) << 4) + 8u * hf);
+                const uint32_t words[2] = {w.x, w.y};
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    uint4 lo, hi;
+                    q2_word_to_bf16(words[j], lo, hi);
+                    sts128(sa + core_off(r, 4 * hf + 2 * j), lo);
+                    sts128(sa + core_off(r, 4 * hf + 2 * j + 1), hi);
+                }
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
@@ -450,7 +515,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
         float sc_next = (rok && nk > 0) ? ldg_f32(srow + (kt0 * KT) / a.group) : 0.f;
         for (int i = 0; i < nk; ++i) {
             const int b = i % NB;
-            const float f = sc_next * FOLD;
+            const float f = sc_next * fold<BITS>();
             if (i + 1 < nk) sc_next = rok ? ldg_f32(srow + ((kt0 + i + 1) * KT) / a.group) : 0.f;
             const bool ok = mbar_wait_bounded(accf0 + 8 * b, (i / NB) & 1, a.status, 6u);
             if (!__all_sync(FULL_MASK, ok)) break;
@@ -522,7 +587,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
                     const int t = ntile * NT + n;
                     float v[8];
 #pragma unroll
-                    for (int p = 0; p < 8; ++p) v[p] = t < a.T ? xch[n * 64 + k8 * 8 + perm8(p)] : 0.f;
+                    for (int p = 0; p < 8; ++p) v[p] = t < a.T ? xch[n * 64 + tile_col(BITS, k8, p)] : 0.f;
                     uint32_t hi[4], lo[4];
                     split8(v, hi, lo);
                     const uint32_t off = core_off(n, k8);
@@ -622,14 +687,16 @@ EncodeTiled encoder()
     return fn;
 }
 
-// Tensor map of packed Q4 codes [rows x K/2 bytes]: boxes of box_rows rows x
-// 128 bytes (4 K tiles), 128-byte swizzle, zero fill outside the matrix.
-bool encode_codes(CUtensorMap *map, const uint8_t *codes, int rows, int K, int box_rows)
+// Tensor map of packed codes [rows x K bits / 8 bytes]: boxes of box_rows
+// rows x 128 bytes (4 Q4 or 8 Q2 K tiles), 128-byte swizzle, zero fill
+// outside the matrix.
+bool encode_codes(CUtensorMap *map, const uint8_t *codes, int bits, int rows, int K, int box_rows)
 {
     EncodeTiled fn = encoder();
     if (!fn) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    const cuuint64_t row_bytes = static_cast<cuuint64_t>(K) * bits / 8;
+    const cuuint64_t dims[2] = {row_bytes, static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {row_bytes};
     const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
     const cuuint32_t estr[2] = {1u, 1u};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(codes), dims, strides, box, estr,
@@ -637,24 +704,30 @@ bool encode_codes(CUtensorMap *map, const uint8_t *codes, int rows, int K, int b
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int NT, bool GU>
+template <int BITS, int NT, bool GU>
 cudaError_t launch_gemm(const TcArgs &a, int mtiles, cudaStream_t stream)
 {
     const size_t smem = 1024 + CODE_SLOTS * CHUNK_BYTES + static_cast<size_t>(stages_for(NT)) * stage_bytes(NT) +
                         512;
-    auto k = tc_ffn<NT, GU>;
+    auto k = tc_ffn<BITS, NT, GU>;
     cudaError_t e = ensure_dynamic_smem(k, smem);
     if (e != cudaSuccess) return e;
     return launch_pdl(k, dim3(mtiles, a.ntiles, a.nsplit), dim3(TC_THREADS), smem, stream, a);
 }
 
-template <bool GU>
+template <int BITS, bool GU>
 cudaError_t launch_gemm_nt(int nt, const TcArgs &a, int mtiles, cudaStream_t stream)
 {
-    if (nt == 128) return launch_gemm<128, GU>(a, mtiles, stream);
-    if (nt == 64) return launch_gemm<64, GU>(a, mtiles, stream);
-    if (nt == 32) return launch_gemm<32, GU>(a, mtiles, stream);
-    return launch_gemm<16, GU>(a, mtiles, stream);
+    if (nt == 128) return launch_gemm<BITS, 128, GU>(a, mtiles, stream);
+    if (nt == 64) return launch_gemm<BITS, 64, GU>(a, mtiles, stream);
+    if (nt == 32) return launch_gemm<BITS, 32, GU>(a, mtiles, stream);
+    return launch_gemm<BITS, 16, GU>(a, mtiles, stream);
+}
+
+template <bool GU>
+cudaError_t launch_gemm_bits(int bits, int nt, const TcArgs &a, int mtiles, cudaStream_t stream)
+{
+    return bits == 4 ? launch_gemm_nt<4, GU>(nt, a, mtiles, stream) : launch_gemm_nt<2, GU>(nt, a, mtiles, stream);
 }
 
 }  // namespace
@@ -670,7 +743,7 @@ size_t tc_batch_workspace(int T, int d_model, int d_ff)
     return tc_layout(T, d_model, d_ff, sms < 152 ? 152 : sms).total;
 }
 
-cudaError_t launch_ffn_batch_tc(const uint8_t *const gu_codes[2], const float *const gu_scales[2],
+cudaError_t launch_ffn_batch_tc(int bits, const uint8_t *const gu_codes[2], const float *const gu_scales[2],
                                 const uint8_t *down_codes, const float *down_scales, const float *X, float *Y,
                                 int T, int d_model, int d_ff, int group, void *workspace, cudaStream_t stream)
 {
@@ -682,7 +755,7 @@ cudaError_t launch_ffn_batch_tc(const uint8_t *const gu_codes[2], const float *c
     unsigned *cnt = reinterpret_cast<unsigned *>(ws + L.cnt);
     const int ncount = (L.gu.mtiles + L.dn.mtiles) * L.ntiles;
 
-    PrepArgs p = {X, ws + L.xb, cnt, ncount, T, d_model, L.nt, L.ntiles};
+    PrepArgs p = {X, bits, ws + L.xb, cnt, ncount, T, d_model, L.nt, L.ntiles};
     {
         const long long total = static_cast<long long>(L.ntiles) * L.nt * (d_model / 8);
         long long blocks = (total + 255) / 256;
@@ -696,8 +769,8 @@ cudaError_t launch_ffn_batch_tc(const uint8_t *const gu_codes[2], const float *c
     }
 
     TcArgs a = {};
-    if (!encode_codes(&a.tmap[0], gu_codes[0], d_ff, d_model, 64) ||
-        !encode_codes(&a.tmap[1], gu_codes[1], d_ff, d_model, 64))
+    if (!encode_codes(&a.tmap[0], gu_codes[0], bits, d_ff, d_model, 64) ||
+        !encode_codes(&a.tmap[1], gu_codes[1], bits, d_ff, d_model, 64))
         return cudaErrorInvalidValue;
     a.scales[0] = gu_scales[0];
     a.scales[1] = gu_scales[1];
@@ -714,11 +787,11 @@ cudaError_t launch_ffn_batch_tc(const uint8_t *const gu_codes[2], const float *c
     a.ntiles = L.ntiles;
     a.kps = L.gu.kps;
     a.nsplit = L.gu.nsplit;
-    cudaError_t e = launch_gemm_nt<true>(L.nt, a, L.gu.mtiles, stream);
+    cudaError_t e = launch_gemm_bits<true>(bits, L.nt, a, L.gu.mtiles, stream);
     if (e != cudaSuccess) return e;
 
     TcArgs b = {};
-    if (!encode_codes(&b.tmap[0], down_codes, d_model, d_ff, MT)) return cudaErrorInvalidValue;
+    if (!encode_codes(&b.tmap[0], down_codes, bits, d_model, d_ff, MT)) return cudaErrorInvalidValue;
     b.tmap[1] = b.tmap[0];
     b.scales[0] = b.scales[1] = down_scales;
     b.B = ws + L.hb;
@@ -734,7 +807,7 @@ cudaError_t launch_ffn_batch_tc(const uint8_t *const gu_codes[2], const float *c
     b.ntiles = L.ntiles;
     b.kps = L.dn.kps;
     b.nsplit = L.dn.nsplit;
-    return launch_gemm_nt<false>(L.nt, b, L.dn.mtiles, stream);
+    return launch_gemm_bits<false>(bits, L.nt, b, L.dn.mtiles, stream);
 }
 
 }  // namespace smoe

@@ -66,7 +66,7 @@ cudaError_t launch_qgemm_tokens(int bits, int nmat, const uint8_t *const codes[2
 // gate/up, then for down).
 bool tc_batch_supported(int T, int d_model, int d_ff, int group);
 size_t tc_batch_workspace(int T, int d_model, int d_ff);
-cudaError_t launch_ffn_batch_tc(const uint8_t *const gu_codes[2], const float *const gu_scales[2],
+cudaError_t launch_ffn_batch_tc(int bits, const uint8_t *const gu_codes[2], const float *const gu_scales[2],
                                 const uint8_t *down_codes, const float *down_scales, const float *X, float *Y,
                                 int T, int d_model, int d_ff, int group, void *workspace, cudaStream_t stream);
 
@@ -74,7 +74,7 @@ cudaError_t launch_ffn_batch_tc(const uint8_t *const gu_codes[2], const float *c
 size_t ffn_batch_workspace(int T, int d_model, int d_ff, int group);
 
 // The whole batch FFN: gate/up into the workspace, then down into Y.
-cudaError_t launch_ffn_batch(const uint8_t *const gu_codes[2], const float *const gu_scales[2],
+cudaError_t launch_ffn_batch(int bits, const uint8_t *const gu_codes[2], const float *const gu_scales[2],
                              const uint8_t *down_codes, const float *down_scales,
                              const float *X, float *Y, int T, int d_model, int d_ff, int group,
                              void *workspace, cudaStream_t stream);

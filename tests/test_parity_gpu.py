@@ -280,14 +280,14 @@ def test_bf16_batch_70_entries(smoe, dev):
 
 # ---------------------------------------------------------------- token batch
 
-def _batch(smoe, dev, T, e, X, d_model, d_ff, group):
+def _batch(smoe, dev, T, e, X, d_model, d_ff, group, bits=4):
     t = {k: to_dev(v, dev) for k, v in e.items()}
     Y = torch.full((max(T, 1), d_model), float("nan"), device=dev)
     need = smoe.smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group)
     ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-    smoe.ffn_batch_q4(t["gate_codes"], t["gate_scales"], t["up_codes"], t["up_scales"],
-                      t["down_codes"], t["down_scales"], to_dev(X, dev), Y, T, d_model, d_ff, group,
-                      ws, need)
+    fn = smoe.ffn_batch_q4 if bits == 4 else smoe.ffn_batch_q2
+    fn(t["gate_codes"], t["gate_scales"], t["up_codes"], t["up_scales"],
+       t["down_codes"], t["down_scales"], to_dev(X, dev), Y, T, d_model, d_ff, group, ws, need)
     torch.cuda.synchronize()
     return Y.cpu().numpy()[:T]
 
@@ -332,6 +332,43 @@ def test_token_batch_ragged_shapes(smoe, dev, d_model, d_ff, group, T):
             e["down_codes"], e["down_scales"])
     _, ref, a = oracle.ffn_batch(*args, T, d_model, d_ff, group, X.astype(np.float64))
     check(Y, ref, a, f"batch {d_model}/{d_ff} g{group} T={T}")
+
+
+@pytest.mark.parametrize("T", [1, 2, 16, 64, 100, 256])
+def test_token_batch_q2(smoe, dev, T):
+    """Q2 codes through the same tiles: eight K tiles per code chunk, and the
+    Q2 order of columns inside a tile on both operands."""
+    d_model, d_ff, group = 4096, 1536, 64
+    e = inp.expert(2, d_model, d_ff, group, seed=8)
+    X = inp.activations((T, d_model), 8)
+    Y = _batch(smoe, dev, T, e, X, d_model, d_ff, group, bits=2)
+    toks = list(range(T)) if T <= 16 else sorted(set([0, 1, T - 1, T // 2] + list(
+        np.random.default_rng(T).integers(0, T, 6))))
+    args = (2, e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"],
+            e["down_codes"], e["down_scales"])
+    for tok in toks:
+        _, ref, a = oracle.ffn_batch(*args, T, d_model, d_ff, group, X.astype(np.float64), tok, 1)
+        check(Y[tok], ref[0], a[0], f"Q2 batch T={T} token {tok}")
+
+
+@pytest.mark.parametrize("d_model,d_ff,group,T", [
+    (320, 192, 64, 20),    # a chunk of 8 K tiles longer than the row: zero fill past the matrix
+    (512, 256, 128, 70),   # groups of 128 columns
+    (256, 0, 64, 5),       # no hidden columns: Y = 0
+])
+def test_token_batch_q2_ragged(smoe, dev, d_model, d_ff, group, T):
+    e = inp.expert(2, d_model, max(d_ff, 64), group, seed=32)
+    if d_ff == 0:
+        X = inp.activations((T, d_model), 32)
+        Y = _batch(smoe, dev, T, e, X, d_model, 0, group, bits=2)
+        assert (Y == 0).all()
+        return
+    X = inp.activations((T, d_model), 32)
+    Y = _batch(smoe, dev, T, e, X, d_model, d_ff, group, bits=2)
+    args = (2, e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"],
+            e["down_codes"], e["down_scales"])
+    _, ref, a = oracle.ffn_batch(*args, T, d_model, d_ff, group, X.astype(np.float64))
+    check(Y, ref, a, f"Q2 batch {d_model}/{d_ff} g{group} T={T}")
 
 
 # ------------------------------------------------------ ragged and edge cases
