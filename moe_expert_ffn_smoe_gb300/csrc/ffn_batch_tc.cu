@@ -21,15 +21,17 @@
 //    accumulators (512 columns), so the MMAs run ahead of the epilogue.
 //
 // Three launches per call, chained with programmatic dependent launch:
-//  1. prep_tokens: X -> B blocks (hi, lo per (token tile, K tile)) and
-//     zeroed split-K counters.
+//  1. prep_tokens: X -> B blocks (hi, lo per (token tile, K tile)).
 //  2. tc_ffn<NT, gate/up>: a CTA tile is 64 gate rows + the same 64 up rows
-//     (128 accumulator rows) over one K range.  The last CTA of a tile's K
-//     splits adds the partial sums in a fixed order, forms SiLU(g) * u and
-//     writes it directly as the B block of the down projection's K tile
-//     (64 hidden columns = one down K tile).
-//  3. tc_ffn<NT, down>: 128 down rows over one K range; the last split
-//     writes Y.
+//     (128 accumulator rows) over one K range.  The K splits of a tile form
+//     one thread-block cluster: each split leaves its partial sums in its
+//     shared memory, then split q adds token columns [q NT/S, (q+1) NT/S)
+//     of every split's partials (in split order, read through distributed
+//     shared memory), forms SiLU(g) * u and writes it directly as the B
+//     block of the down projection's K tile (64 hidden columns = one down K
+//     tile).
+//  3. tc_ffn<NT, down>: 128 down rows over one K range, split the same way;
+//     each split writes Y for its token columns.
 // Inside a GEMM CTA (608 threads): warps 0-7 epilogue (warp w reads TMEM
 // lane quarter w % 4 = 32 tile rows, columns of half w / 4), warps 8-15
 // convert codes to A tiles (thread = half a tile row: 4 of its 8 code
@@ -43,7 +45,9 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
@@ -269,14 +273,52 @@ __device__ __forceinline__ void split8(const float (&v)[8], uint32_t (&hi)[4], u
     }
 }
 
+// SiLU with the fast exponential and division intrinsics (relative error a
+// few units in the last place for |v| < 100, far inside the tolerance; 0
+// once exp(-v) overflows).
+__device__ __forceinline__ float silu_fast(float v) { return __fdividef(v, 1.0f + __expf(-v)); }
+
+// ---- thread-block cluster helpers (the K splits of a tile form a cluster)
+
+// All threads of all CTAs of the cluster: arrive (release) and wait
+// (acquire).  Every thread of the kernel executes each call exactly once.
+__device__ __forceinline__ void cluster_sync()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// The address of shared-memory location `addr` (this CTA's window) in the
+// shared memory of cluster rank `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, int rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 // ---------------------------------------------------------------- token prep
 
 struct PrepArgs {
     const float *X;  // [T x K]
     int bits;        // code width of the weights B is contracted with (K order)
     uint8_t *Bblk;   // [ntiles][K/64] blocks of b_bytes(nt)
-    unsigned *count; // split-K counters of both GEMMs, zeroed here
-    int ncount;
     int T, K, nt, ntiles;
 };
 
@@ -291,7 +333,6 @@ __global__ void __launch_bounds__(256) prep_tokens(PrepArgs a)
     const long long total = static_cast<long long>(a.ntiles) * a.nt * kb_per_t;  // multiple of 8
     const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
     const long long first = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (first < a.ncount) a.count[first] = 0u;
     const long long rounds = (total + stride - 1) / stride;
     for (long long rd = 0; rd < rounds; ++rd) {
         const long long idx = rd * stride + first;
@@ -339,14 +380,35 @@ struct alignas(64) TcArgs {
     CUtensorMap tmap[2];    // codes: gate and up rows (gate/up) or down rows (tmap[0])
     const float *scales[2];
     const uint8_t *B;       // token operand blocks [ntiles][K/64]
-    float *partial;         // split-K partial sums [mtiles][ntiles][nsplit][NT][MT]
-    unsigned *count;        // [mtiles][ntiles] arrivals of the K splits
     float *Y;               // down: [T x M]
     uint8_t *Hb;            // gate/up: down-operand blocks [ntiles][M/64]
     unsigned *status;
     int M;                  // rows per matrix (d_ff for gate/up, d_model for down)
     int K, group, T, ntiles, kps, nsplit;
 };
+
+// Gate/up finish: the hidden values of tokens [n0, n1) of this tile, src[(n -
+// n0) stride + c] for hidden column c (0..63), written as the bf16 hi/lo B
+// block of down K tile `mtile` (tokens past T as zeros).  Work item: (token,
+// 8-column block), spread over threads et = 0 .. nthreads - 1.
+template <int BITS, int NT>
+__device__ __forceinline__ void write_hidden_block(const TcArgs &a, const float *src, int stride, int mtile,
+                                                   int ntile, int n0, int n1, int et, int nthreads)
+{
+    uint8_t *blk = a.Hb + (static_cast<size_t>(ntile) * (a.M / KT) + mtile) * b_bytes(NT);
+    for (int it = et; it < (n1 - n0) * 8; it += nthreads) {
+        const int n = n0 + (it >> 3), k8 = it & 7;
+        const int t = ntile * NT + n;
+        float v[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) v[p] = t < a.T ? src[(n - n0) * stride + tile_col(BITS, k8, p)] : 0.f;
+        uint32_t hi[4], lo[4];
+        split8(v, hi, lo);
+        const uint32_t off = core_off(n, k8);
+        *reinterpret_cast<uint4 *>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+        *reinterpret_cast<uint4 *>(blk + static_cast<size_t>(NT) * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+    }
+}
 
 template <int BITS, int NT, bool GU>
 __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ TcArgs a)
@@ -358,7 +420,6 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
     constexpr int S = stages_for(NT);
     constexpr uint32_t SB = stage_bytes(NT);
     extern __shared__ uint8_t smem_raw[];
-    __shared__ int last_split;
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     const uint32_t codes0 = base;                              // CODE_SLOTS chunks, 1024-aligned
@@ -537,31 +598,8 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
             if (lane == 0) mbar_arrive(acce0 + 8 * b);
         }
 
-        // ---- K splits: every split stores its partial sums; the last one to
-        // arrive adds all of them in split order and finishes the tile.
-        bool finisher = true;
-        if (a.nsplit > 1) {
-            const size_t tile = static_cast<size_t>(mtile) * a.ntiles + ntile;
-            float *mine = a.partial + (tile * a.nsplit + split) * NT * MT;
-#pragma unroll
-            for (int n = 0; n < NH; ++n) mine[(h * NH + n) * MT + r] = y[n];
-            __threadfence();
-            named_barrier(1, EPI_WARPS * 32);
-            if (et == 0) last_split = atomicAdd(&a.count[tile], 1u) == static_cast<unsigned>(a.nsplit - 1);
-            named_barrier(1, EPI_WARPS * 32);
-            finisher = last_split != 0;
-            if (finisher) {
-                __threadfence();
-                const float *all = a.partial + tile * a.nsplit * NT * MT;
-#pragma unroll
-                for (int n = 0; n < NH; ++n) y[n] = 0.f;
-                for (int sp = 0; sp < a.nsplit; ++sp)
-#pragma unroll
-                    for (int n = 0; n < NH; ++n)
-                        y[n] += __ldcg(all + (static_cast<size_t>(sp) * NT + h * NH + n) * MT + r);
-            }
-        }
-        if (finisher) {
+        if (a.nsplit == 1) {
+            // the whole K range is here: finish the tile from registers
             if (GU) {
                 // rows 64..127 hold up for the hidden columns of rows 0..63:
                 // exchange through shared memory (the stages are idle now),
@@ -576,25 +614,11 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
 #pragma unroll
                     for (int n = 0; n < NH; ++n) {
                         float *p = xch + (h * NH + n) * 64 + r;
-                        *p = silu_f32(y[n]) * *p;
+                        *p = silu_fast(y[n]) * *p;
                     }
                 }
                 named_barrier(1, EPI_WARPS * 32);
-                // work item: (token n, 8-column block k8), NT * 8 of them
-                uint8_t *blk = a.Hb + (static_cast<size_t>(ntile) * (a.M / KT) + mtile) * b_bytes(NT);
-                for (int it = et; it < NT * 8; it += EPI_WARPS * 32) {
-                    const int n = it >> 3, k8 = it & 7;
-                    const int t = ntile * NT + n;
-                    float v[8];
-#pragma unroll
-                    for (int p = 0; p < 8; ++p) v[p] = t < a.T ? xch[n * 64 + tile_col(BITS, k8, p)] : 0.f;
-                    uint32_t hi[4], lo[4];
-                    split8(v, hi, lo);
-                    const uint32_t off = core_off(n, k8);
-                    *reinterpret_cast<uint4 *>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                    *reinterpret_cast<uint4 *>(blk + static_cast<size_t>(NT) * 128 + off) =
-                        make_uint4(lo[0], lo[1], lo[2], lo[3]);
-                }
+                write_hidden_block<BITS, NT>(a, xch, 64, mtile, ntile, 0, NT, et, EPI_WARPS * 32);
             } else if (rok) {
 #pragma unroll
                 for (int n = 0; n < NH; ++n) {
@@ -602,10 +626,90 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
                     if (t < a.T) a.Y[static_cast<size_t>(t) * a.M + row] = y[n];
                 }
             }
+        } else {
+            // this split's partial sums stay in its shared memory, [NT][MT]
+            // (the stages are idle now) for the split-K reduction below
+            float *mine = reinterpret_cast<float *>(smem_raw + (stage0 - raw));
+#pragma unroll
+            for (int n = 0; n < NH; ++n) mine[(h * NH + n) * MT + r] = y[n];
         }
     }
     tc_fence_before();
     __syncthreads();
+
+    if (a.nsplit > 1) {
+        // ---- split-K: the cluster is the tile's nsplit K splits.  Every
+        // thread of every split passes both cluster barriers, whatever its
+        // role and whether a wait gave up, so neither can be left waiting.
+        cluster_sync();  // every split's partials are in its shared memory
+        {
+            // every thread of the CTA takes part (the roles are done)
+            const int et = threadIdx.x;
+            constexpr int NTH = TC_THREADS;
+            const int ns = a.nsplit;
+            const int q = static_cast<int>(cluster_rank());
+            const int n0 = q * NT / ns, n1 = (q + 1) * NT / ns;
+            const uint32_t part0 = stage0;  // the same offset in every split
+            float *S = reinterpret_cast<float *>(smem_raw + (codes0 - raw));  // [n1 - n0][MT]
+            // work item: token n of this rank's columns, 4 consecutive rows;
+            // each sum is taken over the splits in split order.  Several
+            // items per thread at a time keep U x nsplit remote loads in flight.
+            const int items = (n1 - n0) * (MT / 4);
+            constexpr int U = 2;
+            for (int first = 0; first < items; first += U * NTH) {
+                float4 v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int sp = 0; sp < 8; ++sp) {
+                    if (sp >= ns) break;  // uniform
+                    float4 pv[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int it = first + u * NTH + et;
+                        pv[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (it < items) {
+                            const int n = n0 + (it >> 5), r4 = it & 31;
+                            pv[u] = ld_dsmem_f32x4(
+                                mapa_shared(part0 + static_cast<uint32_t>(n * MT + 4 * r4) * 4u, sp));
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        v[u].x += pv[u].x;
+                        v[u].y += pv[u].y;
+                        v[u].z += pv[u].z;
+                        v[u].w += pv[u].w;
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int it = first + u * NTH + et;
+                    if (it < items)
+                        reinterpret_cast<float4 *>(S)[((it >> 5) * MT + 4 * (it & 31)) >> 2] = v[u];
+                }
+            }
+            __syncthreads();
+            if (GU) {
+                // SiLU(gate row c) * up row c for the rank's tokens, in place
+                for (int it = et; it < (n1 - n0) * 64; it += NTH) {
+                    const int n = it >> 6, c = it & 63;
+                    float *g = S + n * MT + c;
+                    *g = silu_fast(*g) * g[64];
+                }
+                __syncthreads();
+                write_hidden_block<BITS, NT>(a, S, MT, mtile, ntile, n0, n1, et, NTH);
+            } else {
+                for (int it = et; it < (n1 - n0) * MT; it += NTH) {
+                    const int n = it >> 7, r = it & (MT - 1);
+                    const int t = ntile * NT + n0 + n;
+                    const int row = mtile * MT + r;
+                    if (t < a.T && row < a.M) a.Y[static_cast<size_t>(t) * a.M + row] = S[n * MT + r];
+                }
+            }
+        }
+        cluster_sync();  // no split leaves while another may still read its partials
+    }
     if (threadIdx.x == 0) pdl_launch_dependents();
     if (warp == MMA_WARP) {
         tc_fence_after();
@@ -623,14 +727,54 @@ struct GemmPlan {
     int mtiles, kps, nsplit;
 };
 
-// K splits so that mtiles * ntiles * splits fills about one wave of SMs.
-GemmPlan plan_gemm(int mtiles, int ntiles, int nkt, int sms)
+// Split clusters of a GEMM kernel that can be resident at once (one CTA per
+// SM; a cluster's CTAs share a GPC), cached per kernel and cluster size.
+template <typename K>
+int active_clusters(K kernel, size_t smem, int csize)
+{
+    static std::mutex mu;
+    static std::map<std::pair<const void *, int>, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    const auto key = std::make_pair(reinterpret_cast<const void *>(kernel), csize);
+    auto it = cache.find(key);
+    if (it == cache.end()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(1, 1, static_cast<unsigned>(csize));
+        cfg.blockDim = dim3(TC_THREADS);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = static_cast<unsigned>(csize);
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            n = -1;  // unknown: plan by SM count alone
+        }
+        it = cache.emplace(key, n).first;
+    }
+    return it->second;
+}
+
+// K splits (at most 8: a split set is one portable cluster) so that the
+// tiles' clusters fill about one wave of SMs.
+template <typename K>
+GemmPlan plan_gemm(K kernel, size_t smem, int mtiles, int ntiles, int nkt, int sms)
 {
     GemmPlan p = {mtiles, nkt, 1};
     const int base = mtiles * ntiles;
     int maxs = sms / (base > 0 ? base : 1);
-    if (maxs < 1) maxs = 1;
+    if (maxs > 8) maxs = 8;
     if (maxs > nkt) maxs = nkt;
+    while (maxs > 1) {
+        const int fit = active_clusters(kernel, smem, maxs);
+        if (fit < 0 || base <= fit) break;
+        --maxs;
+    }
+    if (maxs < 1) maxs = 1;
     p.kps = (nkt + maxs - 1) / maxs;
     p.nsplit = (nkt + p.kps - 1) / p.kps;
     return p;
@@ -638,32 +782,17 @@ GemmPlan plan_gemm(int mtiles, int ntiles, int nkt, int sms)
 
 struct TcLayout {
     int nt, ntiles;
-    GemmPlan gu, dn;
-    size_t xb, hb, pgu, pdn, cnt, total;
+    size_t xb, hb, total;
 };
 
-int sizing_sms()
-{
-    const DeviceInfo *dev = device_info();
-    return dev && dev->sm_count > 0 ? dev->sm_count : 152;
-}
-
-TcLayout tc_layout(int T, int d_model, int d_ff, int sms)
+TcLayout tc_layout(int T, int d_model, int d_ff)
 {
     TcLayout L = {};
     L.nt = pick_nt(T);
     L.ntiles = (T + L.nt - 1) / L.nt;
-    L.gu = plan_gemm(d_ff / KT, L.ntiles, d_model / KT, sms);
-    L.dn = plan_gemm((d_model + MT - 1) / MT, L.ntiles, d_ff / KT, sms);
-    const size_t tile_f = static_cast<size_t>(L.nt) * MT * sizeof(float);
     size_t off = 0;
     L.xb = off; off = align256(off + static_cast<size_t>(L.ntiles) * (d_model / KT) * b_bytes(L.nt));
     L.hb = off; off = align256(off + static_cast<size_t>(L.ntiles) * (d_ff / KT) * b_bytes(L.nt));
-    L.pgu = off;
-    if (L.gu.nsplit > 1) off = align256(off + static_cast<size_t>(L.gu.mtiles) * L.ntiles * L.gu.nsplit * tile_f);
-    L.pdn = off;
-    if (L.dn.nsplit > 1) off = align256(off + static_cast<size_t>(L.dn.mtiles) * L.ntiles * L.dn.nsplit * tile_f);
-    L.cnt = off; off = align256(off + static_cast<size_t>(L.gu.mtiles + L.dn.mtiles) * L.ntiles * sizeof(unsigned));
     L.total = off;
     return L;
 }
@@ -705,29 +834,35 @@ bool encode_codes(CUtensorMap *map, const uint8_t *codes, int bits, int rows, in
 }
 
 template <int BITS, int NT, bool GU>
-cudaError_t launch_gemm(const TcArgs &a, int mtiles, cudaStream_t stream)
+cudaError_t launch_gemm(const TcArgs &args, int mtiles, int sms, cudaStream_t stream)
 {
     const size_t smem = 1024 + CODE_SLOTS * CHUNK_BYTES + static_cast<size_t>(stages_for(NT)) * stage_bytes(NT) +
                         512;
     auto k = tc_ffn<BITS, NT, GU>;
     cudaError_t e = ensure_dynamic_smem(k, smem);
     if (e != cudaSuccess) return e;
-    return launch_pdl(k, dim3(mtiles, a.ntiles, a.nsplit), dim3(TC_THREADS), smem, stream, a);
+    TcArgs a = args;
+    const GemmPlan p = plan_gemm(k, smem, mtiles, a.ntiles, a.K / KT, sms);
+    a.kps = p.kps;
+    a.nsplit = p.nsplit;
+    return launch_pdl_cluster(k, dim3(mtiles, a.ntiles, a.nsplit), dim3(TC_THREADS), smem, stream,
+                              static_cast<unsigned>(a.nsplit), a);
 }
 
 template <int BITS, bool GU>
-cudaError_t launch_gemm_nt(int nt, const TcArgs &a, int mtiles, cudaStream_t stream)
+cudaError_t launch_gemm_nt(int nt, const TcArgs &a, int mtiles, int sms, cudaStream_t stream)
 {
-    if (nt == 128) return launch_gemm<BITS, 128, GU>(a, mtiles, stream);
-    if (nt == 64) return launch_gemm<BITS, 64, GU>(a, mtiles, stream);
-    if (nt == 32) return launch_gemm<BITS, 32, GU>(a, mtiles, stream);
-    return launch_gemm<BITS, 16, GU>(a, mtiles, stream);
+    if (nt == 128) return launch_gemm<BITS, 128, GU>(a, mtiles, sms, stream);
+    if (nt == 64) return launch_gemm<BITS, 64, GU>(a, mtiles, sms, stream);
+    if (nt == 32) return launch_gemm<BITS, 32, GU>(a, mtiles, sms, stream);
+    return launch_gemm<BITS, 16, GU>(a, mtiles, sms, stream);
 }
 
 template <bool GU>
-cudaError_t launch_gemm_bits(int bits, int nt, const TcArgs &a, int mtiles, cudaStream_t stream)
+cudaError_t launch_gemm_bits(int bits, int nt, const TcArgs &a, int mtiles, int sms, cudaStream_t stream)
 {
-    return bits == 4 ? launch_gemm_nt<4, GU>(nt, a, mtiles, stream) : launch_gemm_nt<2, GU>(nt, a, mtiles, stream);
+    return bits == 4 ? launch_gemm_nt<4, GU>(nt, a, mtiles, sms, stream)
+                     : launch_gemm_nt<2, GU>(nt, a, mtiles, sms, stream);
 }
 
 }  // namespace
@@ -739,8 +874,7 @@ bool tc_batch_supported(int T, int d_model, int d_ff, int group)
 
 size_t tc_batch_workspace(int T, int d_model, int d_ff)
 {
-    const int sms = sizing_sms();
-    return tc_layout(T, d_model, d_ff, sms < 152 ? 152 : sms).total;
+    return tc_layout(T, d_model, d_ff).total;
 }
 
 cudaError_t launch_ffn_batch_tc(int bits, const uint8_t *const gu_codes[2], const float *const gu_scales[2],
@@ -750,19 +884,15 @@ cudaError_t launch_ffn_batch_tc(int bits, const uint8_t *const gu_codes[2], cons
     const DeviceInfo *dev = device_info();
     if (!dev) return cudaErrorInvalidDevice;
     if (!encoder()) return cudaErrorNotSupported;
-    const TcLayout L = tc_layout(T, d_model, d_ff, dev->sm_count);
+    const TcLayout L = tc_layout(T, d_model, d_ff);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    unsigned *cnt = reinterpret_cast<unsigned *>(ws + L.cnt);
-    const int ncount = (L.gu.mtiles + L.dn.mtiles) * L.ntiles;
 
-    PrepArgs p = {X, bits, ws + L.xb, cnt, ncount, T, d_model, L.nt, L.ntiles};
+    PrepArgs p = {X, bits, ws + L.xb, T, d_model, L.nt, L.ntiles};
     {
         const long long total = static_cast<long long>(L.ntiles) * L.nt * (d_model / 8);
         long long blocks = (total + 255) / 256;
         const long long cap = static_cast<long long>(dev->sm_count) * 8;
         if (blocks > cap) blocks = cap;
-        const long long need = (ncount + 255) / 256;
-        if (blocks < need) blocks = need;
         if (blocks < 1) blocks = 1;
         cudaError_t e = launch_pdl(prep_tokens, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
         if (e != cudaSuccess) return e;
@@ -775,8 +905,6 @@ cudaError_t launch_ffn_batch_tc(int bits, const uint8_t *const gu_codes[2], cons
     a.scales[0] = gu_scales[0];
     a.scales[1] = gu_scales[1];
     a.B = ws + L.xb;
-    a.partial = reinterpret_cast<float *>(ws + L.pgu);
-    a.count = cnt;
     a.Y = nullptr;
     a.Hb = ws + L.hb;
     a.status = device_status_word();
@@ -785,9 +913,7 @@ cudaError_t launch_ffn_batch_tc(int bits, const uint8_t *const gu_codes[2], cons
     a.group = group;
     a.T = T;
     a.ntiles = L.ntiles;
-    a.kps = L.gu.kps;
-    a.nsplit = L.gu.nsplit;
-    cudaError_t e = launch_gemm_bits<true>(bits, L.nt, a, L.gu.mtiles, stream);
+    cudaError_t e = launch_gemm_bits<true>(bits, L.nt, a, d_ff / KT, dev->sm_count, stream);
     if (e != cudaSuccess) return e;
 
     TcArgs b = {};
@@ -795,8 +921,6 @@ cudaError_t launch_ffn_batch_tc(int bits, const uint8_t *const gu_codes[2], cons
     b.tmap[1] = b.tmap[0];
     b.scales[0] = b.scales[1] = down_scales;
     b.B = ws + L.hb;
-    b.partial = reinterpret_cast<float *>(ws + L.pdn);
-    b.count = cnt + static_cast<size_t>(L.gu.mtiles) * L.ntiles;
     b.Y = Y;
     b.Hb = nullptr;
     b.status = a.status;
@@ -805,9 +929,7 @@ cudaError_t launch_ffn_batch_tc(int bits, const uint8_t *const gu_codes[2], cons
     b.group = group;
     b.T = T;
     b.ntiles = L.ntiles;
-    b.kps = L.dn.kps;
-    b.nsplit = L.dn.nsplit;
-    return launch_gemm_bits<false>(bits, L.nt, b, L.dn.mtiles, stream);
+    return launch_gemm_bits<false>(bits, L.nt, b, (d_model + MT - 1) / MT, dev->sm_count, stream);
 }
 
 }  // namespace smoe

@@ -101,6 +101,29 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// launch_pdl with thread-block clusters of (1, 1, cluster_z) CTAs
+// (cluster_z == 1: no cluster attribute).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t stream, unsigned cluster_z, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = cluster_z;
+    cfg.attrs = attr;
+    cfg.numAttrs = cluster_z > 1 ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Opts a kernel into `bytes` of dynamic shared memory.  Static shared memory
 // counts against the default 48 KB too, so the limit is raised for any
 // nonzero size it does not already cover.  It is only ever raised: one
