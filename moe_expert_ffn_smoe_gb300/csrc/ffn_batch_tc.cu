@@ -327,6 +327,9 @@ struct PrepArgs {
 // are zeros.
 __global__ void __launch_bounds__(256) prep_tokens(PrepArgs a)
 {
+    // the next kernel may start its weight-only prologue now: everything it
+    // reads from this grid it reads after its own griddepcontrol.wait
+    pdl_launch_dependents();
     pdl_wait();
     const int kb_per_t = a.K / 8;
     const int nkt = a.K / KT;
@@ -371,7 +374,7 @@ __global__ void __launch_bounds__(256) prep_tokens(PrepArgs a)
         *reinterpret_cast<uint4 *>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4 *>(blk + static_cast<size_t>(a.nt) * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-    pdl_launch_dependents();
+
 }
 
 // ---------------------------------------------------------------- GEMM
@@ -465,6 +468,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_word;
+    // Gate/up lets the down projection start its weight-only prologue now (it
+    // lands on SMs this grid does not hold: one CTA fills an SM); whatever it
+    // reads from this grid, and whatever it overwrites that this grid reads,
+    // it touches only after its own griddepcontrol.wait.  The down projection
+    // triggers at its end: a following call's token prep started early only
+    // competed with it (measured).
+    if (GU && threadIdx.x == 0) pdl_launch_dependents();
 
     if (warp == CODE_WARP) {
         // ---- code chunks (weights never depend on an earlier kernel)
@@ -643,7 +653,9 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
         // role and whether a wait gave up, so neither can be left waiting.
         cluster_sync();  // every split's partials are in its shared memory
         {
-            // every thread of the CTA takes part (the roles are done)
+            // every thread of the CTA takes part (the roles are done); each
+            // writes outputs, so each first waits for the previous grid
+            pdl_wait();
             const int et = threadIdx.x;
             constexpr int NTH = TC_THREADS;
             const int ns = a.nsplit;
@@ -710,7 +722,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
         }
         cluster_sync();  // no split leaves while another may still read its partials
     }
-    if (threadIdx.x == 0) pdl_launch_dependents();
+    if (!GU && threadIdx.x == 0) pdl_launch_dependents();
     if (warp == MMA_WARP) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(NCOLS) : "memory");
