@@ -257,8 +257,9 @@ int matvec_bf16_batch(int n, const uint16_t *const *w, const float *const *x,
 
 /*
  * Bytes of device workspace ffn_batch_q4 and ffn_batch_q2 need for these
- * sizes (the hidden activations [T x d_ff] f32 and any partial sums),
- * rounded up to 256.
+ * sizes (the token operand and the hidden activations in the tensor-core
+ * operand form, or the hidden activations [T x d_ff] f32 on the CUDA-core
+ * path), rounded up to 256.
  * Returns 0 for T <= 0 and (size_t)-1 for sizes the call would refuse.
  */
 size_t smoe_ffn_batch_workspace_bytes(int T, int d_model, int d_ff, int group);
@@ -321,9 +322,8 @@ int ffn_batch_q2(const uint8_t *gate_codes, const float *gate_scales,
  * smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group), exceeds that size
  * are refused with SMOE_ERR_SHAPE before anything is launched (at
  * d_model = 4096, d_ff = 1536 every T up to 256 fits; for T >= 2 the
- * workspace holds the split token operands of the tensor-core path, the
- * hidden activations in the down projection's operand form and the split-K
- * partial sums).
+ * workspace holds the split token operands of the tensor-core path and the
+ * hidden activations in the down projection's operand form).
  * The function calls no cudaMalloc, cudaFree or other allocating routine.
  *
  * The first call on a device looks up the array's device address with
