@@ -452,11 +452,12 @@ def rows_breakdown(smoe, dev, steps, pattern=""):
     out = {}
     s = torch.cuda.Stream(device=dev)
 
-    def timed(launch, n):
+    def timed(launch, n, calls_per=1):
+        """calls_per: C-ABI calls one launch(i) makes (sizes the stream hold)."""
         with torch.cuda.stream(s):
             for i in range(3):
                 launch(i)
-            return time_steps(lambda k: [launch(i) for i in range(k)], n, s, hold=n)
+            return time_steps(lambda k: [launch(i) for i in range(k)], n, s, hold=n * calls_per)
 
     if pattern in "q2_8expert_decode":
         q2_row(smoe, dev, steps, out, hbm_peak)
@@ -471,6 +472,8 @@ def rows_breakdown(smoe, dev, steps, pattern=""):
     for T in (16, 256):
         if pattern in f"q2_token_batch_T{T}":
             batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T, bits=2)
+    if pattern in "q4_experts_batch_8xT16":
+        experts_batch_row(smoe, dev, steps, out, hbm_peak, timed, s)
     if pattern in "q4_ffn_256":
         small_row(smoe, dev, steps, out, timed, s)
     return out
@@ -526,7 +529,7 @@ def bf16_batch_row(smoe, dev, steps, out, hbm_peak, timed, s, n=8, rows=512, col
         for j in range(n):
             smoe.matvec_bf16(ws[i % ncp][j], xs[j], ys[j], rows, cols, stream=s)
 
-    t_s = timed(singles, nl)
+    t_s = timed(singles, nl, calls_per=n)
     b = n * (rows * cols * 2 + cols * 4 + rows * 4)
     out[f"bf16_batch_{n}x{rows}x{cols}"] = {
         "GB/s": round(b * nl / t_b / 1e9, 1), "us_per_call": round(t_b / nl * 1e6, 3),
@@ -561,6 +564,44 @@ def batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T, bits=4):
                                    "frac": round(b * nl / t / 1e9 / hbm_peak, 4),
                                    "TFLOP/s": round(flops * nl / t / 1e12, 2), "bytes_per_call": b}
     del experts
+    torch.cuda.empty_cache()
+
+
+def experts_batch_row(smoe, dev, steps, out, hbm_peak, timed, s, n=8, T=16):
+    """Token batches of n experts (T tokens each) in one smoe_experts_ffn_batch_q4
+    call, against the same batches as n ffn_batch_q4 calls."""
+    import torch
+    ncp = 4  # weight sets of n experts, rotated: 4 x 8 x 10.6 MB > L2
+    sets = [[{k: torch.from_numpy(v).to(dev) for k, v in inp.expert(4, D_MODEL, D_FF, GROUP, 9 + 1000 * c, e).items()}
+             for e in range(n)] for c in range(ncp)]
+    Xs = [torch.from_numpy(inp.activations((T, D_MODEL), 9 + e)).to(dev) for e in range(n)]
+    Ys = [torch.empty((T, D_MODEL), device=dev) for _ in range(n)]
+    Ts = [T] * n
+    need = smoe.smoe_experts_ffn_batch_workspace_bytes(Ts, D_MODEL, D_FF, GROUP)
+    ws = torch.empty(need, dtype=torch.uint8, device=dev)
+    key = ("gate_codes", "gate_scales", "up_codes", "up_scales", "down_codes", "down_scales")
+
+    def grouped(i):
+        ex = sets[i % ncp]
+        smoe.smoe_experts_ffn_batch_q4(*[[x[k] for x in ex] for k in key], Xs, Ys, Ts, D_MODEL, D_FF, GROUP,
+                                       ws, need, stream=s)
+
+    need1 = smoe.smoe_ffn_batch_workspace_bytes(T, D_MODEL, D_FF, GROUP)
+    ws1 = torch.empty(need1, dtype=torch.uint8, device=dev)
+
+    def singles(i):
+        for e, x in enumerate(sets[i % ncp]):
+            smoe.ffn_batch_q4(*[x[k] for k in key], Xs[e], Ys[e], T, D_MODEL, D_FF, GROUP, ws1, need1, stream=s)
+
+    nl = max(20, min(steps // 8, 200))
+    t_g = timed(grouped, nl)
+    t_s = timed(singles, nl, calls_per=n)
+    b = n * (expert_bytes(4) + 2 * T * D_MODEL * 4)
+    out[f"q4_experts_batch_{n}xT{T}"] = {
+        "GB/s": round(b * nl / t_g / 1e9, 1), "us_per_call": round(t_g / nl * 1e6, 3),
+        "frac": round(b * nl / t_g / 1e9 / hbm_peak, 4), "bytes_per_call": b,
+        "single_calls_us": round(t_s / nl * 1e6, 3)}
+    del sets
     torch.cuda.empty_cache()
 
 

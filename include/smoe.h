@@ -304,6 +304,49 @@ int ffn_batch_q2(const uint8_t *gate_codes, const float *gate_scales,
                  int T, int d_model, int d_ff, int group,
                  void *workspace, size_t workspace_bytes, void *stream);
 
+/*
+ * Token batches of several experts in one submission ("Token-Batch Fused
+ * FFN", applied per claimed expert: every expert with routed tokens gets its
+ * own token matrix): for e in [0, n_experts), expert e's FFN over its T[e]
+ * tokens,
+ *
+ *   Y[e][t] = down_e . (SiLU(gate_e . X[e][t]) * (up_e . X[e][t])),  t < T[e].
+ *
+ * gate_codes .. down_scales: host arrays of n_experts device pointers, each
+ * expert laid out as for ffn_batch_q4 / ffn_batch_q2; X, Y: host arrays of
+ * device pointers to f32 [T[e] x d_model]; T: host array of token counts
+ * (>= 0; an expert with T[e] == 0 is skipped and may hold null pointers).
+ * One shape (d_model, d_ff, group) for all experts.  When d_model, d_ff and
+ * group are multiples of 64 every expert's token tiles share one grid per
+ * 32 experts (three launches), so many small batches pay one launch ramp;
+ * other shapes run expert after expert.  workspace: at least
+ * smoe_experts_ffn_batch_workspace_bytes(n_experts, T, d_model, d_ff, group)
+ * bytes, 16-byte aligned, caller-owned, contents unspecified on return.
+ * No output may overlap any input, the workspace or another output.
+ */
+size_t smoe_experts_ffn_batch_workspace_bytes(int n_experts, const int *T,
+                                              int d_model, int d_ff, int group);
+int smoe_experts_ffn_batch_q4(int n_experts, const uint8_t *const *gate_codes,
+                              const float *const *gate_scales,
+                              const uint8_t *const *up_codes,
+                              const float *const *up_scales,
+                              const uint8_t *const *down_codes,
+                              const float *const *down_scales,
+                              const float *const *X, float *const *Y,
+                              const int *T, int d_model, int d_ff, int group,
+                              void *workspace, size_t workspace_bytes,
+                              void *stream);
+int smoe_experts_ffn_batch_q2(int n_experts, const uint8_t *const *gate_codes,
+                              const float *const *gate_scales,
+                              const uint8_t *const *up_codes,
+                              const float *const *up_scales,
+                              const uint8_t *const *down_codes,
+                              const float *const *down_scales,
+                              const float *const *X, float *const *Y,
+                              const int *T, int d_model, int d_ff, int group,
+                              void *workspace, size_t workspace_bytes,
+                              void *stream);
+
 /* Size of the device array ffn_batch_q4_noalloc uses as its workspace. */
 #define SMOE_NOALLOC_SCRATCH_BYTES (32u << 20)
 

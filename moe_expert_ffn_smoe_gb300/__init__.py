@@ -60,6 +60,9 @@ _SIGS = {
     "smoe_ffn_batch_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "ffn_batch_q4": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "ffn_batch_q2": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "smoe_experts_ffn_batch_workspace_bytes": ([_I, _P, _I, _I, _I], _SZ),
+    "smoe_experts_ffn_batch_q4": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
+    "smoe_experts_ffn_batch_q2": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
     "ffn_batch_q4_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "smoe_last_device_status": ([_P], _I),
 }
@@ -245,6 +248,38 @@ def ffn_batch_q2(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_
                              _ptr(down_codes), _ptr(down_scales), _ptr(X), _ptr(Y), T, d_model,
                              d_ff, group, _ptr(workspace), workspace_bytes, _stream(stream)),
            "ffn_batch_q2")
+
+
+def smoe_experts_ffn_batch_workspace_bytes(T, d_model, d_ff, group):
+    """T: list of per-expert token counts."""
+    t = (ctypes.c_int * max(1, len(T)))(*T)
+    return _lib.smoe_experts_ffn_batch_workspace_bytes(len(T), t, d_model, d_ff, group)
+
+
+def _experts_batch(fn, name, gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X, Y, T,
+                   d_model, d_ff, group, workspace, workspace_bytes, stream):
+    n = len(T)
+    lists = (gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X, Y)
+    if any(len(v) != n for v in lists):
+        raise ValueError(f"{name}: per-expert lists differ in length")
+    arrs = [_ptr_array(v) for v in lists]
+    t = (ctypes.c_int * max(1, n))(*T)
+    _check(fn(n, *arrs, t, d_model, d_ff, group, _ptr(workspace), workspace_bytes, _stream(stream)), name)
+
+
+def smoe_experts_ffn_batch_q4(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X, Y, T,
+                              d_model, d_ff, group, workspace, workspace_bytes, stream=None):
+    """Per-expert lists of tensors (X[e], Y[e]: [T[e], d_model]) and token counts T."""
+    _experts_batch(_lib.smoe_experts_ffn_batch_q4, "smoe_experts_ffn_batch_q4", gate_codes, gate_scales,
+                   up_codes, up_scales, down_codes, down_scales, X, Y, T, d_model, d_ff, group, workspace,
+                   workspace_bytes, stream)
+
+
+def smoe_experts_ffn_batch_q2(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X, Y, T,
+                              d_model, d_ff, group, workspace, workspace_bytes, stream=None):
+    _experts_batch(_lib.smoe_experts_ffn_batch_q2, "smoe_experts_ffn_batch_q2", gate_codes, gate_scales,
+                   up_codes, up_scales, down_codes, down_scales, X, Y, T, d_model, d_ff, group, workspace,
+                   workspace_bytes, stream)
 
 
 def ffn_batch_q4_noalloc(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X,

@@ -319,6 +319,63 @@ int ffn_batch_impl(int bits, const uint8_t *gate_codes, const float *gate_scales
                                             static_cast<cudaStream_t>(stream)));
 }
 
+// smoe_experts_ffn_batch_q4/q2: per-expert checks, then the grouped
+// token-batch launches.
+int experts_batch_impl(int bits, int n, const uint8_t *const *gc, const float *const *gs,
+                       const uint8_t *const *uc, const float *const *us, const uint8_t *const *dc,
+                       const float *const *ds, const float *const *X, float *const *Y, const int *T, int d_model,
+                       int d_ff, int group, void *workspace, size_t ws_bytes, void *stream)
+{
+    if (n < 0) return SMOE_ERR_SHAPE;
+    int st = check_q_shape(bits, d_ff, d_model, group);
+    if (st != SMOE_OK) return st;
+    st = check_q_shape(bits, d_model, d_ff, group);
+    if (st != SMOE_OK) return st;
+    if (n == 0 || d_model == 0) return SMOE_OK;
+    if (!T) return SMOE_ERR_NULL;
+    bool any = false;
+    for (int e = 0; e < n; ++e) {
+        if (T[e] < 0) return SMOE_ERR_SHAPE;
+        any = any || T[e] > 0;
+    }
+    if (!any) return SMOE_OK;
+    if (!gc || !gs || !uc || !us || !dc || !ds || !X || !Y) return SMOE_ERR_NULL;
+    const size_t need = smoe::ffn_batch_workspace_experts(n, T, d_model, d_ff, group);
+    if (need > 0) {
+        if (!workspace || ws_bytes < need) return SMOE_ERR_WORKSPACE;
+        if (!aligned16(workspace)) return SMOE_ERR_ALIGN;
+    }
+    const Span w = {workspace, need};
+    for (int e = 0; e < n; ++e) {
+        if (T[e] == 0) continue;
+        const void *ptrs[8] = {gc[e], gs[e], uc[e], us[e], dc[e], ds[e], X[e], Y[e]};
+        for (const void *p : ptrs) {
+            if (!p) return SMOE_ERR_NULL;
+            if (!aligned16(p)) return SMOE_ERR_ALIGN;
+        }
+    }
+    // every output against every input, the workspace and the other outputs
+    for (int e = 0; e < n; ++e) {
+        if (T[e] == 0) continue;
+        const Span o = {Y[e], static_cast<size_t>(T[e]) * static_cast<size_t>(d_model) * sizeof(float)};
+        if (need > 0 && overlap(o, w)) return SMOE_ERR_ALIAS;
+        for (int f = 0; f < n; ++f) {
+            if (T[f] == 0) continue;
+            const Span ins[7] = {{gc[f], q_bytes(bits, d_ff, d_model)}, {gs[f], scale_bytes(d_ff, d_model, group)},
+                                 {uc[f], q_bytes(bits, d_ff, d_model)}, {us[f], scale_bytes(d_ff, d_model, group)},
+                                 {dc[f], q_bytes(bits, d_model, d_ff)}, {ds[f], scale_bytes(d_model, d_ff, group)},
+                                 {X[f], static_cast<size_t>(T[f]) * static_cast<size_t>(d_model) * sizeof(float)}};
+            for (const Span &in : ins)
+                if (overlap(o, in) || (need > 0 && overlap(w, in))) return SMOE_ERR_ALIAS;
+            if (f > e && overlap(o, Span{Y[f], static_cast<size_t>(T[f]) * static_cast<size_t>(d_model) *
+                                                   sizeof(float)}))
+                return SMOE_ERR_ALIAS;
+        }
+    }
+    return to_status(smoe::launch_ffn_batch_experts(bits, n, gc, gs, uc, us, dc, ds, X, Y, T, d_model, d_ff, group,
+                                                    workspace, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 
 extern "C" {
@@ -494,6 +551,38 @@ int ffn_batch_q2(const uint8_t *gate_codes, const float *gate_scales, const uint
 {
     return ffn_batch_impl(2, gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales, X, Y, T,
                           d_model, d_ff, group, workspace, workspace_bytes, stream);
+}
+
+size_t smoe_experts_ffn_batch_workspace_bytes(int n_experts, const int *T, int d_model, int d_ff, int group)
+{
+    if (n_experts <= 0) return 0;
+    if (!T) return static_cast<size_t>(-1);
+    // the Q4 layout rules (Q2's are stricter: a Q2 shape passes them too)
+    if (check_q_shape(4, d_ff, d_model, group) != SMOE_OK || check_q_shape(4, d_model, d_ff, group) != SMOE_OK)
+        return static_cast<size_t>(-1);
+    for (int e = 0; e < n_experts; ++e)
+        if (T[e] < 0) return static_cast<size_t>(-1);
+    return smoe::ffn_batch_workspace_experts(n_experts, T, d_model, d_ff, group);
+}
+
+int smoe_experts_ffn_batch_q4(int n_experts, const uint8_t *const *gate_codes, const float *const *gate_scales,
+                              const uint8_t *const *up_codes, const float *const *up_scales,
+                              const uint8_t *const *down_codes, const float *const *down_scales,
+                              const float *const *X, float *const *Y, const int *T, int d_model, int d_ff,
+                              int group, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return experts_batch_impl(4, n_experts, gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales,
+                              X, Y, T, d_model, d_ff, group, workspace, workspace_bytes, stream);
+}
+
+int smoe_experts_ffn_batch_q2(int n_experts, const uint8_t *const *gate_codes, const float *const *gate_scales,
+                              const uint8_t *const *up_codes, const float *const *up_scales,
+                              const uint8_t *const *down_codes, const float *const *down_scales,
+                              const float *const *X, float *const *Y, const int *T, int d_model, int d_ff,
+                              int group, void *workspace, size_t workspace_bytes, void *stream)
+{
+    return experts_batch_impl(2, n_experts, gate_codes, gate_scales, up_codes, up_scales, down_codes, down_scales,
+                              X, Y, T, d_model, d_ff, group, workspace, workspace_bytes, stream);
 }
 
 int smoe_last_device_status(void *stream)

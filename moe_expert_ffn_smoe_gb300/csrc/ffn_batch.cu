@@ -242,6 +242,39 @@ cudaError_t launch_ffn_batch(int bits, const uint8_t *const gu_codes[2], const f
     return launch_qgemm_tokens(4, 1, dc, ds, H, Y, T, d_model, d_ff, group, stream);
 }
 
+size_t ffn_batch_workspace_experts(int n, const int *T, int d_model, int d_ff, int group)
+{
+    if (tc_batch_shape_supported(d_model, d_ff, group)) return tc_batch_workspace_experts(n, T, d_model, d_ff);
+    size_t need = 0;
+    for (int e = 0; e < n; ++e) {
+        const size_t w = ffn_batch_workspace(T[e], d_model, d_ff, group);
+        need = w > need ? w : need;
+    }
+    return need;
+}
+
+cudaError_t launch_ffn_batch_experts(int bits, int n, const uint8_t *const *gc, const float *const *gs,
+                                     const uint8_t *const *uc, const float *const *us,
+                                     const uint8_t *const *dc, const float *const *ds, const float *const *X,
+                                     float *const *Y, const int *T, int d_model, int d_ff, int group,
+                                     void *workspace, cudaStream_t stream)
+{
+    if (tc_batch_shape_supported(d_model, d_ff, group))
+        return launch_ffn_batch_tc_experts(bits, n, gc, gs, uc, us, dc, ds, X, Y, T, d_model, d_ff, group,
+                                           workspace, stream);
+    // one expert after another; each call's kernels finish reading the
+    // workspace before the next call's first kernel writes it (stream order)
+    for (int e = 0; e < n; ++e) {
+        if (T[e] <= 0) continue;
+        const uint8_t *guc[2] = {gc[e], uc[e]};
+        const float *gus[2] = {gs[e], us[e]};
+        cudaError_t err = launch_ffn_batch(bits, guc, gus, dc[e], ds[e], X[e], Y[e], T[e], d_model, d_ff, group,
+                                           workspace, stream);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
+}
+
 unsigned *device_status_word()
 {
     constexpr int kMaxDevices = 64;

@@ -76,6 +76,7 @@ constexpr uint32_t A_BYTES = MT * KT * 2;
 template <int BITS>
 constexpr float fold() { return BITS == 4 ? 16.0f / 7.5f : 4.0f / 1.5f; }
 constexpr size_t kTcSmemBudget = 200 * 1024;
+constexpr int TC_MAX_EXPERTS = 32;  // experts per launch (grouped token batch)
 
 // B block of one (token tile, K tile): hi [NT x 64] bf16, then lo.
 __host__ __device__ constexpr uint32_t b_bytes(int nt) { return static_cast<uint32_t>(nt) * 256u; }
@@ -313,19 +314,34 @@ __device__ __forceinline__ float4 ld_dsmem_f32x4(uint32_t addr)
     return v;
 }
 
+// The expert owning global token tile g: the last e with tile0[e] <= g.
+__device__ __forceinline__ int expert_of_tile(const int *tile0, int n, int g)
+{
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile0[mid] <= g) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
 // ---------------------------------------------------------------- token prep
 
 struct PrepArgs {
-    const float *X;  // [T x K]
+    const float *X[TC_MAX_EXPERTS];   // expert e's tokens [T[e] x K]
+    int T[TC_MAX_EXPERTS];
+    int tile0[TC_MAX_EXPERTS + 1];    // first global token tile of each expert
+    int n;                            // experts
     int bits;        // code width of the weights B is contracted with (K order)
-    uint8_t *Bblk;   // [ntiles][K/64] blocks of b_bytes(nt)
-    int T, K, nt, ntiles;
+    uint8_t *Bblk;   // [ntiles][K/64] blocks of b_bytes(nt), global token tiles
+    int K, nt, ntiles;
 };
 
-// One thread per (token, 8-column block): the token's 8 values split into
-// bf16 hi/lo in the tile layout.  Tokens past T (padding of the last tile)
-// are zeros.
-__global__ void __launch_bounds__(256) prep_tokens(PrepArgs a)
+// One thread per (token slot of a global tile, 8-column block): the token's 8
+// values split into bf16 hi/lo in the tile layout.  Slots past an expert's T
+// (padding of its last tile) are zeros.
+__global__ void __launch_bounds__(256) prep_tokens(const __grid_constant__ PrepArgs a)
 {
     // the next kernel may start its weight-only prologue now: everything it
     // reads from this grid it reads after its own griddepcontrol.wait
@@ -340,13 +356,16 @@ __global__ void __launch_bounds__(256) prep_tokens(PrepArgs a)
     for (long long rd = 0; rd < rounds; ++rd) {
         const long long idx = rd * stride + first;
         if (idx >= total) break;
-        const int t = static_cast<int>(idx / kb_per_t);
+        const int slot = static_cast<int>(idx / kb_per_t);  // global token slot
         const int kb = static_cast<int>(idx % kb_per_t);
         const int kt = kb / 8;
         const int k8 = kb % 8;
+        const int gt = slot / a.nt;
+        const int e = expert_of_tile(a.tile0, a.n, gt);
+        const int t = (gt - a.tile0[e]) * a.nt + slot % a.nt;  // the expert's token
         float v[8];
-        if (t < a.T) {
-            const float *src = a.X + static_cast<size_t>(t) * a.K + static_cast<size_t>(kt) * KT;
+        if (t < a.T[e]) {
+            const float *src = a.X[e] + static_cast<size_t>(t) * a.K + static_cast<size_t>(kt) * KT;
             if (a.bits == 4) {
                 // the block's 8 contiguous columns, permuted in registers
                 const float4 *q = reinterpret_cast<const float4 *>(src + 8 * k8);
@@ -369,42 +388,48 @@ __global__ void __launch_bounds__(256) prep_tokens(PrepArgs a)
         }
         uint32_t hi[4], lo[4];
         split8(v, hi, lo);
-        uint8_t *blk = a.Bblk + (static_cast<size_t>(t / a.nt) * nkt + kt) * b_bytes(a.nt);
-        const uint32_t off = core_off(t % a.nt, k8);
+        uint8_t *blk = a.Bblk + (static_cast<size_t>(gt) * nkt + kt) * b_bytes(a.nt);
+        const uint32_t off = core_off(slot % a.nt, k8);
         *reinterpret_cast<uint4 *>(blk + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
         *reinterpret_cast<uint4 *>(blk + static_cast<size_t>(a.nt) * 128 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
     }
-
 }
 
 // ---------------------------------------------------------------- GEMM
 
+// One GEMM launch over the token tiles of n experts: global token tile g
+// belongs to the expert e with tile0[e] <= g < tile0[e + 1].
 struct alignas(64) TcArgs {
-    CUtensorMap tmap[2];    // codes: gate and up rows (gate/up) or down rows (tmap[0])
-    const float *scales[2];
-    const uint8_t *B;       // token operand blocks [ntiles][K/64]
-    float *Y;               // down: [T x M]
+    CUtensorMap tmap[TC_MAX_EXPERTS][2];  // codes: gate and up rows (gate/up) or down rows ([e][0])
+    const float *scales[TC_MAX_EXPERTS][2];
+    float *Y[TC_MAX_EXPERTS];             // down: [T[e] x M]
+    int T[TC_MAX_EXPERTS];
+    int tile0[TC_MAX_EXPERTS + 1];
+    const uint8_t *B;       // token operand blocks [ntiles][K/64] (global tiles)
     uint8_t *Hb;            // gate/up: down-operand blocks [ntiles][M/64]
     unsigned *status;
+    int n;                  // experts
     int M;                  // rows per matrix (d_ff for gate/up, d_model for down)
-    int K, group, T, ntiles, kps, nsplit;
+    int K, group, ntiles, kps, nsplit;
 };
 
-// Gate/up finish: the hidden values of tokens [n0, n1) of this tile, src[(n -
-// n0) stride + c] for hidden column c (0..63), written as the bf16 hi/lo B
-// block of down K tile `mtile` (tokens past T as zeros).  Work item: (token,
+// Gate/up finish: the hidden values of tokens [n0, n1) of this tile (global
+// token tile gtile, the expert's tile ltile of an expert with Te tokens),
+// src[(n - n0) stride + c] for hidden column c (0..63), written as the bf16
+// hi/lo B block of down K tile `mtile` (tokens past Te as zeros).  Work item: (token,
 // 8-column block), spread over threads et = 0 .. nthreads - 1.
 template <int BITS, int NT>
 __device__ __forceinline__ void write_hidden_block(const TcArgs &a, const float *src, int stride, int mtile,
-                                                   int ntile, int n0, int n1, int et, int nthreads)
+                                                   int gtile, int ltile, int Te, int n0, int n1, int et,
+                                                   int nthreads)
 {
-    uint8_t *blk = a.Hb + (static_cast<size_t>(ntile) * (a.M / KT) + mtile) * b_bytes(NT);
+    uint8_t *blk = a.Hb + (static_cast<size_t>(gtile) * (a.M / KT) + mtile) * b_bytes(NT);
     for (int it = et; it < (n1 - n0) * 8; it += nthreads) {
         const int n = n0 + (it >> 3), k8 = it & 7;
-        const int t = ntile * NT + n;
+        const int t = ltile * NT + n;
         float v[8];
 #pragma unroll
-        for (int p = 0; p < 8; ++p) v[p] = t < a.T ? src[(n - n0) * stride + tile_col(BITS, k8, p)] : 0.f;
+        for (int p = 0; p < 8; ++p) v[p] = t < Te ? src[(n - n0) * stride + tile_col(BITS, k8, p)] : 0.f;
         uint32_t hi[4], lo[4];
         split8(v, hi, lo);
         const uint32_t off = core_off(n, k8);
@@ -435,7 +460,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int mtile = blockIdx.x;
-    const int ntile = blockIdx.y;
+    const int gtile = blockIdx.y;  // global token tile
+    const int xe = expert_of_tile(a.tile0, a.n, gtile);
+    const int ltile = gtile - a.tile0[xe];  // the expert's token tile
+    const int Te = a.T[xe];
     const int split = blockIdx.z;
     const int nkt = a.K / KT;
     const int kt0 = split * a.kps;
@@ -488,10 +516,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
                 const int x = (kt0 + c * CHUNK_KT) * TILE_BYTES;  // byte offset along the row: multiple of 16
                 mbar_arrive_expect_tx(cfull0 + 8 * slot, CHUNK_BYTES);
                 if (GU) {
-                    tma_load_2d(dst, &a.tmap[0], x, mtile * 64, cfull0 + 8 * slot);
-                    tma_load_2d(dst + CHUNK_BYTES / 2, &a.tmap[1], x, mtile * 64, cfull0 + 8 * slot);
+                    tma_load_2d(dst, &a.tmap[xe][0], x, mtile * 64, cfull0 + 8 * slot);
+                    tma_load_2d(dst + CHUNK_BYTES / 2, &a.tmap[xe][1], x, mtile * 64, cfull0 + 8 * slot);
                 } else {
-                    tma_load_2d(dst, &a.tmap[0], x, mtile * MT, cfull0 + 8 * slot);
+                    tma_load_2d(dst, &a.tmap[xe][0], x, mtile * MT, cfull0 + 8 * slot);
                 }
             }
         }
@@ -499,7 +527,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
         // ---- token blocks, produced by the previous kernel
         pdl_wait();
         if (lane == 0) {
-            const uint8_t *src = a.B + (static_cast<size_t>(ntile) * nkt + kt0) * b_bytes(NT);
+            const uint8_t *src = a.B + (static_cast<size_t>(gtile) * nkt + kt0) * b_bytes(NT);
             for (int i = 0; i < nk; ++i) {
                 const int s = i % S;
                 if (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 8u)) break;
@@ -579,7 +607,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
         const int mat = GU ? (r >> 6) : 0;
         const int row = GU ? mtile * 64 + (r & 63) : mtile * MT + r;
         const bool rok = row < a.M;
-        const float *srow = a.scales[mat] + static_cast<size_t>(rok ? row : 0) * ngroups;
+        const float *srow = a.scales[xe][mat] + static_cast<size_t>(rok ? row : 0) * ngroups;
         float y[NH];
 #pragma unroll
         for (int n = 0; n < NH; ++n) y[n] = 0.f;
@@ -628,12 +656,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
                     }
                 }
                 named_barrier(1, EPI_WARPS * 32);
-                write_hidden_block<BITS, NT>(a, xch, 64, mtile, ntile, 0, NT, et, EPI_WARPS * 32);
+                write_hidden_block<BITS, NT>(a, xch, 64, mtile, gtile, ltile, Te, 0, NT, et, EPI_WARPS * 32);
             } else if (rok) {
 #pragma unroll
                 for (int n = 0; n < NH; ++n) {
-                    const int t = ntile * NT + h * NH + n;
-                    if (t < a.T) a.Y[static_cast<size_t>(t) * a.M + row] = y[n];
+                    const int t = ltile * NT + h * NH + n;
+                    if (t < Te) a.Y[xe][static_cast<size_t>(t) * a.M + row] = y[n];
                 }
             }
         } else {
@@ -710,13 +738,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
                     *g = silu_fast(*g) * g[64];
                 }
                 __syncthreads();
-                write_hidden_block<BITS, NT>(a, S, MT, mtile, ntile, n0, n1, et, NTH);
+                write_hidden_block<BITS, NT>(a, S, MT, mtile, gtile, ltile, Te, n0, n1, et, NTH);
             } else {
                 for (int it = et; it < (n1 - n0) * MT; it += NTH) {
                     const int n = it >> 7, r = it & (MT - 1);
-                    const int t = ntile * NT + n0 + n;
+                    const int t = ltile * NT + n0 + n;
                     const int row = mtile * MT + r;
-                    if (t < a.T && row < a.M) a.Y[static_cast<size_t>(t) * a.M + row] = S[n * MT + r];
+                    if (t < Te && row < a.M) a.Y[xe][static_cast<size_t>(t) * a.M + row] = S[n * MT + r];
                 }
             }
         }
@@ -797,11 +825,46 @@ struct TcLayout {
     size_t xb, hb, total;
 };
 
-TcLayout tc_layout(int T, int d_model, int d_ff)
+// The experts of one grouped launch: up to TC_MAX_EXPERTS with T > 0, their
+// first global token tile and one token-tile width for all of them (from
+// the largest T).
+struct TcGroup {
+    int n;
+    int idx[TC_MAX_EXPERTS];
+    int tile0[TC_MAX_EXPERTS + 1];
+    int nt;
+};
+
+// Splits experts [0, n) with T > 0 into groups; returns the group count.
+int make_groups(int n, const int *T, TcGroup *groups, int max_groups)
+{
+    int g = 0;
+    TcGroup cur = {};
+    auto flush = [&]() {
+        if (cur.n == 0) return;
+        int tmax = 1;
+        for (int i = 0; i < cur.n; ++i) tmax = T[cur.idx[i]] > tmax ? T[cur.idx[i]] : tmax;
+        cur.nt = pick_nt(tmax);
+        cur.tile0[0] = 0;
+        for (int i = 0; i < cur.n; ++i) cur.tile0[i + 1] = cur.tile0[i] + (T[cur.idx[i]] + cur.nt - 1) / cur.nt;
+        if (g < max_groups) groups[g] = cur;
+        ++g;
+        cur = TcGroup{};
+    };
+    for (int e = 0; e < n; ++e) {
+        if (T[e] <= 0) continue;
+        cur.idx[cur.n++] = e;
+        if (cur.n == TC_MAX_EXPERTS) flush();
+    }
+    flush();
+    return g;
+}
+
+TcLayout tc_layout_tiles(int ntiles, int nt, int d_model, int d_ff)
 {
     TcLayout L = {};
-    L.nt = pick_nt(T);
-    L.ntiles = (T + L.nt - 1) / L.nt;
+    L.nt = nt;
+    L.ntiles = ntiles;
     size_t off = 0;
     L.xb = off; off = align256(off + static_cast<size_t>(L.ntiles) * (d_model / KT) * b_bytes(L.nt));
     L.hb = off; off = align256(off + static_cast<size_t>(L.ntiles) * (d_ff / KT) * b_bytes(L.nt));
@@ -881,67 +944,139 @@ cudaError_t launch_gemm_bits(int bits, int nt, const TcArgs &a, int mtiles, int 
 
 bool tc_batch_supported(int T, int d_model, int d_ff, int group)
 {
-    return T >= 2 && group % KT == 0 && d_model % KT == 0 && d_ff % KT == 0 && d_model > 0 && d_ff > 0;
+    return T >= 2 && tc_batch_shape_supported(d_model, d_ff, group);
+}
+
+bool tc_batch_shape_supported(int d_model, int d_ff, int group)
+{
+    return group % KT == 0 && d_model % KT == 0 && d_ff % KT == 0 && d_model > 0 && d_ff > 0;
+}
+
+size_t tc_batch_workspace_experts(int n, const int *T, int d_model, int d_ff)
+{
+    const int max_groups = (n + TC_MAX_EXPERTS - 1) / TC_MAX_EXPERTS + 1;
+    TcGroup *groups = new TcGroup[max_groups];
+    const int ng = make_groups(n, T, groups, max_groups);
+    size_t need = 0;
+    for (int g = 0; g < ng && g < max_groups; ++g) {
+        const size_t t = tc_layout_tiles(groups[g].tile0[groups[g].n], groups[g].nt, d_model, d_ff).total;
+        need = t > need ? t : need;
+    }
+    delete[] groups;
+    return need;
 }
 
 size_t tc_batch_workspace(int T, int d_model, int d_ff)
 {
-    return tc_layout(T, d_model, d_ff).total;
+    return tc_batch_workspace_experts(1, &T, d_model, d_ff);
+}
+
+cudaError_t launch_ffn_batch_tc_experts(int bits, int n, const uint8_t *const *gc, const float *const *gs,
+                                        const uint8_t *const *uc, const float *const *us,
+                                        const uint8_t *const *dc, const float *const *ds,
+                                        const float *const *X, float *const *Y, const int *T, int d_model,
+                                        int d_ff, int group, void *workspace, cudaStream_t stream)
+{
+    const DeviceInfo *dev = device_info();
+    if (!dev) return cudaErrorInvalidDevice;
+    if (!encoder()) return cudaErrorNotSupported;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    unsigned *status = device_status_word();
+    // launches go group after group on the stream: a group's token prep
+    // waits for the previous group's down projection before it overwrites
+    // the shared workspace
+    for (int first = 0; first < n;) {
+        TcGroup G;
+        {
+            // the next group: experts first .. with T > 0, at most TC_MAX_EXPERTS
+            int last = first, cnt = 0;
+            while (last < n && cnt < TC_MAX_EXPERTS) {
+                if (T[last] > 0) ++cnt;
+                ++last;
+            }
+            TcGroup tmp[2];
+            const int ng = make_groups(last - first, T + first, tmp, 2);
+            if (ng == 0) {
+                first = last;
+                continue;
+            }
+            G = tmp[0];
+            for (int i = 0; i < G.n; ++i) G.idx[i] += first;
+            first = last;
+        }
+        const int ntiles = G.tile0[G.n];
+        const TcLayout L = tc_layout_tiles(ntiles, G.nt, d_model, d_ff);
+
+        PrepArgs p = {};
+        for (int i = 0; i < G.n; ++i) {
+            p.X[i] = X[G.idx[i]];
+            p.T[i] = T[G.idx[i]];
+        }
+        for (int i = 0; i <= G.n; ++i) p.tile0[i] = G.tile0[i];
+        p.n = G.n;
+        p.bits = bits;
+        p.Bblk = ws + L.xb;
+        p.K = d_model;
+        p.nt = G.nt;
+        p.ntiles = ntiles;
+        {
+            const long long total = static_cast<long long>(ntiles) * G.nt * (d_model / 8);
+            long long blocks = (total + 255) / 256;
+            const long long cap = static_cast<long long>(dev->sm_count) * 8;
+            if (blocks > cap) blocks = cap;
+            if (blocks < 1) blocks = 1;
+            cudaError_t e = launch_pdl(prep_tokens, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
+            if (e != cudaSuccess) return e;
+        }
+
+        // TcArgs is ~10 KB: built on the heap, passed by value at launch
+        TcArgs *a = new TcArgs();
+        TcArgs *b = new TcArgs();
+        bool ok = true;
+        for (int i = 0; i < G.n && ok; ++i) {
+            const int e = G.idx[i];
+            ok = encode_codes(&a->tmap[i][0], gc[e], bits, d_ff, d_model, 64) &&
+                 encode_codes(&a->tmap[i][1], uc[e], bits, d_ff, d_model, 64) &&
+                 encode_codes(&b->tmap[i][0], dc[e], bits, d_model, d_ff, MT);
+            b->tmap[i][1] = b->tmap[i][0];
+            a->scales[i][0] = gs[e];
+            a->scales[i][1] = us[e];
+            b->scales[i][0] = b->scales[i][1] = ds[e];
+            a->Y[i] = nullptr;
+            b->Y[i] = Y[e];
+            a->T[i] = b->T[i] = T[e];
+        }
+        for (int i = 0; i <= G.n; ++i) a->tile0[i] = b->tile0[i] = G.tile0[i];
+        a->n = b->n = G.n;
+        a->B = ws + L.xb;
+        a->Hb = ws + L.hb;
+        a->status = b->status = status;
+        a->M = d_ff;
+        a->K = d_model;
+        b->B = ws + L.hb;
+        b->Hb = nullptr;
+        b->M = d_model;
+        b->K = d_ff;
+        a->group = b->group = group;
+        a->ntiles = b->ntiles = ntiles;
+        cudaError_t e = ok ? cudaSuccess : cudaErrorInvalidValue;
+        if (e == cudaSuccess) e = launch_gemm_bits<true>(bits, G.nt, *a, d_ff / KT, dev->sm_count, stream);
+        if (e == cudaSuccess)
+            e = launch_gemm_bits<false>(bits, G.nt, *b, (d_model + MT - 1) / MT, dev->sm_count, stream);
+        delete a;
+        delete b;
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 cudaError_t launch_ffn_batch_tc(int bits, const uint8_t *const gu_codes[2], const float *const gu_scales[2],
                                 const uint8_t *down_codes, const float *down_scales, const float *X, float *Y,
                                 int T, int d_model, int d_ff, int group, void *workspace, cudaStream_t stream)
 {
-    const DeviceInfo *dev = device_info();
-    if (!dev) return cudaErrorInvalidDevice;
-    if (!encoder()) return cudaErrorNotSupported;
-    const TcLayout L = tc_layout(T, d_model, d_ff);
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-
-    PrepArgs p = {X, bits, ws + L.xb, T, d_model, L.nt, L.ntiles};
-    {
-        const long long total = static_cast<long long>(L.ntiles) * L.nt * (d_model / 8);
-        long long blocks = (total + 255) / 256;
-        const long long cap = static_cast<long long>(dev->sm_count) * 8;
-        if (blocks > cap) blocks = cap;
-        if (blocks < 1) blocks = 1;
-        cudaError_t e = launch_pdl(prep_tokens, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, p);
-        if (e != cudaSuccess) return e;
-    }
-
-    TcArgs a = {};
-    if (!encode_codes(&a.tmap[0], gu_codes[0], bits, d_ff, d_model, 64) ||
-        !encode_codes(&a.tmap[1], gu_codes[1], bits, d_ff, d_model, 64))
-        return cudaErrorInvalidValue;
-    a.scales[0] = gu_scales[0];
-    a.scales[1] = gu_scales[1];
-    a.B = ws + L.xb;
-    a.Y = nullptr;
-    a.Hb = ws + L.hb;
-    a.status = device_status_word();
-    a.M = d_ff;
-    a.K = d_model;
-    a.group = group;
-    a.T = T;
-    a.ntiles = L.ntiles;
-    cudaError_t e = launch_gemm_bits<true>(bits, L.nt, a, d_ff / KT, dev->sm_count, stream);
-    if (e != cudaSuccess) return e;
-
-    TcArgs b = {};
-    if (!encode_codes(&b.tmap[0], down_codes, bits, d_model, d_ff, MT)) return cudaErrorInvalidValue;
-    b.tmap[1] = b.tmap[0];
-    b.scales[0] = b.scales[1] = down_scales;
-    b.B = ws + L.hb;
-    b.Y = Y;
-    b.Hb = nullptr;
-    b.status = a.status;
-    b.M = d_model;
-    b.K = d_ff;
-    b.group = group;
-    b.T = T;
-    b.ntiles = L.ntiles;
-    return launch_gemm_bits<false>(bits, L.nt, b, (d_model + MT - 1) / MT, dev->sm_count, stream);
+    return launch_ffn_batch_tc_experts(bits, 1, &gu_codes[0], &gu_scales[0], &gu_codes[1], &gu_scales[1],
+                                       &down_codes, &down_scales, &X, &Y, &T, d_model, d_ff, group, workspace,
+                                       stream);
 }
 
 }  // namespace smoe

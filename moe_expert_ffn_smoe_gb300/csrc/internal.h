@@ -65,7 +65,16 @@ cudaError_t launch_qgemm_tokens(int bits, int nmat, const uint8_t *const codes[2
 // and the launch of its four kernels (operand preparation and GEMM for
 // gate/up, then for down).
 bool tc_batch_supported(int T, int d_model, int d_ff, int group);
+bool tc_batch_shape_supported(int d_model, int d_ff, int group);
 size_t tc_batch_workspace(int T, int d_model, int d_ff);
+// Token batches of n experts (expert e: T[e] tokens, T[e] == 0 skipped) on
+// the tensor cores in one launch set per 32 experts; shapes already checked.
+size_t tc_batch_workspace_experts(int n, const int *T, int d_model, int d_ff);
+cudaError_t launch_ffn_batch_tc_experts(int bits, int n, const uint8_t *const *gc, const float *const *gs,
+                                        const uint8_t *const *uc, const float *const *us,
+                                        const uint8_t *const *dc, const float *const *ds,
+                                        const float *const *X, float *const *Y, const int *T, int d_model,
+                                        int d_ff, int group, void *workspace, cudaStream_t stream);
 cudaError_t launch_ffn_batch_tc(int bits, const uint8_t *const gu_codes[2], const float *const gu_scales[2],
                                 const uint8_t *down_codes, const float *down_scales, const float *X, float *Y,
                                 int T, int d_model, int d_ff, int group, void *workspace, cudaStream_t stream);
@@ -78,6 +87,15 @@ cudaError_t launch_ffn_batch(int bits, const uint8_t *const gu_codes[2], const f
                              const uint8_t *down_codes, const float *down_scales,
                              const float *X, float *Y, int T, int d_model, int d_ff, int group,
                              void *workspace, cudaStream_t stream);
+
+// Token batches of n experts: the grouped tensor-core launches when the
+// shape allows, else expert after expert through launch_ffn_batch.
+size_t ffn_batch_workspace_experts(int n, const int *T, int d_model, int d_ff, int group);
+cudaError_t launch_ffn_batch_experts(int bits, int n, const uint8_t *const *gc, const float *const *gs,
+                                     const uint8_t *const *uc, const float *const *us,
+                                     const uint8_t *const *dc, const float *const *ds, const float *const *X,
+                                     float *const *Y, const int *T, int d_model, int d_ff, int group,
+                                     void *workspace, cudaStream_t stream);
 
 // Reads and clears the device status word of the current device after
 // synchronising `stream`.

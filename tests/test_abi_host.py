@@ -204,3 +204,41 @@ def test_bf16_batch_refusals(smoe):
     assert call(y=[A + 0x4000000, A + 0x4000000 + 32, A + 0x4200000]) == smoe.SMOE_ERR_ALIAS  # two outputs
     assert call(y=[A + 0x4000000, A + 0x1000000 + 256, A + 0x4200000]) == smoe.SMOE_ERR_ALIAS  # y1 over w1
     assert call(y=[A + 0x3200000, A + 0x4100000, A + 0x4200000]) == smoe.SMOE_ERR_ALIAS   # y0 over x2
+
+
+def test_experts_batch_workspace_and_refusals(smoe):
+    L = smoe._lib
+    I = lambda v: (ctypes.c_int * len(v))(*v)
+    P = lambda v: (ctypes.c_void_p * len(v))(*v)
+    T = [16, 0, 3]
+    need = L.smoe_experts_ffn_batch_workspace_bytes(3, I(T), 4096, 1536, 64)
+    assert need > 0 and need % 256 == 0
+    assert need >= L.smoe_ffn_batch_workspace_bytes(16, 4096, 1536, 64)
+    assert L.smoe_experts_ffn_batch_workspace_bytes(0, None, 4096, 1536, 64) == 0
+    assert L.smoe_experts_ffn_batch_workspace_bytes(2, I([4, -1]), 4096, 1536, 64) == ctypes.c_size_t(-1).value
+    assert L.smoe_experts_ffn_batch_workspace_bytes(2, I([4, 4]), 4096, 1536, 48) == ctypes.c_size_t(-1).value
+    w = [[A + 0x1000000 * (3 * k + e) for e in range(3)] for k in range(6)]
+    X = [A + 0x20000000 + 0x1000000 * e for e in range(3)]
+    Y = [A + 0x30000000 + 0x1000000 * e for e in range(3)]
+    ws = A + 0x40000000
+    f = L.smoe_experts_ffn_batch_q4
+
+    def args(T=T, X=X, Y=Y, wsp=ws, wsb=need, group=64, n=3):
+        return (n, *[P(v) for v in w], P(X), P(Y), I(T), 4096, 1536, group, wsp, wsb, None)
+
+    assert f(*args(n=-1)) == smoe.SMOE_ERR_SHAPE
+    assert f(*args(T=[16, -2, 3])) == smoe.SMOE_ERR_SHAPE
+    assert f(*args(group=48)) == smoe.SMOE_ERR_SHAPE
+    assert f(*args(T=[0, 0, 0])) == smoe.SMOE_OK                               # nothing to do
+    assert f(*args(wsb=need - 256)) == smoe.SMOE_ERR_WORKSPACE
+    assert f(*args(wsp=ws + 8)) == smoe.SMOE_ERR_ALIGN
+    need3 = L.smoe_experts_ffn_batch_workspace_bytes(3, I([16, 5, 3]), 4096, 1536, 64)
+    assert f(*args(X=[X[0], 0, X[2]], T=[16, 5, 3], wsb=need3)) == smoe.SMOE_ERR_NULL
+    assert f(*args(Y=[Y[0], Y[0] + 64, Y[2]], T=[16, 5, 3], wsb=need3)) == smoe.SMOE_ERR_ALIAS   # two outputs
+    assert f(*args(Y=[X[2] + 256, Y[1], Y[2]])) == smoe.SMOE_ERR_ALIAS                # Y0 over X2
+    assert f(*args(wsp=w[4][2] + 1024)) == smoe.SMOE_ERR_ALIAS                         # workspace over down codes
+    # an expert with no tokens may hold null pointers
+    X2 = [X[0], 0, X[2]]
+    Y2 = [Y[0], 0, Y[2]]
+    assert f(*args(X=X2, Y=Y2, wsp=0)) == smoe.SMOE_ERR_WORKSPACE                       # still needs the workspace
+    assert smoe._lib.smoe_experts_ffn_batch_q2(*args(group=32)) == smoe.SMOE_ERR_SHAPE  # Q2 groups of 64
