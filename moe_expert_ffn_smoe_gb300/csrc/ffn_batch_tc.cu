@@ -93,6 +93,16 @@ __host__ __device__ constexpr int stages_for(int nt)
 // epilogue.
 __host__ __device__ constexpr int accbufs_for(int nt) { return 256 / nt < 16 ? 256 / nt : 16; }
 
+// Token tiles of at most 32: the converters store A straight into tensor
+// memory (8 stages of 32 columns after 256 columns of accumulators), so a K
+// tile's A makes no round trip through shared memory.
+__host__ __device__ constexpr bool a_in_tmem(int nt) { return nt <= 32; }
+constexpr uint32_t A_TMEM_COL0 = 256;
+constexpr int A_TMEM_STAGES = 8;
+__host__ __device__ constexpr int tc_accbufs(int nt) { return a_in_tmem(nt) ? (128 / nt < 8 ? 128 / nt : 8) : accbufs_for(nt); }
+__host__ __device__ constexpr int tc_stages(int nt) { return a_in_tmem(nt) ? A_TMEM_STAGES : stages_for(nt); }
+__host__ __device__ constexpr uint32_t tc_stage_bytes(int nt) { return a_in_tmem(nt) ? round1024(b_bytes(nt)) : stage_bytes(nt); }
+
 // Byte offset of (row, 8-column block k8) in a [rows x 64] bf16 tile laid out
 // as 8x8 core matrices: core (row/8, k8) at ((row/8)*8 + k8)*128, row%8 at 16*(row%8).
 __host__ __device__ __forceinline__ uint32_t core_off(int row, int k8)
@@ -137,6 +147,31 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t a, uint64_t b, 
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+
+// The same MMA with A read from tensor memory (M = 128 rows in the 128
+// lanes, K along the columns, two bf16 per 32-bit column).
+__device__ __forceinline__ void mma_bf16_ta(uint32_t tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// 16 consecutive 32-bit columns of this warp's 32 TMEM lanes (this
+// thread's lane), from registers.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::
+            "r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
@@ -443,10 +478,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
 {
     constexpr int CHUNK_KT = chunk_kt<BITS>();
     constexpr int TILE_BYTES = KT * BITS / 8;  // bytes of one row's codes per K tile
-    constexpr int NB = accbufs_for(NT);
-    constexpr uint32_t NCOLS = NB * 2 * NT;  // a power of two in [64, 512]
-    constexpr int S = stages_for(NT);
-    constexpr uint32_t SB = stage_bytes(NT);
+    constexpr bool ATM = a_in_tmem(NT);
+    constexpr int NB = tc_accbufs(NT);
+    constexpr uint32_t NCOLS = ATM ? 512u : NB * 2 * NT;  // a power of two in [64, 512]
+    constexpr int S = tc_stages(NT);
+    constexpr uint32_t SB = tc_stage_bytes(NT);
+    constexpr uint32_t B_OFF = ATM ? 0u : A_BYTES;  // B within a stage
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -532,7 +569,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
                 const int s = i % S;
                 if (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 8u)) break;
                 mbar_arrive_expect_tx(full0 + 8 * s, b_bytes(NT));
-                bulk_g2s(stage0 + s * SB + A_BYTES, src + static_cast<size_t>(i) * b_bytes(NT), b_bytes(NT),
+                bulk_g2s(stage0 + s * SB + B_OFF, src + static_cast<size_t>(i) * b_bytes(NT), b_bytes(NT),
                          full0 + 8 * s);
             }
         }
@@ -547,11 +584,16 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
                 if (i >= NB && !mbar_wait_bounded(acce0 + 8 * b, ((i / NB) - 1) & 1, a.status, 4u)) break;
                 tc_fence_after();
                 const uint32_t sa = stage0 + s * SB;
-                const uint32_t sb = sa + A_BYTES;
+                const uint32_t sb = sa + B_OFF;
                 const uint32_t d = tmem + static_cast<uint32_t>(b * 2 * NT);
 #pragma unroll
-                for (int kk = 0; kk < KT / 16; ++kk)
-                    mma_bf16(d, smem_desc(sa + kk * 256), smem_desc(sb + kk * 256), idesc, kk != 0);
+                for (int kk = 0; kk < KT / 16; ++kk) {
+                    if (ATM)
+                        mma_bf16_ta(d, tmem + A_TMEM_COL0 + static_cast<uint32_t>(s * 32 + kk * 8),
+                                    smem_desc(sb + kk * 256), idesc, kk != 0);
+                    else
+                        mma_bf16(d, smem_desc(sa + kk * 256), smem_desc(sb + kk * 256), idesc, kk != 0);
+                }
                 mma_commit(empty0 + 8 * s);
                 mma_commit(accf0 + 8 * b);
             }
@@ -569,7 +611,36 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
             if (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 5u)) break;
             const uint32_t row = codes0 + slot * CHUNK_BYTES + static_cast<uint32_t>(r) * 128u;
             const uint32_t sa = stage0 + s * SB;
-            if (BITS == 4) {
+            if (ATM) {
+                // this thread's 16 columns (32 bf16) of tile row r, in the
+                // K order of the B operand, straight into tensor memory
+                uint32_t v[16];
+                if (BITS == 4) {
+                    const uint4 w = lds128v(row + (((2u * sub + static_cast<uint32_t>(hf)) ^ rsw) << 4));
+                    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 c = q4_word_to_bf16(words[q]);
+                        v[4 * q] = c.x; v[4 * q + 1] = c.y; v[4 * q + 2] = c.z; v[4 * q + 3] = c.w;
+                    }
+                } else {
+                    const uint2 w = lds64v(row + ((static_cast<uint32_t>(sub) ^ rsw) << 4) + 8u * hf);
+                    const uint32_t words[2] = {w.x, w.y};
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        uint4 lo, hi;
+                        q2_word_to_bf16(words[q], lo, hi);
+                        v[8 * q] = lo.x; v[8 * q + 1] = lo.y; v[8 * q + 2] = lo.z; v[8 * q + 3] = lo.w;
+                        v[8 * q + 4] = hi.x; v[8 * q + 5] = hi.y; v[8 * q + 6] = hi.z; v[8 * q + 7] = hi.w;
+                    }
+                }
+                tc_fence_after();  // after the wait for the MMA that last read this stage
+                tmem_st16(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + A_TMEM_COL0 +
+                              static_cast<uint32_t>(s * 32 + 16 * hf),
+                          v);
+                tmem_wait_st();
+                tc_fence_before();
+            } else if (BITS == 4) {
                 // 16-byte unit 2 sub + hf of the (swizzled) chunk row: 4 words, one block each
                 const uint4 w = lds128v(row + (((2u * sub + static_cast<uint32_t>(hf)) ^ rsw) << 4));
                 const uint32_t words[4] = {w.x, w.y, w.z, w.w};
@@ -587,7 +658,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
                     sts128(sa + core_off(r, 4 * hf + 2 * j + 1), hi);
                 }
             }
-            fence_proxy_async_smem();
+            if (!ATM) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(full0 + 8 * s);
@@ -911,8 +982,11 @@ bool encode_codes(CUtensorMap *map, const uint8_t *codes, int bits, int rows, in
 template <int BITS, int NT, bool GU>
 cudaError_t launch_gemm(const TcArgs &args, int mtiles, int sms, cudaStream_t stream)
 {
-    const size_t smem = 1024 + CODE_SLOTS * CHUNK_BYTES + static_cast<size_t>(stages_for(NT)) * stage_bytes(NT) +
-                        512;
+    // one CTA per SM: each allocates all 512 TMEM columns, so a second CTA
+    // on the SM would wait in tcgen05.alloc; more than half the shared
+    // memory keeps a second one off
+    size_t smem = 1024 + CODE_SLOTS * CHUNK_BYTES + static_cast<size_t>(tc_stages(NT)) * tc_stage_bytes(NT) + 512;
+    if (smem < (120u << 10)) smem = 120u << 10;
     auto k = tc_ffn<BITS, NT, GU>;
     cudaError_t e = ensure_dynamic_smem(k, smem);
     if (e != cudaSuccess) return e;
