@@ -1,45 +1,52 @@
 // Token-batch FFN on the tensor cores (tcgen05, TMEM), the S-MoE page "Metal
 // Compute Kernels", section "Token-Batch Fused FFN": for T tokens the three
 // projections are dense contractions, Y = W X^T with the weights' K axis
-// contracted against every token.
+// contracted against every token.  One launch set serves the token batches
+// of up to 32 experts (the page's batch per claimed expert): their token
+// tiles are concatenated along the grid's y axis.
 //
 // Exactness plan (the scale varies per (row, group), so it cannot be folded
 // into an operand):
 //  * A (weights, 128 rows x 64 columns per K tile, one group slice) holds
-//    each code c as the bf16 value (c - Z)/16 = (2c - 15)/32, which is exact
-//    (an odd numerator of at most 4 bits).  It is made from the exact bf16
-//    1 + c/16 (a bit pattern) minus 1 + Z/16 = 1.46875, a subtraction whose
-//    exact result is representable.  Per 64-column tile of one group the
-//    accumulator is then D = sum (c - Z) x / 16 and
-//        sum w x = s sum (c - Z) x / Z = s (16/Z) D.
+//    each code c as the exact bf16 value (c - Z)/DEN: Q4 (c - 7.5)/16 =
+//    (2c - 15)/32 (an odd numerator of at most 4 bits), made from the exact
+//    bf16 1 + c/16 (a bit pattern) minus 1.46875; Q2 (c - 1.5)/4 from
+//    1 + c/4 minus 1.375.  Each subtraction's exact result is representable.
+//    Per 64-column tile of one group the accumulator is then
+//    D = sum (c - Z) x / DEN and sum w x = s sum (c - Z) x / Z = s (DEN/Z) D.
 //  * B (tokens, NT x 64) holds x split into two bf16 halves, hi = bf16(x) and
 //    lo = bf16(x - hi), stored as one operand of 2 NT rows (hi rows, then
 //    lo rows), so one MMA of N = 2 NT computes both halves; the epilogue
 //    adds the hi and lo columns (x represented to about 2^-17 relative).
 //  * Each 64-column tile's accumulator is read back from TMEM and added to
-//    per-thread f32 sums with the tile's scale.  TMEM holds up to 16 tiles'
-//    accumulators (512 columns), so the MMAs run ahead of the epilogue.
+//    per-thread f32 sums with the tile's scale.  TMEM holds several tiles'
+//    accumulators, so the MMAs run ahead of the epilogue.
+//  * Token tiles of 64 or 128: A goes through shared memory (canonical
+//    no-swizzle K-major layout, proxy fence) and TMEM holds up to 16
+//    accumulators.  Token tiles of 16 or 32: A goes straight into TMEM
+//    (tcgen05.st; 8 stages after 256 columns of accumulators) and the MMAs
+//    read it there.
 //
 // Three launches per call, chained with programmatic dependent launch:
 //  1. prep_tokens: X -> B blocks (hi, lo per (token tile, K tile)).
-//  2. tc_ffn<NT, gate/up>: a CTA tile is 64 gate rows + the same 64 up rows
-//     (128 accumulator rows) over one K range.  The K splits of a tile form
-//     one thread-block cluster: each split leaves its partial sums in its
-//     shared memory, then split q adds token columns [q NT/S, (q+1) NT/S)
-//     of every split's partials (in split order, read through distributed
-//     shared memory), forms SiLU(g) * u and writes it directly as the B
-//     block of the down projection's K tile (64 hidden columns = one down K
-//     tile).
-//  3. tc_ffn<NT, down>: 128 down rows over one K range, split the same way;
-//     each split writes Y for its token columns.
+//  2. tc_ffn<BITS, NT, gate/up>: a CTA tile is 64 gate rows + the same 64 up
+//     rows (128 accumulator rows) over one K range.  The K splits of a tile
+//     form one thread-block cluster: each split leaves its partial sums in
+//     its shared memory, then split q adds token columns [q NT/S, (q+1)
+//     NT/S) of every split's partials (in split order, read through
+//     distributed shared memory), forms SiLU(g) * u and writes it directly
+//     as the B block of the down projection's K tile (64 hidden columns =
+//     one down K tile).
+//  3. tc_ffn<BITS, NT, down>: 128 down rows over one K range, split the same
+//     way; each split writes Y for its token columns.
 // Inside a GEMM CTA (608 threads): warps 0-7 epilogue (warp w reads TMEM
 // lane quarter w % 4 = 32 tile rows, columns of half w / 4), warps 8-15
-// convert codes to A tiles (thread = half a tile row: 4 of its 8 code
-// words), warp 16 issues the MMAs, warp 17 streams code chunks with 2-D
-// tensor copies (TMA, 128-byte swizzle: 4 K tiles x 128 rows per chunk),
-// warp 18 streams the token B blocks with bulk copies.  Two converter and
-// two epilogue warps per SM sub-partition keep those dependent chains
-// overlapped.  Every hand-off is an mbarrier with one
+// convert codes to A tiles (thread = half a tile row: 4 of its 8 Q4 code
+// words, 2 of its 4 Q2 words), warp 16 issues the MMAs, warp 17 streams code
+// chunks with 2-D tensor copies (TMA, 128-byte swizzle: 128 bytes x 64 or
+// 128 rows per chunk), warp 18 streams the token B blocks with bulk copies.
+// Two converter and two epilogue warps per SM sub-partition keep those
+// dependent chains overlapped.  Every hand-off is an mbarrier with one
 // in-order waiter per role, so each awaited phase parity is unambiguous;
 // every wait is bounded.
 #include <cuda.h>
