@@ -53,6 +53,10 @@ def lib():
         h.oracle_ffn_batch.argtypes = [ctypes.c_int, _u8p, _f32p, _u8p, _f32p, _u8p, _f32p,
                                        _L, _L, _L, _L, _f64p, _L, _L, _f64p, _f64p, _f64p]
         h.oracle_matvec_bf16.argtypes = [_u16p, _L, _L, _f64p, _L, _L, _f64p, _f64p]
+        _lp = ctypes.POINTER(ctypes.c_long)
+        h.oracle_topk.argtypes = [_f64p, _L, _L, _lp, _f64p]
+        h.oracle_route.argtypes = [_u16p, _L, _L, _f64p, _L, _f64p, _f64p, _lp, _f64p]
+        h.oracle_combine.argtypes = [_f64p, _f64p, _L, _L, _f64p, _f64p]
         _lib = h
     return _lib
 
@@ -177,6 +181,46 @@ def matvec_bf16(w_bits, rows, cols, x, row0=0, nrows=None):
     _check(lib().oracle_matvec_bf16(_p(w, _u16p), rows, cols, _p(x, _f64p), row0, nrows,
                                     _p(y, _f64p), _p(a, _f64p)), "matvec_bf16")
     return y, a
+
+
+def topk(logits, k):
+    """(expert indices in selection order, weights) from given logits: the k
+    largest, ties to the lower index, NaN below every number; weights are a
+    softmax over the selected logits."""
+    v = _c(logits, np.float64).reshape(-1)
+    idx = np.empty(k, dtype=np.int64)
+    w = np.empty(k)
+    _check(lib().oracle_topk(_p(v, _f64p), v.size, k, idx.ctypes.data_as(ctypes.POINTER(ctypes.c_long)),
+                             _p(w, _f64p)), "topk")
+    return idx, w
+
+
+def route(g_bits, n_experts, d_model, x, k):
+    """Router of a bf16 gate matrix [n_experts x d_model]:
+    (logits, sum|g*x| per expert, indices, weights)."""
+    g = _c(g_bits, np.uint16)
+    x = _c(x, np.float64).reshape(-1)
+    if g.size < n_experts * d_model or x.size < d_model:
+        raise ValueError("route: arrays smaller than the stated shape")
+    logits, a = np.empty(n_experts), np.empty(n_experts)
+    idx = np.empty(k, dtype=np.int64)
+    w = np.empty(k)
+    _check(lib().oracle_route(_p(g, _u16p), n_experts, d_model, _p(x, _f64p), k, _p(logits, _f64p),
+                              _p(a, _f64p), idx.ctypes.data_as(ctypes.POINTER(ctypes.c_long)), _p(w, _f64p)),
+           "route")
+    return logits, a, idx, w
+
+
+def combine(expert_out, w):
+    """(out, sum|w*y| per output) for the k rows of expert_out [k x d_model]."""
+    eo = _c(expert_out, np.float64)
+    wv = _c(w, np.float64).reshape(-1)
+    k = wv.size
+    d_model = eo.size // max(k, 1)
+    out, a = np.empty(d_model), np.empty(d_model)
+    _check(lib().oracle_combine(_p(eo, _f64p), _p(wv, _f64p), k, d_model, _p(out, _f64p), _p(a, _f64p)),
+           "combine")
+    return out, a
 
 
 def host_threads() -> int:

@@ -301,3 +301,79 @@ int oracle_matvec_bf16(const uint16_t *w, long rows, long cols, const double *x,
     for_rows(bf16_row, &c, row0, row0 + nrows);
     return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Routing and combine.  The pages run the exact-routing gate matvec (n_experts
+ * x d_model) on the host and describe neither the selection nor the
+ * weighting; the readings taken here:
+ *   logits = G x with bf16 G (the matvec above);
+ *   the k experts with the largest logits, in descending logit order, ties
+ *     to the lower expert index, NaN below every number;
+ *   their weights: exp(l_i - l_max) / sum over the k selected of
+ *     exp(l_j - l_max) (a softmax over all experts renormalised over the
+ *     selected k gives the same values);
+ *   combine: out[j] = sum over the k selected, in selection order, of
+ *     w_i * y_i[j]. */
+
+/* 1 if (va, ia) ranks before (vb, ib). */
+static int ranks_before(double va, long ia, double vb, long ib)
+{
+    const int na = isnan(va), nb = isnan(vb);
+    if (na != nb) return nb;          /* a number ranks before NaN */
+    if (!na && va != vb) return va > vb;
+    return ia < ib;                   /* equal values (or both NaN): lower index */
+}
+
+/* Selection and weights from given logits (k <= n). */
+int oracle_topk(const double *logits, long n, long k, long *idx, double *w)
+{
+    if (n < 1 || k < 1 || k > n) return -1;
+    char *taken = (char *)calloc((size_t)n, 1);
+    if (!taken) return -1;
+    for (long r = 0; r < k; ++r) {
+        long best = -1;
+        for (long e = 0; e < n; ++e) {
+            if (taken[e]) continue;
+            if (best < 0 || ranks_before(logits[e], e, logits[best], best)) best = e;
+        }
+        taken[best] = 1;
+        idx[r] = best;
+    }
+    free(taken);
+    const double lmax = logits[idx[0]];
+    double sum = 0.0;
+    for (long r = 0; r < k; ++r) {
+        w[r] = exp(logits[idx[r]] - lmax);
+        sum += w[r];
+    }
+    for (long r = 0; r < k; ++r) w[r] /= sum;
+    return 0;
+}
+
+/* logits (and sum |g x| per expert) of the bf16 router, then the selection. */
+int oracle_route(const uint16_t *g, long n_experts, long d_model, const double *x, long k,
+                 double *logits, double *absdot, long *idx, double *w)
+{
+    int rc = oracle_matvec_bf16(g, n_experts, d_model, x, 0, n_experts, logits, absdot);
+    if (rc) return rc;
+    return oracle_topk(logits, n_experts, k, idx, w);
+}
+
+/* out[j] = sum_i w[i] * eo[i][j] over the k rows of eo [k x d_model], in row
+ * order, with sum |w[i] * eo[i][j]| per output for the tolerance. */
+int oracle_combine(const double *eo, const double *w, long k, long d_model, double *out,
+                   double *absdot)
+{
+    if (k < 0 || d_model < 0) return -1;
+    for (long j = 0; j < d_model; ++j) {
+        double acc = 0.0, mag = 0.0;
+        for (long i = 0; i < k; ++i) {
+            const double t = w[i] * eo[i * d_model + j];
+            acc += t;
+            mag += fabs(t);
+        }
+        out[j] = acc;
+        if (absdot) absdot[j] = mag;
+    }
+    return 0;
+}

@@ -361,6 +361,75 @@ def test_golden_q4_ffn_256_seed0_unchanged():
         np.testing.assert_allclose(now[key], stored[key], rtol=1e-15, atol=0)
 
 
+# ------------------------------------------------------- routing / combine
+# The pages leave selection and weighting open; these pin the readings in
+# the oracle (largest logits first, ties to the lower index, NaN last,
+# weights a softmax over the selected logits, combine in selection order).
+
+def test_topk_order_and_ties():
+    idx, w = oracle.topk(np.array([0.1, 3.0, -1.0, 3.0, 2.0]), 3)
+    assert list(idx) == [1, 3, 4]            # 3 (index 1) before 3 (index 3), then 2
+    assert w[0] == w[1] and w[2] < w[1]
+
+
+def test_topk_nan_ranks_last_and_infinities():
+    idx, w = oracle.topk(np.array([np.nan, -np.inf, 0.0, np.inf]), 3)
+    assert list(idx) == [3, 2, 1]
+    idx, _ = oracle.topk(np.array([np.nan, np.nan, 5.0]), 3)
+    assert list(idx) == [2, 0, 1]            # two NaNs: lower index first
+
+
+def test_topk_weights_are_a_distribution_invariant_to_shifts():
+    rng = np.random.default_rng(3)
+    l = rng.normal(size=128) * 3
+    idx, w = oracle.topk(l, 8)
+    assert abs(w.sum() - 1.0) < 1e-15 and (w > 0).all() and (np.diff(w) <= 0).all()
+    idx2, w2 = oracle.topk(l + 1000.0, 8)
+    assert list(idx2) == list(idx)
+    np.testing.assert_allclose(w2, w, rtol=1e-12)
+
+
+def test_topk_weight_ratio_of_logits_one_apart():
+    # logits 1 apart: weight ratio e; equal logits: equal weights
+    idx, w = oracle.topk(np.array([0.0, 1.0, 1.0, -5.0]), 3)
+    assert list(idx) == [1, 2, 0]
+    assert w[0] == w[1]
+    assert abs(w[0] / w[2] - np.e) < 1e-14
+
+
+def test_topk_all_experts_equal_logits_is_uniform():
+    idx, w = oracle.topk(np.zeros(8), 8)
+    assert list(idx) == list(range(8))
+    np.testing.assert_allclose(w, np.full(8, 0.125), rtol=0, atol=1e-16)
+
+
+def test_route_one_hot_gate_rows():
+    # gate row e holds bf16 1.0 at column e: logit e = x[e]
+    n, d = 6, 16
+    g = np.zeros((n, d), np.uint16)
+    for e in range(n):
+        g[e, e] = 0x3F80
+    x = np.array([0.5, -2.0, 4.0, 1.0, 4.0, -7.0] + [9.0] * (d - n))
+    logits, a, idx, w = oracle.route(g, n, d, x, 2)
+    np.testing.assert_array_equal(logits, x[:n])
+    np.testing.assert_array_equal(a, np.abs(x[:n]))
+    assert list(idx) == [2, 4] and w[0] == w[1] == 0.5
+
+
+def test_combine_one_hot_and_linearity():
+    rng = np.random.default_rng(4)
+    eo = rng.normal(size=(3, 10))
+    for i in range(3):
+        w = np.zeros(3)
+        w[i] = 1.0
+        out, a = oracle.combine(eo, w)
+        np.testing.assert_array_equal(out, eo[i])
+        np.testing.assert_array_equal(a, np.abs(eo[i]))
+    o1, _ = oracle.combine(eo, np.array([0.2, 0.3, 0.5]))
+    o2, _ = oracle.combine(eo, np.array([0.4, 0.6, 1.0]))
+    np.testing.assert_allclose(o2, 2 * o1, rtol=1e-15)
+
+
 # -------------------------------------------------------------- mutations
 
 MUTATIONS = [
@@ -375,6 +444,12 @@ MUTATIONS = [
      "hidden[i] = oracle_silu(uv[i]) * gv[i];"),
     ("crumb order reversed", "return (b >> (2 * (k % 4))) & 0x03;",
      "return (b >> (6 - 2 * (k % 4))) & 0x03;"),
+    ("ties to the higher index", "return ia < ib;                   /* equal values",
+     "return ia > ib;                   /* equal values"),
+    ("NaN ranked first", "if (na != nb) return nb;", "if (na != nb) return na;"),
+    ("weights not normalised", "for (long r = 0; r < k; ++r) w[r] /= sum;", "(void)sum;"),
+    ("combine weight of the wrong row", "const double t = w[i] * eo[i * d_model + j];",
+     "const double t = w[k - 1 - i] * eo[i * d_model + j];"),
 ]
 
 
