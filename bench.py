@@ -474,6 +474,8 @@ def rows_breakdown(smoe, dev, steps, pattern=""):
             batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T, bits=2)
     if pattern in "q4_experts_batch_8xT16":
         experts_batch_row(smoe, dev, steps, out, hbm_peak, timed, s)
+    if pattern in "route_128x4096_top8":
+        route_row(smoe, dev, steps, out, timed, s)
     if pattern in "q4_ffn_256":
         small_row(smoe, dev, steps, out, timed, s)
     return out
@@ -602,6 +604,27 @@ def experts_batch_row(smoe, dev, steps, out, hbm_peak, timed, s, n=8, T=16):
         "frac": round(b * nl / t_g / 1e9 / hbm_peak, 4), "bytes_per_call": b,
         "single_calls_us": round(t_s / nl * 1e6, 3)}
     del sets
+    torch.cuda.empty_cache()
+
+
+def route_row(smoe, dev, steps, out, timed, s, n=128, d=D_MODEL, k=N_EXPERTS):
+    """Router of one token (bf16 gate 128 x 4096, top-8 with weights) and the
+    combine of 8 expert outputs."""
+    import torch
+    ncp = 8
+    gs = [torch.from_numpy(inp.bf16_rows(n, d, 10, 1 + c).view(np.int16)).to(dev) for c in range(ncp)]
+    x = torch.from_numpy(inp.activations(d, 10)).to(dev)
+    logits = torch.empty(n, device=dev)
+    idx = torch.empty(k, dtype=torch.int32, device=dev)
+    w = torch.empty(k, device=dev)
+    eo = torch.from_numpy(inp.activations((k, d), 11)).to(dev)
+    y = torch.empty(d, device=dev)
+    nl = max(20, min(steps // 4, 400))
+    t_r = timed(lambda i: smoe.smoe_route_topk_bf16(gs[i % ncp], x, n, d, k, logits, idx, w, stream=s), nl)
+    t_c = timed(lambda i: smoe.smoe_combine(k, eo, w, y, d, stream=s), nl)
+    out[f"route_{n}x{d}_top{k}"] = {"us_per_route": round(t_r / nl * 1e6, 3),
+                                    "us_per_combine": round(t_c / nl * 1e6, 3)}
+    del gs
     torch.cuda.empty_cache()
 
 

@@ -347,6 +347,47 @@ int smoe_experts_ffn_batch_q2(int n_experts, const uint8_t *const *gate_codes,
                               void *workspace, size_t workspace_bytes,
                               void *stream);
 
+/* Limits of smoe_route_topk_bf16. */
+#define SMOE_MAX_TOP_K 64
+#define SMOE_MAX_ROUTE_EXPERTS 8192
+
+/*
+ * Router of one token: logits of a bf16 gate matrix and the top-k experts
+ * with their weights.  The page runs this "exact-routing gate matvec"
+ * (n_experts x d_model) on the host and leaves selection and weighting
+ * open; the reading implemented here:
+ *
+ *   logits[e] = sum_k bf16(gate_w[e][k]) * x[k]          (as matvec_bf16)
+ *   top_idx   = the k largest logits in descending order, ties to the lower
+ *               expert index, NaN below every number
+ *   top_w[r]  = exp(logits[top_idx[r]] - logits[top_idx[0]])
+ *               / sum over r' < k of exp(logits[top_idx[r']] - logits[top_idx[0]])
+ *
+ * gate_w: bf16 [n_experts x d_model]; x: f32 [d_model]; logits: f32
+ * [n_experts], top_idx: int32 [k], top_w: f32 [k], all device memory
+ * written by the call (16-byte aligned inputs; outputs 4-byte aligned).
+ * 1 <= k <= min(n_experts, SMOE_MAX_TOP_K), n_experts <=
+ * SMOE_MAX_ROUTE_EXPERTS, d_model a multiple of 8 and at most SMOE_MAX_COLS.
+ * Outputs may not overlap inputs or each other.  Two launches (the matvec,
+ * then one CTA for the selection).
+ */
+int smoe_route_topk_bf16(const uint16_t *gate_w, const float *x, int n_experts,
+                         int d_model, int k, float *logits, int *top_idx,
+                         float *top_w, void *stream);
+
+/*
+ * Weighted combine of a token's k expert outputs (the reading above):
+ *
+ *   out[j] = sum over r < k, in order, of top_w[r] * expert_out[r][j]
+ *
+ * expert_out: f32 [k x d_model] (row r the output of the r-th selected
+ * expert, e.g. rows of smoe_experts_ffn_q4's out in selection order); top_w:
+ * f32 [k] on the device; out: f32 [d_model], written.  k >= 0 (k == 0
+ * writes zeros); out may not overlap the inputs.
+ */
+int smoe_combine(int k, const float *expert_out, const float *top_w,
+                 float *out, int d_model, void *stream);
+
 /* Size of the device array ffn_batch_q4_noalloc uses as its workspace. */
 #define SMOE_NOALLOC_SCRATCH_BYTES (32u << 20)
 

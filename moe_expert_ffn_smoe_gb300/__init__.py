@@ -60,6 +60,8 @@ _SIGS = {
     "smoe_ffn_batch_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "ffn_batch_q4": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "ffn_batch_q2": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "smoe_route_topk_bf16": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
+    "smoe_combine": ([_I, _P, _P, _P, _I, _P], _I),
     "smoe_experts_ffn_batch_workspace_bytes": ([_I, _P, _I, _I, _I], _SZ),
     "smoe_experts_ffn_batch_q4": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
     "smoe_experts_ffn_batch_q2": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
@@ -248,6 +250,20 @@ def ffn_batch_q2(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_
                              _ptr(down_codes), _ptr(down_scales), _ptr(X), _ptr(Y), T, d_model,
                              d_ff, group, _ptr(workspace), workspace_bytes, _stream(stream)),
            "ffn_batch_q2")
+
+
+SMOE_MAX_TOP_K = 64
+SMOE_MAX_ROUTE_EXPERTS = 8192
+
+
+def smoe_route_topk_bf16(gate_w, x, n_experts, d_model, k, logits, top_idx, top_w, stream=None):
+    _check(_lib.smoe_route_topk_bf16(_ptr(gate_w), _ptr(x), n_experts, d_model, k, _ptr(logits), _ptr(top_idx),
+                                     _ptr(top_w), _stream(stream)), "smoe_route_topk_bf16")
+
+
+def smoe_combine(k, expert_out, top_w, out, d_model, stream=None):
+    _check(_lib.smoe_combine(k, _ptr(expert_out), _ptr(top_w), _ptr(out), d_model, _stream(stream)),
+           "smoe_combine")
 
 
 def smoe_experts_ffn_batch_workspace_bytes(T, d_model, d_ff, group):

@@ -585,6 +585,42 @@ int smoe_experts_ffn_batch_q2(int n_experts, const uint8_t *const *gate_codes, c
                               X, Y, T, d_model, d_ff, group, workspace, workspace_bytes, stream);
 }
 
+int smoe_route_topk_bf16(const uint16_t *gate_w, const float *x, int n_experts, int d_model, int k, float *logits,
+                         int *top_idx, float *top_w, void *stream)
+{
+    if (n_experts < 1 || n_experts > SMOE_MAX_ROUTE_EXPERTS) return SMOE_ERR_SHAPE;
+    if (k < 1 || k > n_experts || k > SMOE_MAX_TOP_K) return SMOE_ERR_SHAPE;
+    if (d_model < 0 || d_model > SMOE_MAX_COLS || d_model % 8 != 0) return SMOE_ERR_SHAPE;
+    if (!logits || !top_idx || !top_w) return SMOE_ERR_NULL;
+    if (d_model > 0 && (!gate_w || !x)) return SMOE_ERR_NULL;
+    if (!aligned16(logits) || (d_model > 0 && (!aligned16(gate_w) || !aligned16(x)))) return SMOE_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(top_idx) & 3u) || (reinterpret_cast<uintptr_t>(top_w) & 3u))
+        return SMOE_ERR_ALIGN;
+    const Span outs[3] = {{logits, static_cast<size_t>(n_experts) * sizeof(float)},
+                          {top_idx, static_cast<size_t>(k) * sizeof(int)},
+                          {top_w, static_cast<size_t>(k) * sizeof(float)}};
+    const Span ins[2] = {{gate_w, static_cast<size_t>(n_experts) * static_cast<size_t>(d_model) * 2},
+                         {x, static_cast<size_t>(d_model) * sizeof(float)}};
+    if (any_alias(outs, 3, ins, d_model > 0 ? 2 : 0)) return SMOE_ERR_ALIAS;
+    return to_status(smoe::launch_route(gate_w, x, n_experts, d_model, k, logits, top_idx, top_w,
+                                        static_cast<cudaStream_t>(stream)));
+}
+
+int smoe_combine(int k, const float *expert_out, const float *top_w, float *out, int d_model, void *stream)
+{
+    if (k < 0 || d_model < 0) return SMOE_ERR_SHAPE;
+    if (d_model == 0) return SMOE_OK;
+    if (!out || (k > 0 && (!expert_out || !top_w))) return SMOE_ERR_NULL;
+    if ((reinterpret_cast<uintptr_t>(out) & 3u) || (k > 0 && ((reinterpret_cast<uintptr_t>(expert_out) & 3u) ||
+                                                             (reinterpret_cast<uintptr_t>(top_w) & 3u))))
+        return SMOE_ERR_ALIGN;
+    const Span o[1] = {{out, static_cast<size_t>(d_model) * sizeof(float)}};
+    const Span ins[2] = {{expert_out, static_cast<size_t>(k) * static_cast<size_t>(d_model) * sizeof(float)},
+                         {top_w, static_cast<size_t>(k) * sizeof(float)}};
+    if (any_alias(o, 1, ins, k > 0 ? 2 : 0)) return SMOE_ERR_ALIAS;
+    return to_status(smoe::launch_combine(k, expert_out, top_w, out, d_model, static_cast<cudaStream_t>(stream)));
+}
+
 int smoe_last_device_status(void *stream)
 {
     unsigned v = 0;

@@ -55,6 +55,12 @@ cudaError_t launch_bf16_gemv(const uint16_t *w, const float *x, float *y, int ro
 cudaError_t launch_bf16_gemv_batch(int n, const uint16_t *const *w, const float *const *x, float *const *y,
                                    const int *rows, const int *cols, cudaStream_t stream);
 
+// Router logits (bf16 matvec), then top-k indices and weights (route.cu).
+cudaError_t launch_route(const uint16_t *gate_w, const float *x, int n_experts, int d_model, int k, float *logits,
+                         int *idx, float *w, cudaStream_t stream);
+// out = sum_i w[i] eo[i] over k rows of d_model (route.cu).
+cudaError_t launch_combine(int k, const float *eo, const float *w, float *out, int d_model, cudaStream_t stream);
+
 // Token batch: Y[T x units] = W X^T for T tokens (nmat == 2: fused gate/up,
 // Y = hidden).  Shapes already validated.
 cudaError_t launch_qgemm_tokens(int bits, int nmat, const uint8_t *const codes[2],

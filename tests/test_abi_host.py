@@ -242,3 +242,28 @@ def test_experts_batch_workspace_and_refusals(smoe):
     Y2 = [Y[0], 0, Y[2]]
     assert f(*args(X=X2, Y=Y2, wsp=0)) == smoe.SMOE_ERR_WORKSPACE                       # still needs the workspace
     assert smoe._lib.smoe_experts_ffn_batch_q2(*args(group=32)) == smoe.SMOE_ERR_SHAPE  # Q2 groups of 64
+
+
+def test_route_and_combine_refusals(smoe):
+    L = smoe._lib
+    g, x = A, A + 0x1000000
+    lg, ix, w = A + 0x2000000, A + 0x2100000, A + 0x2200000
+    r = lambda n=128, d=4096, k=8, g=g, x=x, lg=lg, ix=ix, w=w: L.smoe_route_topk_bf16(g, x, n, d, k, lg, ix, w, None)
+    assert r(k=0) == smoe.SMOE_ERR_SHAPE
+    assert r(k=129) == smoe.SMOE_ERR_SHAPE
+    assert r(n=200, k=smoe.SMOE_MAX_TOP_K + 1) == smoe.SMOE_ERR_SHAPE
+    assert r(n=smoe.SMOE_MAX_ROUTE_EXPERTS + 1) == smoe.SMOE_ERR_SHAPE
+    assert r(d=4100) == smoe.SMOE_ERR_SHAPE
+    assert r(n=0) == smoe.SMOE_ERR_SHAPE
+    assert r(lg=0) == smoe.SMOE_ERR_NULL
+    assert r(g=0) == smoe.SMOE_ERR_NULL
+    assert r(lg=lg + 4) == smoe.SMOE_ERR_ALIGN
+    assert r(ix=ix + 2) == smoe.SMOE_ERR_ALIGN
+    assert r(lg=g + 1024) == smoe.SMOE_ERR_ALIAS          # logits inside the gate matrix
+    assert r(w=ix + 16) == smoe.SMOE_ERR_ALIAS            # weights over the indices
+    c = lambda k=8, eo=A, tw=A + 0x100000, out=A + 0x200000, d=4096: L.smoe_combine(k, eo, tw, out, d, None)
+    assert c(k=-1) == smoe.SMOE_ERR_SHAPE
+    assert c(d=0) == smoe.SMOE_OK
+    assert c(eo=0) == smoe.SMOE_ERR_NULL
+    assert c(out=A + 0x200002) == smoe.SMOE_ERR_ALIGN
+    assert c(out=A + 4096) == smoe.SMOE_ERR_ALIAS          # out inside the expert outputs
