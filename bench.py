@@ -621,8 +621,10 @@ def route_row(smoe, dev, steps, out, timed, s, n=128, d=D_MODEL, k=N_EXPERTS):
     y = torch.empty(d, device=dev)
     nl = max(20, min(steps // 4, 400))
     t_r = timed(lambda i: smoe.smoe_route_topk_bf16(gs[i % ncp], x, n, d, k, logits, idx, w, stream=s), nl)
+    t_l = timed(lambda i: smoe.matvec_bf16(gs[i % ncp], x, logits, n, d, stream=s), nl)
     t_c = timed(lambda i: smoe.smoe_combine(k, eo, w, y, d, stream=s), nl)
     out[f"route_{n}x{d}_top{k}"] = {"us_per_route": round(t_r / nl * 1e6, 3),
+                                    "us_per_logits_matvec": round(t_l / nl * 1e6, 3),
                                     "us_per_combine": round(t_c / nl * 1e6, 3)}
     del gs
     torch.cuda.empty_cache()

@@ -51,6 +51,8 @@ def _route(smoe, dev, g, x, n, d, k):
     (3, 16, 3, 3),          # every expert selected
     (8192, 512, 64, 4),     # the largest n and k accepted
     (130, 2048, 7, 5),      # a ragged expert count
+    (256, 1024, 64, 11),    # the largest n of the rank-counting selection
+    (257, 1024, 8, 12),     # the smallest n of the round-by-round selection
 ])
 def test_route(smoe, dev, n, d, k, seed):
     g = inp.bf16_rows(n, d, seed, 1)
@@ -63,23 +65,29 @@ def test_route(smoe, dev, n, d, k, seed):
     np.testing.assert_allclose(w, ow, rtol=2e-6, atol=1e-7)
 
 
-def test_route_ties_go_to_the_lower_index(smoe, dev):
-    n, d, k = 16, 64, 6
+@pytest.mark.parametrize("n", [16, 600])
+def test_route_ties_go_to_the_lower_index(smoe, dev, n):
+    """Three equal rows holding the largest logit: all three are selected,
+    in ascending index order, ahead of every other expert."""
+    d, k = 64, 6
     g = inp.bf16_rows(n, d, 6, 1)
-    g[9] = g[2]                   # equal rows: equal logits
-    g[12] = g[2]
     x = inp.activations(d, 6)
+    ref, _ = oracle.matvec_bf16(g, n, d, x.astype(np.float64))
+    m = int(np.argmax(ref))
+    tied = sorted({m, (m + 7) % n, (m + n // 2) % n})
+    for e in tied:
+        g[e] = g[m]
     logits, idx, w = _route(smoe, dev, g, x, n, d, k)
-    assert logits[2] == logits[9] == logits[12]
+    assert logits[tied[0]] == logits[tied[1]] == logits[tied[2]]
     oi, ow = oracle.topk(logits.astype(np.float64), k)
     np.testing.assert_array_equal(idx, oi)
-    pos = {int(e): r for r, e in enumerate(idx)}
-    if 2 in pos and 9 in pos:
-        assert pos[2] < pos[9]
+    np.testing.assert_array_equal(idx[:3], tied)
+    assert w[0] == w[1] == w[2]
 
 
-def test_route_nan_token_selects_by_index(smoe, dev):
-    n, d, k = 32, 64, 4
+@pytest.mark.parametrize("n", [32, 300])
+def test_route_nan_token_selects_by_index(smoe, dev, n):
+    d, k = 64, 4
     g = inp.bf16_rows(n, d, 7, 1)
     x = inp.activations(d, 7)
     x[5] = np.nan
