@@ -433,6 +433,19 @@ int ffn_batch_q4_noalloc(const uint8_t *gate_codes, const float *gate_scales,
  */
 int smoe_last_device_status(void *stream);
 
+/*
+ * Diagnostic of the device-side failure detection: launches one warp whose
+ * bounded wait can never succeed -- kind 0: an mbarrier that expects two
+ * arrivals and gets one; kind 1: a device counter that nothing increments --
+ * with the limit the kernels use (about two seconds of SM clock).  The wait
+ * gives up, records a timeout in the status word and the warp returns with
+ * nothing in flight, so the context stays usable; the next
+ * smoe_last_device_status(stream) returns SMOE_ERR_TIMEOUT.  Asynchronous:
+ * returns SMOE_OK once launched, SMOE_ERR_SHAPE for another kind, and
+ * SMOE_ERR_LAUNCH if CUDA refuses the launch.
+ */
+int smoe_selftest_bounded_wait(int kind, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -67,6 +67,7 @@ _SIGS = {
     "smoe_experts_ffn_batch_q2": ([_I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
     "ffn_batch_q4_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "smoe_last_device_status": ([_P], _I),
+    "smoe_selftest_bounded_wait": ([_I, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -310,3 +311,9 @@ def ffn_batch_q4_noalloc(gate_codes, gate_scales, up_codes, up_scales, down_code
 
 def smoe_last_device_status(stream=None):
     return _lib.smoe_last_device_status(_stream(stream))
+
+
+def smoe_selftest_bounded_wait(kind, stream=None):
+    """One warp whose bounded wait never succeeds (kind 0: mbarrier, 1: device
+    counter); smoe_last_device_status then reports SMOE_ERR_TIMEOUT."""
+    _check(_lib.smoe_selftest_bounded_wait(kind, _stream(stream)), "smoe_selftest_bounded_wait")

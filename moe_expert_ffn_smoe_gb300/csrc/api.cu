@@ -621,6 +621,12 @@ int smoe_combine(int k, const float *expert_out, const float *top_w, float *out,
     return to_status(smoe::launch_combine(k, expert_out, top_w, out, d_model, static_cast<cudaStream_t>(stream)));
 }
 
+int smoe_selftest_bounded_wait(int kind, void *stream)
+{
+    if (kind != 0 && kind != 1) return SMOE_ERR_SHAPE;
+    return to_status(smoe::launch_bounded_wait_selftest(kind, static_cast<cudaStream_t>(stream)));
+}
+
 int smoe_last_device_status(void *stream)
 {
     unsigned v = 0;

@@ -177,4 +177,24 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return false;
 }
 
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Waits (bounded, about two seconds of SM clock) until *p >= target.
+__device__ __forceinline__ bool wait_count(const unsigned *p, unsigned target)
+{
+    if (ld_acquire_gpu(p) >= target) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 0; i < (1u << 24); ++i) {
+        __nanosleep(128);
+        if (ld_acquire_gpu(p) >= target) return true;
+        if (clock64() - t0 > 4000000000LL) break;
+    }
+    return false;
+}
+
 }  // namespace smoe

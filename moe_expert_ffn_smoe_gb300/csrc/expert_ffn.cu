@@ -47,26 +47,6 @@ struct FFNArgs {
 
 namespace {
 
-__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
-{
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Waits (bounded, about two seconds of SM clock) until *p >= target.
-__device__ bool wait_count(const unsigned *p, unsigned target)
-{
-    if (ld_acquire_gpu(p) >= target) return true;
-    const long long t0 = clock64();
-    for (uint32_t i = 0; i < (1u << 24); ++i) {
-        __nanosleep(128);
-        if (ld_acquire_gpu(p) >= target) return true;
-        if (clock64() - t0 > 4000000000LL) break;
-    }
-    return false;
-}
-
 template <int BITS, int L1, int CPL1, int L2, int CPL2>
 __global__ void __launch_bounds__(384, 1) expert_ffn(const __grid_constant__ FFNArgs a)
 {

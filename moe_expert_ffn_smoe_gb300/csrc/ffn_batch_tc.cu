@@ -540,6 +540,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_word;
+    // A wait that gives up ends its role's loop and sets `failed`; `issued`
+    // counts the copies (code chunks, token blocks) or MMA groups the role
+    // started, so that they can be waited for before the CTA releases its
+    // shared and tensor memory.
+    bool failed = false;
+    int issued = 0;
     // Gate/up lets the down projection start its weight-only prologue now (it
     // lands on SMs this grid does not hold: one CTA fills an SM); whatever it
     // reads from this grid, and whatever it overwrites that this grid reads,
@@ -551,11 +557,13 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
     if (warp == CODE_WARP) {
         // ---- code chunks (weights never depend on an earlier kernel)
         if (lane == 0) {
-            for (int c = 0; c < nchunks; ++c) {
+            for (int c = 0; c < nchunks; ++c, ++issued) {
                 const int slot = c % CODE_SLOTS;
                 if (c >= CODE_SLOTS &&
-                    !mbar_wait_bounded(cempty0 + 8 * slot, ((c / CODE_SLOTS) - 1) & 1, a.status, 7u))
+                    !mbar_wait_bounded(cempty0 + 8 * slot, ((c / CODE_SLOTS) - 1) & 1, a.status, 7u)) {
+                    failed = true;
                     break;
+                }
                 const uint32_t dst = codes0 + slot * CHUNK_BYTES;
                 const int x = (kt0 + c * CHUNK_KT) * TILE_BYTES;  // byte offset along the row: multiple of 16
                 mbar_arrive_expect_tx(cfull0 + 8 * slot, CHUNK_BYTES);
@@ -572,9 +580,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
         pdl_wait();
         if (lane == 0) {
             const uint8_t *src = a.B + (static_cast<size_t>(gtile) * nkt + kt0) * b_bytes(NT);
-            for (int i = 0; i < nk; ++i) {
+            for (int i = 0; i < nk; ++i, ++issued) {
                 const int s = i % S;
-                if (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 8u)) break;
+                if (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 8u)) {
+                    failed = true;
+                    break;
+                }
                 mbar_arrive_expect_tx(full0 + 8 * s, b_bytes(NT));
                 bulk_g2s(stage0 + s * SB + B_OFF, src + static_cast<size_t>(i) * b_bytes(NT), b_bytes(NT),
                          full0 + 8 * s);
@@ -584,11 +595,14 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
         // ---- MMA issue
         if (lane == 0) {
             const uint32_t idesc = instr_desc(MT, 2 * NT);
-            for (int i = 0; i < nk; ++i) {
+            for (int i = 0; i < nk; ++i, ++issued) {
                 const int s = i % S;
                 const int b = i % NB;
-                if (!mbar_wait_bounded(full0 + 8 * s, (i / S) & 1, a.status, 3u)) break;
-                if (i >= NB && !mbar_wait_bounded(acce0 + 8 * b, ((i / NB) - 1) & 1, a.status, 4u)) break;
+                if (!mbar_wait_bounded(full0 + 8 * s, (i / S) & 1, a.status, 3u) ||
+                    (i >= NB && !mbar_wait_bounded(acce0 + 8 * b, ((i / NB) - 1) & 1, a.status, 4u))) {
+                    failed = true;
+                    break;
+                }
                 tc_fence_after();
                 const uint32_t sa = stage0 + s * SB;
                 const uint32_t sb = sa + B_OFF;
@@ -613,9 +627,12 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
         const uint32_t rsw = static_cast<uint32_t>(r & 7);  // 128-byte swizzle of the chunk rows
         for (int i = 0; i < nk; ++i) {
             const int c = i / CHUNK_KT, sub = i % CHUNK_KT, slot = c % CODE_SLOTS;
-            if (sub == 0 && !mbar_wait_bounded(cfull0 + 8 * slot, (c / CODE_SLOTS) & 1, a.status, 5u)) break;
             const int s = i % S;
-            if (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 5u)) break;
+            if ((sub == 0 && !mbar_wait_bounded(cfull0 + 8 * slot, (c / CODE_SLOTS) & 1, a.status, 5u)) ||
+                (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 5u))) {
+                failed = true;
+                break;
+            }
             const uint32_t row = codes0 + slot * CHUNK_BYTES + static_cast<uint32_t>(r) * 128u;
             const uint32_t sa = stage0 + s * SB;
             if (ATM) {
@@ -695,7 +712,10 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
             const float f = sc_next * fold<BITS>();
             if (i + 1 < nk) sc_next = rok ? ldg_f32(srow + ((kt0 + i + 1) * KT) / a.group) : 0.f;
             const bool ok = mbar_wait_bounded(accf0 + 8 * b, (i / NB) & 1, a.status, 6u);
-            if (!__all_sync(FULL_MASK, ok)) break;
+            if (!__all_sync(FULL_MASK, ok)) {
+                failed = true;
+                break;
+            }
             tc_fence_after();
             // hi columns [c, c + CH) and the matching lo columns, CH at a time
             constexpr int CH = NH < 16 ? NH : (NH > 32 ? 8 : 16);
@@ -751,7 +771,31 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
         }
     }
     tc_fence_before();
-    __syncthreads();
+    if (__syncthreads_or(failed)) {
+        // A wait gave up: outputs are unspecified, but nothing this CTA
+        // started may land after it exits.  Each producer waits (bounded)
+        // for its last copies or MMAs; a completed phase of a barrier
+        // implies the earlier ones of the same barrier.
+        if (lane == 0 && warp == CODE_WARP) {
+            // the last chunk issued into each slot (its full barrier counts
+            // only the producer's arrival and the chunk's bytes)
+            for (int c = issued > CODE_SLOTS ? issued - CODE_SLOTS : 0; c < issued; ++c)
+                mbar_wait_bounded(cfull0 + 8 * (c % CODE_SLOTS), (c / CODE_SLOTS) & 1, nullptr, 0u);
+        } else if (lane == 0 && warp == MMA_WARP && issued > 0) {
+            // the commit of the last MMA group tracks every earlier one
+            const int i = issued - 1;
+            mbar_wait_bounded(accf0 + 8 * (i % NB), (i / NB) & 1, nullptr, 0u);
+        } else if (lane == 0 && warp == BPROD_WARP && issued > 0) {
+            // token blocks share their stage's full barrier with the
+            // converters' arrivals, which a converter that gave up never
+            // makes: give the at most S blocks in flight a bounded time (one
+            // block is at most 64 KB; this is about a millisecond)
+            const long long t0 = clock64();
+            while (clock64() - t0 < 2000000LL) __nanosleep(1000);
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
 
     if (a.nsplit > 1) {
         // ---- split-K: the cluster is the tile's nsplit K splits.  Every

@@ -106,6 +106,9 @@ cudaError_t launch_ffn_batch_experts(int bits, int n, const uint8_t *const *gc, 
 // Reads and clears the device status word of the current device after
 // synchronising `stream`.
 cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned *value);
+// One warp whose bounded wait never succeeds (kind 0: an mbarrier, kind 1:
+// a device counter); it records a timeout in the status word (selftest.cu).
+cudaError_t launch_bounded_wait_selftest(int kind, cudaStream_t stream);
 
 // cudaLaunchKernelEx with programmatic dependent launch enabled.
 template <typename... KArgs, typename... Args>

@@ -267,3 +267,8 @@ def test_route_and_combine_refusals(smoe):
     assert c(eo=0) == smoe.SMOE_ERR_NULL
     assert c(out=A + 0x200002) == smoe.SMOE_ERR_ALIGN
     assert c(out=A + 4096) == smoe.SMOE_ERR_ALIAS          # out inside the expert outputs
+
+
+def test_selftest_refuses_unknown_kind(smoe):
+    for kind in (-1, 2, 7):
+        assert smoe._lib.smoe_selftest_bounded_wait(kind, None) == smoe.SMOE_ERR_SHAPE
