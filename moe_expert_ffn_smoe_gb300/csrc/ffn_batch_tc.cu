@@ -101,13 +101,24 @@ __host__ __device__ constexpr int stages_for(int nt)
 __host__ __device__ constexpr int accbufs_for(int nt) { return 256 / nt < 16 ? 256 / nt : 16; }
 
 // Token tiles of at most 32: the converters store A straight into tensor
-// memory (8 stages of 32 columns after 256 columns of accumulators), so a K
-// tile's A makes no round trip through shared memory.
+// memory (stages of 32 columns after the accumulators), so a K tile's A
+// makes no round trip through shared memory.  Such a CTA takes all 512
+// columns (256 of accumulators, 8 A stages) and holds an SM alone; with
+// tiles of 16 and more tiles than SMs, a CTA takes 256 (128 of
+// accumulators, 4 A stages) so that two share an SM (`two`): two CTAs per
+// SM give each a slower K loop, so this pays only where the tiles would
+// otherwise run in more waves.
 __host__ __device__ constexpr bool a_in_tmem(int nt) { return nt <= 32; }
-constexpr uint32_t A_TMEM_COL0 = 256;
-constexpr int A_TMEM_STAGES = 8;
-__host__ __device__ constexpr int tc_accbufs(int nt) { return a_in_tmem(nt) ? (128 / nt < 8 ? 128 / nt : 8) : accbufs_for(nt); }
-__host__ __device__ constexpr int tc_stages(int nt) { return a_in_tmem(nt) ? A_TMEM_STAGES : stages_for(nt); }
+__host__ __device__ constexpr uint32_t a_tmem_col0(bool two) { return two ? 128u : 256u; }
+__host__ __device__ constexpr int tc_accbufs(int nt, bool two)
+{
+    return a_in_tmem(nt) ? (static_cast<int>(a_tmem_col0(two)) / (2 * nt) < 8 ? static_cast<int>(a_tmem_col0(two)) / (2 * nt) : 8)
+                         : accbufs_for(nt);
+}
+__host__ __device__ constexpr int tc_stages(int nt, bool two)
+{
+    return a_in_tmem(nt) ? (two ? 4 : 8) : stages_for(nt);
+}
 __host__ __device__ constexpr uint32_t tc_stage_bytes(int nt) { return a_in_tmem(nt) ? round1024(b_bytes(nt)) : stage_bytes(nt); }
 
 // Byte offset of (row, 8-column block k8) in a [rows x 64] bf16 tile laid out
@@ -480,15 +491,17 @@ __device__ __forceinline__ void write_hidden_block(const TcArgs &a, const float 
     }
 }
 
-template <int BITS, int NT, bool GU>
-__global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ TcArgs a)
+template <int BITS, int NT, bool GU, bool TWO>
+__global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_constant__ TcArgs a)
 {
     constexpr int CHUNK_KT = chunk_kt<BITS>();
     constexpr int TILE_BYTES = KT * BITS / 8;  // bytes of one row's codes per K tile
     constexpr bool ATM = a_in_tmem(NT);
-    constexpr int NB = tc_accbufs(NT);
-    constexpr uint32_t NCOLS = ATM ? 512u : NB * 2 * NT;  // a power of two in [64, 512]
-    constexpr int S = tc_stages(NT);
+    static_assert(!TWO || NT == 16, "two CTAs per SM only with 16-token tiles");
+    constexpr int NB = tc_accbufs(NT, TWO);
+    constexpr uint32_t ACOL0 = a_tmem_col0(TWO);  // first A stage column (ATM)
+    constexpr uint32_t NCOLS = ATM ? 2u * ACOL0 : NB * 2 * NT;  // a power of two in [64, 512]
+    constexpr int S = tc_stages(NT, TWO);
     constexpr uint32_t SB = tc_stage_bytes(NT);
     constexpr uint32_t B_OFF = ATM ? 0u : A_BYTES;  // B within a stage
     extern __shared__ uint8_t smem_raw[];
@@ -610,7 +623,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
 #pragma unroll
                 for (int kk = 0; kk < KT / 16; ++kk) {
                     if (ATM)
-                        mma_bf16_ta(d, tmem + A_TMEM_COL0 + static_cast<uint32_t>(s * 32 + kk * 8),
+                        mma_bf16_ta(d, tmem + ACOL0 + static_cast<uint32_t>(s * 32 + kk * 8),
                                     smem_desc(sb + kk * 256), idesc, kk != 0);
                     else
                         mma_bf16(d, smem_desc(sa + kk * 256), smem_desc(sb + kk * 256), idesc, kk != 0);
@@ -659,7 +672,7 @@ __global__ void __launch_bounds__(TC_THREADS, 1) tc_ffn(const __grid_constant__ 
                     }
                 }
                 tc_fence_after();  // after the wait for the MMA that last read this stage
-                tmem_st16(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + A_TMEM_COL0 +
+                tmem_st16(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + ACOL0 +
                               static_cast<uint32_t>(s * 32 + 16 * hf),
                           v);
                 tmem_wait_st();
@@ -924,11 +937,11 @@ int active_clusters(K kernel, size_t smem, int csize)
 // K splits (at most 8: a split set is one portable cluster) so that the
 // tiles' clusters fill about one wave of SMs.
 template <typename K>
-GemmPlan plan_gemm(K kernel, size_t smem, int mtiles, int ntiles, int nkt, int sms)
+GemmPlan plan_gemm(K kernel, size_t smem, int mtiles, int ntiles, int nkt, int slots)
 {
     GemmPlan p = {mtiles, nkt, 1};
     const int base = mtiles * ntiles;
-    int maxs = sms / (base > 0 ? base : 1);
+    int maxs = slots / (base > 0 ? base : 1);
     if (maxs > 8) maxs = 8;
     if (maxs > nkt) maxs = nkt;
     while (maxs > 1) {
@@ -1030,23 +1043,32 @@ bool encode_codes(CUtensorMap *map, const uint8_t *codes, int bits, int rows, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BITS, int NT, bool GU>
-cudaError_t launch_gemm(const TcArgs &args, int mtiles, int sms, cudaStream_t stream)
+template <int BITS, int NT, bool GU, bool TWO>
+cudaError_t launch_gemm_k(const TcArgs &args, int mtiles, int sms, cudaStream_t stream)
 {
-    // one CTA per SM: each allocates all 512 TMEM columns, so a second CTA
-    // on the SM would wait in tcgen05.alloc; more than half the shared
-    // memory keeps a second one off
-    size_t smem = 1024 + CODE_SLOTS * CHUNK_BYTES + static_cast<size_t>(tc_stages(NT)) * tc_stage_bytes(NT) + 512;
-    if (smem < (120u << 10)) smem = 120u << 10;
-    auto k = tc_ffn<BITS, NT, GU>;
+    // CTAs per SM: a CTA allocates all 512 TMEM columns (one per SM) or 256
+    // (two per SM), and a CTA beyond that would wait in tcgen05.alloc, so
+    // shared memory is padded to keep it off: more than half of the SM's
+    // 228 KB for one, more than a third for two
+    size_t smem = 1024 + CODE_SLOTS * CHUNK_BYTES + static_cast<size_t>(tc_stages(NT, TWO)) * tc_stage_bytes(NT) + 512;
+    const size_t pad = TWO ? (80u << 10) : (120u << 10);
+    if (smem < pad) smem = pad;
+    auto k = tc_ffn<BITS, NT, GU, TWO>;
     cudaError_t e = ensure_dynamic_smem(k, smem);
     if (e != cudaSuccess) return e;
     TcArgs a = args;
-    const GemmPlan p = plan_gemm(k, smem, mtiles, a.ntiles, a.K / KT, sms);
+    const GemmPlan p = plan_gemm(k, smem, mtiles, a.ntiles, a.K / KT, sms * (TWO ? 2 : 1));
     a.kps = p.kps;
     a.nsplit = p.nsplit;
     return launch_pdl_cluster(k, dim3(mtiles, a.ntiles, a.nsplit), dim3(TC_THREADS), smem, stream,
                               static_cast<unsigned>(a.nsplit), a);
+}
+
+template <int BITS, int NT, bool GU>
+cudaError_t launch_gemm(const TcArgs &args, int mtiles, int sms, cudaStream_t stream)
+{
+    if (NT == 16 && mtiles * args.ntiles > sms) return launch_gemm_k<BITS, 16, GU, true>(args, mtiles, sms, stream);
+    return launch_gemm_k<BITS, NT, GU, false>(args, mtiles, sms, stream);
 }
 
 template <int BITS, bool GU>

@@ -112,3 +112,19 @@ def test_experts_batch_matches_single_expert_calls(smoe, dev):
     torch.cuda.synchronize()
     _check_expert(4, experts[1], Xs[1], Y1.cpu().numpy(), 16, d_model, d_ff, group, "single call", sample=4)
     _check_expert(4, experts[1], Xs[1], Ys[1][:16], 16, d_model, d_ff, group, "grouped call", sample=4)
+
+
+@pytest.mark.parametrize("bits,d_model,d_ff,Ts", [
+    (4, 4096, 1536, [16] * 7 + [9]),            # 192 gate/up and 256 down tiles
+    (2, 4096, 1536, [16] * 7 + [9]),
+    (4, 2048, 2048, [16] * 5 + [12]),           # 192 gate/up tiles, 96 down tiles
+])
+def test_experts_batch_more_tiles_than_sms(smoe, dev, bits, d_model, d_ff, Ts):
+    """16-token tiles outnumbering the SMs: those kernels run two CTAs per SM
+    on half the tensor memory each (the last case only for gate/up, so the
+    two layouts follow each other)."""
+    group = 64
+    experts, Xs, Ys = _run(smoe, dev, bits, Ts, d_model, d_ff, group, 70 + bits)
+    for e, T in enumerate(Ts):
+        _check_expert(bits, experts[e], Xs[e], Ys[e][:T], T, d_model, d_ff, group,
+                      f"Q{bits} expert {e} T={T}", sample=3)
