@@ -359,6 +359,22 @@ def gpu_arm(args, rank, world, local):
     clock_rec = clocks.stop()
     barrier(world)
     t = max_over_ranks(t, world, dev)
+    # distribution: each step between its own events (the stream held while
+    # they are enqueued, so no step waits on the host)
+    n_dist = max(3, min(args.steps, 400))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_dist)]
+    torch.cuda.synchronize()
+    hold_stream(wl.stream, n_dist)
+    with torch.cuda.stream(wl.stream):
+        for i, (a, b) in enumerate(evs):
+            a.record(wl.stream)
+            wl.graphs[i % len(wl.graphs)].replay()
+            b.record(wl.stream)
+    torch.cuda.synchronize()
+    per = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+    per_step = {"median": round(statistics.median(per), 3), "p10": round(per[len(per) // 10], 3),
+                "p90": round(per[(9 * len(per)) // 10], 3), "n": n_dist,
+                "how": "each step (one graph replay) between its own events"}
     t_calls = time_steps(lambda k: calls.run(k), args.steps, calls.stream)
     t_calls = max_over_ranks(t_calls, world, dev)
     t_one = time_steps(lambda k: one.run(k), args.steps, one.stream)
@@ -437,6 +453,7 @@ def gpu_arm(args, rank, world, local):
                              "programmatic dependent launch between kernels",
                    "parallelism": f"replicas x{world} (experts are independent; no collective)"},
         "us_per_8expert_ffn": round(ms * 1e3, 3),
+        "per_step_us": per_step,
         "one_call": {"GB/s": round(sb * args.steps * world / t_one / 1e9, 2),
                      "us_per_8expert_ffn": round(t_one / args.steps * 1e6, 3),
                      "launch": "1 C-ABI call per step (smoe_experts_ffn_q4: one launch for gate/up and "
