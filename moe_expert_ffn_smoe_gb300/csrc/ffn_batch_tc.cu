@@ -608,11 +608,11 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
         // ---- MMA issue
         if (lane == 0) {
             const uint32_t idesc = instr_desc(MT, 2 * NT);
+            int s = 0, b = 0;
+            uint32_t spar = 0, bpar = 0;  // stage and accumulator buffer, round parities
             for (int i = 0; i < nk; ++i, ++issued) {
-                const int s = i % S;
-                const int b = i % NB;
-                if (!mbar_wait_bounded(full0 + 8 * s, (i / S) & 1, a.status, 3u) ||
-                    (i >= NB && !mbar_wait_bounded(acce0 + 8 * b, ((i / NB) - 1) & 1, a.status, 4u))) {
+                if (!mbar_wait_bounded(full0 + 8 * s, spar, a.status, 3u) ||
+                    (i >= NB && !mbar_wait_bounded(acce0 + 8 * b, bpar ^ 1u, a.status, 4u))) {
                     failed = true;
                     break;
                 }
@@ -630,6 +630,14 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                 }
                 mma_commit(empty0 + 8 * s);
                 mma_commit(accf0 + 8 * b);
+                if (++s == S) {
+                    s = 0;
+                    spar ^= 1u;
+                }
+                if (++b == NB) {
+                    b = 0;
+                    bpar ^= 1u;
+                }
             }
         }
     } else if (warp >= CONV_WARP0) {
@@ -638,11 +646,13 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
         const int ct = threadIdx.x - CONV_WARP0 * 32;
         const int r = ct & (MT - 1), hf = ct >> 7;
         const uint32_t rsw = static_cast<uint32_t>(r & 7);  // 128-byte swizzle of the chunk rows
+        // K tile i: tile `sub` of the chunk in code slot `slot` (fill parity
+        // cpar), stage s (round parity spar); counters instead of divisions
+        int sub = 0, slot = 0, s = 0;
+        uint32_t cpar = 0, spar = 0;
         for (int i = 0; i < nk; ++i) {
-            const int c = i / CHUNK_KT, sub = i % CHUNK_KT, slot = c % CODE_SLOTS;
-            const int s = i % S;
-            if ((sub == 0 && !mbar_wait_bounded(cfull0 + 8 * slot, (c / CODE_SLOTS) & 1, a.status, 5u)) ||
-                (i >= S && !mbar_wait_bounded(empty0 + 8 * s, ((i / S) - 1) & 1, a.status, 5u))) {
+            if ((sub == 0 && !mbar_wait_bounded(cfull0 + 8 * slot, cpar, a.status, 5u)) ||
+                (i >= S && !mbar_wait_bounded(empty0 + 8 * s, spar ^ 1u, a.status, 5u))) {
                 failed = true;
                 break;
             }
@@ -701,6 +711,17 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                 mbar_arrive(full0 + 8 * s);
                 if (sub == CHUNK_KT - 1 || i == nk - 1) mbar_arrive(cempty0 + 8 * slot);
             }
+            if (++s == S) {
+                s = 0;
+                spar ^= 1u;
+            }
+            if (++sub == CHUNK_KT) {
+                sub = 0;
+                if (++slot == CODE_SLOTS) {
+                    slot = 0;
+                    cpar ^= 1u;
+                }
+            }
         }
     } else {
         // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. + 31 (= tile
@@ -719,12 +740,20 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
         float y[NH];
 #pragma unroll
         for (int n = 0; n < NH; ++n) y[n] = 0.f;
-        float sc_next = (rok && nk > 0) ? ldg_f32(srow + (kt0 * KT) / a.group) : 0.f;
+        // scale group gnext holds the next K tile to fold, its rnext-th of tpg
+        const int tpg = a.group / KT;
+        int gnext = kt0 / tpg, rnext = kt0 - gnext * tpg;
+        float sc_next = (rok && nk > 0) ? ldg_f32(srow + gnext) : 0.f;
+        int b = 0;
+        uint32_t bpar = 0;  // accumulator buffer b, round parity
         for (int i = 0; i < nk; ++i) {
-            const int b = i % NB;
             const float f = sc_next * fold<BITS>();
-            if (i + 1 < nk) sc_next = rok ? ldg_f32(srow + ((kt0 + i + 1) * KT) / a.group) : 0.f;
-            const bool ok = mbar_wait_bounded(accf0 + 8 * b, (i / NB) & 1, a.status, 6u);
+            if (++rnext == tpg) {
+                rnext = 0;
+                ++gnext;
+            }
+            if (i + 1 < nk) sc_next = rok ? ldg_f32(srow + gnext) : 0.f;
+            const bool ok = mbar_wait_bounded(accf0 + 8 * b, bpar, a.status, 6u);
             if (!__all_sync(FULL_MASK, ok)) {
                 failed = true;
                 break;
@@ -745,6 +774,10 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(acce0 + 8 * b);
+            if (++b == NB) {
+                b = 0;
+                bpar ^= 1u;
+            }
         }
 
         if (a.nsplit == 1) {
