@@ -411,6 +411,16 @@ def gpu_arm(args, rank, world, local):
                       f"is ahead: {t_gu_alone * 1e6:.3f} us",
             "peak_kind": f"{peak_kind} burst HBM copy bandwidth"}
 
+    # The other kernel of the step, timed the same way.
+    dn_ptrs = [[[t[k] for t in ex] for k in ("down_codes", "down_scales")] for ex in wl.copies]
+    t_dn = kernel_chain_seconds(lambda i: smoe.smoe_experts_down_q4(*dn_ptrs[i % len(wl.copies)], wl.hidden, wl.out,
+                                                                    D_MODEL, D_FF, GROUP, stream=wl.stream),
+                                nlaunch, wl.stream)
+    dn_bytes = N_EXPERTS * q_bytes(4, D_MODEL, D_FF, GROUP) + N_EXPERTS * D_FF * 4 + N_EXPERTS * D_MODEL * 4
+    down_kernel = {"kernel": "qgemv_reg<Q4,down> (smoe_experts_down_q4, 8 experts x 4096x1536)",
+                   "us_per_launch": round(t_dn * 1e6, 3), "GB/s": round(dn_bytes / t_dn / 1e9, 1),
+                   "frac": round(dn_bytes / t_dn / 1e9 / hbm_peak, 4), "algorithmic_bytes_per_launch": dn_bytes}
+
     # End to end: token in from pinned host memory, outputs back to pinned host memory.
     x_host = torch.from_numpy(inp.activations(D_MODEL, 5)).pin_memory()
     out_host = torch.empty((N_EXPERTS, D_MODEL)).pin_memory()
@@ -456,7 +466,7 @@ def gpu_arm(args, rank, world, local):
                              "launch": "16 single-expert calls (8 x smoe_gate_up_q4 + smoe_down_q4) per "
                                        "step in a CUDA graph"},
         "hbm_frac": round(value / world / hbm_peak, 4),
-        "roofline": roof, "e2e": e2e, "gpu_launches": 2 * args.steps,
+        "roofline": roof, "down_kernel": down_kernel, "e2e": e2e, "gpu_launches": 2 * args.steps,
         "clocks": clock_rec,
     }
     return result, wl, smoe, dev
@@ -512,8 +522,22 @@ def q2_row(smoe, dev, steps, out, hbm_peak):
     n = max(50, steps // 4)
     t = time_steps(lambda k: q2.run(k), n, q2.stream)
     sb = step_bytes(2)
+    # each grouped kernel alone, in a chain of launches on rotating copies
+    nc = len(q2.copies)
+    gu = [[[t[k] for t in ex] for k in ("gate_codes", "gate_scales", "up_codes", "up_scales")] for ex in q2.copies]
+    dn = [[[t[k] for t in ex] for k in ("down_codes", "down_scales")] for ex in q2.copies]
+    t_gu = kernel_chain_seconds(lambda i: smoe.smoe_experts_gate_up_q2(*gu[i % nc], q2.x, q2.hidden, D_FF, D_MODEL,
+                                                                       GROUP, stream=q2.stream), 4 * nc, q2.stream)
+    t_dn = kernel_chain_seconds(lambda i: smoe.smoe_experts_down_q2(*dn[i % nc], q2.hidden, q2.out, D_MODEL, D_FF,
+                                                                    GROUP, stream=q2.stream), 4 * nc, q2.stream)
+    b_gu = N_EXPERTS * 2 * q_bytes(2, D_FF, D_MODEL, GROUP)
+    b_dn = N_EXPERTS * q_bytes(2, D_MODEL, D_FF, GROUP)
     out["q2_8expert_decode"] = {"GB/s": round(sb * n / t / 1e9, 1), "us_per_step": round(t / n * 1e6, 3),
-                                "frac": round(sb * n / t / 1e9 / hbm_peak, 4), "bytes_per_step": sb}
+                                "frac": round(sb * n / t / 1e9 / hbm_peak, 4), "bytes_per_step": sb,
+                                "gate_up_us": round(t_gu * 1e6, 3),
+                                "gate_up_frac": round(b_gu / t_gu / 1e9 / hbm_peak, 4),
+                                "down_us": round(t_dn * 1e6, 3),
+                                "down_frac": round(b_dn / t_dn / 1e9 / hbm_peak, 4)}
     del q2
     torch.cuda.empty_cache()
 
