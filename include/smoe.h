@@ -76,7 +76,8 @@ typedef enum smoe_status {
     SMOE_ERR_WORKSPACE = 4, /* workspace missing or smaller than required       */
     SMOE_ERR_LAUNCH = 5,    /* CUDA refused a launch or a device query          */
     SMOE_ERR_TIMEOUT = 6,   /* a device-side bounded wait gave up               */
-    SMOE_ERR_ALIAS = 7      /* an output overlaps an input or another output    */
+    SMOE_ERR_ALIAS = 7,     /* an output overlaps an input or another output    */
+    SMOE_ERR_MEMORY = 8     /* a buffer is not accessible from the device       */
 } smoe_status;
 
 /* ABI version (SMOE_ABI_VERSION of the built library). */
@@ -432,6 +433,21 @@ int ffn_batch_q4_noalloc(const uint8_t *gate_codes, const float *gate_scales,
  * status word cannot be read.
  */
 int smoe_last_device_status(void *stream);
+
+/*
+ * dst[0 .. bytes) = src[0 .. bytes), copied by the SMs (not a copy engine)
+ * so that a step's input and output transfers run in the same chain of
+ * kernels as its compute (programmatic dependent launch on both sides; the
+ * copy waits for the kernel before it, since that kernel may still read
+ * dst).  Each buffer may be device memory, managed memory or pinned host
+ * memory (cudaHostAlloc / cudaHostRegister / a pinned tensor), which the
+ * SMs read and write over the host link; the caller owns both.  Both
+ * pointers and `bytes` must be multiples of 16.  Asynchronous on `stream`.
+ * Returns SMOE_OK (bytes == 0 is a no-op), SMOE_ERR_NULL, SMOE_ERR_ALIGN,
+ * SMOE_ERR_ALIAS when the ranges overlap, SMOE_ERR_MEMORY when a buffer is
+ * pageable host memory or unknown to CUDA, SMOE_ERR_LAUNCH.
+ */
+int smoe_copy(void *dst, const void *src, size_t bytes, void *stream);
 
 /*
  * Diagnostic of the device-side failure detection: launches one warp whose

@@ -33,6 +33,7 @@ SMOE_ERR_WORKSPACE = 4
 SMOE_ERR_LAUNCH = 5
 SMOE_ERR_TIMEOUT = 6
 SMOE_ERR_ALIAS = 7
+SMOE_ERR_MEMORY = 8
 SMOE_MAX_COLS = 32768
 SMOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 SMOE_FFN_SYNC_BYTES = 512
@@ -68,6 +69,7 @@ _SIGS = {
     "ffn_batch_q4_noalloc": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P], _I),
     "smoe_last_device_status": ([_P], _I),
     "smoe_selftest_bounded_wait": ([_I, _P], _I),
+    "smoe_copy": ([_P, _P, ctypes.c_size_t, _P], _I),
 }
 for _name, (_args, _res) in _SIGS.items():
     _f = getattr(_lib, _name)
@@ -311,6 +313,12 @@ def ffn_batch_q4_noalloc(gate_codes, gate_scales, up_codes, up_scales, down_code
 
 def smoe_last_device_status(stream=None):
     return _lib.smoe_last_device_status(_stream(stream))
+
+
+def smoe_copy(dst, src, nbytes, stream=None):
+    """dst <- src (nbytes) by the SMs; tensors or addresses of device memory or
+    pinned host memory."""
+    _check(_lib.smoe_copy(_ptr(dst), _ptr(src), nbytes, _stream(stream)), "smoe_copy")
 
 
 def smoe_selftest_bounded_wait(kind, stream=None):

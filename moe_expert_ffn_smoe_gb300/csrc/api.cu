@@ -445,6 +445,7 @@ const char *smoe_status_string(int status)
     case SMOE_ERR_LAUNCH: return "CUDA launch or device query failed";
     case SMOE_ERR_TIMEOUT: return "a device-side bounded wait gave up";
     case SMOE_ERR_ALIAS: return "an output overlaps an input or another output";
+    case SMOE_ERR_MEMORY: return "a buffer is not accessible from the device";
     default: return "unknown status";
     }
 }
@@ -619,6 +620,19 @@ int smoe_combine(int k, const float *expert_out, const float *top_w, float *out,
                          {top_w, static_cast<size_t>(k) * sizeof(float)}};
     if (any_alias(o, 1, ins, k > 0 ? 2 : 0)) return SMOE_ERR_ALIAS;
     return to_status(smoe::launch_combine(k, expert_out, top_w, out, d_model, static_cast<cudaStream_t>(stream)));
+}
+
+int smoe_copy(void *dst, const void *src, size_t bytes, void *stream)
+{
+    if (bytes == 0) return SMOE_OK;
+    if (!dst || !src) return SMOE_ERR_NULL;
+    if (((reinterpret_cast<uintptr_t>(dst) | reinterpret_cast<uintptr_t>(src) | bytes) & 15u) != 0)
+        return SMOE_ERR_ALIGN;
+    if (overlap(Span{dst, bytes}, Span{src, bytes})) return SMOE_ERR_ALIAS;
+    void *d = smoe::device_address(dst);
+    const void *s = smoe::device_address(src);
+    if (!d || !s) return SMOE_ERR_MEMORY;
+    return to_status(smoe::launch_copy16(d, s, bytes, static_cast<cudaStream_t>(stream)));
 }
 
 int smoe_selftest_bounded_wait(int kind, void *stream)

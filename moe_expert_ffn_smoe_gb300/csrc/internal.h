@@ -106,6 +106,13 @@ cudaError_t launch_ffn_batch_experts(int bits, int n, const uint8_t *const *gc, 
 // Reads and clears the device status word of the current device after
 // synchronising `stream`.
 cudaError_t read_and_clear_device_status(cudaStream_t stream, unsigned *value);
+// dst[0 .. bytes) = src[0 .. bytes), both device addresses, 16-byte aligned,
+// bytes a multiple of 16, by the SMs (copy.cu).
+cudaError_t launch_copy16(void *dst, const void *src, size_t bytes, cudaStream_t stream);
+// Device address of a device-accessible buffer, null for pageable host
+// memory or an unknown pointer (copy.cu).
+void *device_address(const void *p);
+
 // One warp whose bounded wait never succeeds (kind 0: an mbarrier, kind 1:
 // a device counter); it records a timeout in the status word (selftest.cu).
 cudaError_t launch_bounded_wait_selftest(int kind, cudaStream_t stream);

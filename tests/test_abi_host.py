@@ -272,3 +272,16 @@ def test_route_and_combine_refusals(smoe):
 def test_selftest_refuses_unknown_kind(smoe):
     for kind in (-1, 2, 7):
         assert smoe._lib.smoe_selftest_bounded_wait(kind, None) == smoe.SMOE_ERR_SHAPE
+
+
+def test_copy_refusals(smoe):
+    L = smoe._lib
+    A = 0x7f0000000000
+    assert L.smoe_copy(None, None, 0, None) == smoe.SMOE_OK                # nothing to copy
+    assert L.smoe_copy(None, A, 64, None) == smoe.SMOE_ERR_NULL
+    assert L.smoe_copy(A, None, 64, None) == smoe.SMOE_ERR_NULL
+    assert L.smoe_copy(A + 8, A + 4096, 64, None) == smoe.SMOE_ERR_ALIGN   # dst
+    assert L.smoe_copy(A, A + 4104, 64, None) == smoe.SMOE_ERR_ALIGN       # src
+    assert L.smoe_copy(A, A + 4096, 40, None) == smoe.SMOE_ERR_ALIGN       # size
+    assert L.smoe_copy(A, A + 48, 64, None) == smoe.SMOE_ERR_ALIAS         # overlapping ranges
+    assert smoe.smoe_status_string(smoe.SMOE_ERR_MEMORY) != "unknown status"
