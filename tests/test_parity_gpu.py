@@ -197,6 +197,8 @@ def test_unpack_probes_gate_up(smoe, dev, bits):
     (200, 32768, 12),    # the widest rows: 8 chunks per thread, x read from shared memory
     (777, 4104, 13),     # a ragged last chunk round (513 chunks per row)
     (100, 12288, 14),    # 3 chunks per thread
+    (1024, 8192, 15),    # 2 chunks per thread, fewer rows than 8 per CTA
+    (9, 2056, 17),       # a ragged last chunk round with few rows
 ])
 def test_bf16_full(smoe, dev, rows, cols, seed):
     w = inp.bf16_rows(rows, cols, seed, 1)
