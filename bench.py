@@ -154,6 +154,12 @@ def max_over_ranks(v, world, dev=None):
     return float(t.item())
 
 
+def job_gbs(bytes_per_step, steps, world, seconds):
+    """Whole-job throughput: every rank runs `steps` steps of `bytes_per_step`
+    (weak scaling); `seconds` is the slowest rank's time (max_over_ranks)."""
+    return bytes_per_step * steps * world / seconds / 1e9
+
+
 # ------------------------------------------------------------ the GPU arm
 
 class DecodeWorkload:
@@ -383,7 +389,7 @@ def gpu_arm(args, rank, world, local):
     t_one = max_over_ranks(t_one, world, dev)
 
     sb = step_bytes(4)
-    value = sb * args.steps * world / t / 1e9
+    value = job_gbs(sb, args.steps, world, t)
     ms = t / args.steps * 1e3
     hbm_peak, peak_kind = peaks()
 
