@@ -4,11 +4,15 @@
  *
  * Every operation is defined by the S-MoE documentation page
  * "Metal Compute Kernels"; each declaration names the section it follows.
+ * Two support functions are not steps of that method: smoe_copy (a step's
+ * host I/O) and smoe_selftest_bounded_wait (a diagnostic of the device-side
+ * failure detection).
  *
  * Common conventions
  * ------------------
- * Pointers.  Every pointer argument except `stream` and the results of the
- *   query functions is a DEVICE pointer owned by the caller.  The library
+ * Pointers.  Every pointer argument except `stream`, the results of the
+ *   query functions and the two buffers of smoe_copy (which may also be
+ *   pinned host memory) is a DEVICE pointer owned by the caller.  The library
  *   allocates no memory of its own on any call and keeps no pointer after the
  *   call returns.
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
