@@ -16,8 +16,12 @@
 //    D = sum (c - Z) x / DEN and sum w x = s sum (c - Z) x / Z = s (DEN/Z) D.
 //  * B (tokens, NT x 64) holds x split into two bf16 halves, hi = bf16(x) and
 //    lo = bf16(x - hi), stored as one operand of 2 NT rows (hi rows, then
-//    lo rows), so one MMA of N = 2 NT computes both halves; the epilogue
-//    adds the hi and lo columns (x represented to about 2^-17 relative).
+//    lo rows), x represented to about 2^-17 relative.  Token tiles of 128:
+//    per K step one MMA of N = 128 takes the hi rows and a second the lo
+//    rows, accumulating into the same 128 columns, so four accumulators fit
+//    in TMEM.  Smaller tiles: one MMA of N = 2 NT computes both halves into
+//    2 NT columns and the epilogue adds the hi and lo columns (two MMAs of a
+//    small N cost more than one of twice the N).
 //  * Each 64-column tile's accumulator is read back from TMEM and added to
 //    per-thread f32 sums with the tile's scale.  TMEM holds several tiles'
 //    accumulators, so the MMAs run ahead of the epilogue.
@@ -95,10 +99,13 @@ __host__ __device__ constexpr int stages_for(int nt)
                ? static_cast<int>((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / stage_bytes(nt))
                : 8;
 }
-// TMEM accumulator buffers: as many 2 NT-column buffers as fit in 512
-// columns (at most 16), so the MMAs of later K tiles rarely wait for the
-// epilogue.
-__host__ __device__ constexpr int accbufs_for(int nt) { return 256 / nt < 16 ? 256 / nt : 16; }
+// hi and lo accumulated into the same columns (token tiles of 128)
+__host__ __device__ constexpr bool hilo_shared(int nt) { return nt == 128; }
+// TMEM columns of one accumulator
+__host__ __device__ constexpr int acc_cols(int nt) { return hilo_shared(nt) ? nt : 2 * nt; }
+// TMEM accumulator buffers: as many as fit in 512 columns (at most 16), so
+// the MMAs of later K tiles rarely wait for the epilogue.
+__host__ __device__ constexpr int accbufs_for(int nt) { return 512 / acc_cols(nt) < 16 ? 512 / acc_cols(nt) : 16; }
 
 // Token tiles of at most 32: the converters store A straight into tensor
 // memory (stages of 32 columns after the accumulators), so a K tile's A
@@ -112,7 +119,8 @@ __host__ __device__ constexpr bool a_in_tmem(int nt) { return nt <= 32; }
 __host__ __device__ constexpr uint32_t a_tmem_col0(bool two) { return two ? 128u : 256u; }
 __host__ __device__ constexpr int tc_accbufs(int nt, bool two)
 {
-    return a_in_tmem(nt) ? (static_cast<int>(a_tmem_col0(two)) / (2 * nt) < 8 ? static_cast<int>(a_tmem_col0(two)) / (2 * nt) : 8)
+    return a_in_tmem(nt) ? (static_cast<int>(a_tmem_col0(two)) / acc_cols(nt) < 8
+                                ? static_cast<int>(a_tmem_col0(two)) / acc_cols(nt) : 8)
                          : accbufs_for(nt);
 }
 __host__ __device__ constexpr int tc_stages(int nt, bool two)
@@ -500,7 +508,9 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
     static_assert(!TWO || NT == 16, "two CTAs per SM only with 16-token tiles");
     constexpr int NB = tc_accbufs(NT, TWO);
     constexpr uint32_t ACOL0 = a_tmem_col0(TWO);  // first A stage column (ATM)
-    constexpr uint32_t NCOLS = ATM ? 2u * ACOL0 : NB * 2 * NT;  // a power of two in [64, 512]
+    constexpr bool HL = hilo_shared(NT);
+    constexpr int AC = acc_cols(NT);  // TMEM columns of one accumulator
+    constexpr uint32_t NCOLS = ATM ? 2u * ACOL0 : NB * AC;  // a power of two in [64, 512]
     constexpr int S = tc_stages(NT, TWO);
     constexpr uint32_t SB = tc_stage_bytes(NT);
     constexpr uint32_t B_OFF = ATM ? 0u : A_BYTES;  // B within a stage
@@ -607,7 +617,8 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
     } else if (warp == MMA_WARP) {
         // ---- MMA issue
         if (lane == 0) {
-            const uint32_t idesc = instr_desc(MT, 2 * NT);
+            const uint32_t idesc = instr_desc(MT, HL ? NT : 2 * NT);
+            constexpr uint32_t LO = static_cast<uint32_t>(NT) * 128u;  // the lo rows of a token block
             int s = 0, b = 0;
             uint32_t spar = 0, bpar = 0;  // stage and accumulator buffer, round parities
             for (int i = 0; i < nk; ++i, ++issued) {
@@ -619,14 +630,18 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                 tc_fence_after();
                 const uint32_t sa = stage0 + s * SB;
                 const uint32_t sb = sa + B_OFF;
-                const uint32_t d = tmem + static_cast<uint32_t>(b * 2 * NT);
+                const uint32_t d = tmem + static_cast<uint32_t>(b * AC);
 #pragma unroll
                 for (int kk = 0; kk < KT / 16; ++kk) {
-                    if (ATM)
-                        mma_bf16_ta(d, tmem + ACOL0 + static_cast<uint32_t>(s * 32 + kk * 8),
-                                    smem_desc(sb + kk * 256), idesc, kk != 0);
-                    else
-                        mma_bf16(d, smem_desc(sa + kk * 256), smem_desc(sb + kk * 256), idesc, kk != 0);
+                    if (ATM) {
+                        const uint32_t at = tmem + ACOL0 + static_cast<uint32_t>(s * 32 + kk * 8);
+                        mma_bf16_ta(d, at, smem_desc(sb + kk * 256), idesc, kk != 0);
+                        if (HL) mma_bf16_ta(d, at, smem_desc(sb + LO + kk * 256), idesc, 1u);
+                    } else {
+                        const uint64_t ad = smem_desc(sa + kk * 256);
+                        mma_bf16(d, ad, smem_desc(sb + kk * 256), idesc, kk != 0);
+                        if (HL) mma_bf16(d, ad, smem_desc(sb + LO + kk * 256), idesc, 1u);
+                    }
                 }
                 mma_commit(empty0 + 8 * s);
                 mma_commit(accf0 + 8 * b);
@@ -759,17 +774,18 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                 break;
             }
             tc_fence_after();
-            // hi columns [c, c + CH) and the matching lo columns, CH at a time
+            // columns [c, c + CH) of this warp's half, CH at a time (and,
+            // when hi and lo have their own columns, the lo columns NT later)
             constexpr int CH = NH < 16 ? NH : (NH > 32 ? 8 : 16);
-            const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * 2 * NT + h * NH);
+            const uint32_t tq = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * AC + h * NH);
 #pragma unroll
             for (int c = 0; c < NH; c += CH) {
                 float vh[CH], vl[CH];
                 tmem_ld<CH>(tq + c, vh);
-                tmem_ld<CH>(tq + NT + c, vl);
+                if (!HL) tmem_ld<CH>(tq + NT + c, vl);
                 tmem_wait_ld();
 #pragma unroll
-                for (int n = 0; n < CH; ++n) y[c + n] = fmaf(f, vh[n] + vl[n], y[c + n]);
+                for (int n = 0; n < CH; ++n) y[c + n] = fmaf(f, HL ? vh[n] : vh[n] + vl[n], y[c + n]);
             }
             tc_fence_before();
             __syncwarp();
