@@ -460,7 +460,7 @@ __global__ void __launch_bounds__(256) prep_tokens(const __grid_constant__ PrepA
 
 // One GEMM launch over the token tiles of n experts: global token tile g
 // belongs to the expert e with tile0[e] <= g < tile0[e + 1].
-struct alignas(64) TcArgs {
+struct alignas(128) TcArgs {  // CUtensorMap members are 128-byte aligned
     CUtensorMap tmap[TC_MAX_EXPERTS][2];  // codes: gate and up rows (gate/up) or down rows ([e][0])
     const float *scales[TC_MAX_EXPERTS][2];
     float *Y[TC_MAX_EXPERTS];             // down: [T[e] x M]
