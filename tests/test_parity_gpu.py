@@ -325,6 +325,8 @@ def test_token_batch_small_shape_all_tokens(smoe, dev):
 @pytest.mark.parametrize("d_model,d_ff,group,T", [
     (320, 192, 64, 20),    # code chunks and the last down row tile run past the matrix
     (512, 256, 128, 70),   # groups of 128 columns: one scale per two K tiles
+    (768, 384, 192, 40),   # groups of 192: three K tiles per scale, K splits starting mid-group
+    (768, 384, 192, 16),   # the same with 16-token tiles (A in tensor memory)
 ])
 def test_token_batch_ragged_shapes(smoe, dev, d_model, d_ff, group, T):
     e = inp.expert(4, d_model, d_ff, group, seed=31)
@@ -356,6 +358,7 @@ def test_token_batch_q2(smoe, dev, T):
 @pytest.mark.parametrize("d_model,d_ff,group,T", [
     (320, 192, 64, 20),    # a chunk of 8 K tiles longer than the row: zero fill past the matrix
     (512, 256, 128, 70),   # groups of 128 columns
+    (768, 384, 192, 40),   # groups of 192: three K tiles per scale
     (256, 0, 64, 5),       # no hidden columns: Y = 0
 ])
 def test_token_batch_q2_ragged(smoe, dev, d_model, d_ff, group, T):
