@@ -11,6 +11,23 @@ been built, importing this package raises ImportError.
 Pointer arguments accept a torch.Tensor (its data_ptr()), an int device
 address, or None (NULL).  `stream` accepts a torch.cuda.Stream, an int
 cudaStream_t, or None for torch's current stream on the current device.
+
+One MoE layer for one token, every step on the GPU::
+
+    import moe_expert_ffn_smoe_gb300 as smoe
+    # gate: bf16 bits [n_experts, d_model] as int16; x: f32 [d_model]
+    smoe.smoe_route_topk_bf16(gate, x, n_experts, d_model, k, logits, idx, w)
+    sel = idx.tolist()          # or keep the expert tables on the device
+    smoe.smoe_experts_ffn_q4([gc[e] for e in sel], [gs[e] for e in sel],
+                             [uc[e] for e in sel], [us[e] for e in sel],
+                             [dc[e] for e in sel], [ds[e] for e in sel],
+                             x, expert_out, d_model, d_ff, group, ws, ws_bytes)
+    smoe.smoe_combine(k, expert_out, w, out, d_model)
+
+(`ws`: smoe_experts_ffn_workspace_bytes(k, d_ff) bytes whose first
+SMOE_FFN_SYNC_BYTES are zero before the first call.)  Several tokens per
+expert go through smoe_experts_ffn_batch_q4/q2; a dense bf16 matvec is
+matvec_bf16, many of them in one submission matvec_bf16_batch.
 """
 import ctypes
 import os
