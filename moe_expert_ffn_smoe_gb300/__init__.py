@@ -17,7 +17,7 @@ One MoE layer for one token, every step on the GPU::
     import moe_expert_ffn_smoe_gb300 as smoe
     # gate: bf16 bits [n_experts, d_model] as int16; x: f32 [d_model]
     smoe.smoe_route_topk_bf16(gate, x, n_experts, d_model, k, logits, idx, w)
-    sel = idx.tolist()          # or keep the expert tables on the device
+    sel = idx.tolist()          # the selection comes to the host (a sync)
     smoe.smoe_experts_ffn_q4([gc[e] for e in sel], [gs[e] for e in sel],
                              [uc[e] for e in sel], [us[e] for e in sel],
                              [dc[e] for e in sel], [ds[e] for e in sel],
