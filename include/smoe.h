@@ -401,7 +401,7 @@ int smoe_combine(int k, const float *expert_out, const float *top_w,
  * program that has already divided all device memory among its own pools, a
  * plugin loaded into such a program, or a latency-critical caller for which
  * cudaMalloc's implicit device-wide synchronisation is not acceptable.  The
- * paper has no counterpart to this entry point; it exists only for such
+ * S-MoE page has no counterpart to this entry point; it exists only for such
  * callers.
  *
  * Same arguments, results and checks as ffn_batch_q4, without `workspace`:

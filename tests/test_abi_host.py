@@ -285,3 +285,34 @@ def test_copy_refusals(smoe):
     assert L.smoe_copy(A, A + 4096, 40, None) == smoe.SMOE_ERR_ALIGN       # size
     assert L.smoe_copy(A, A + 48, 64, None) == smoe.SMOE_ERR_ALIAS         # overlapping ranges
     assert smoe.smoe_status_string(smoe.SMOE_ERR_MEMORY) != "unknown status"
+
+
+def test_q2_grouped_and_one_launch_refusals(smoe):
+    """The Q2 grouped and one-launch entries apply the Q2 layout rules
+    (cols a multiple of 64, groups a multiple of 64) before any launch."""
+    L = smoe._lib
+    P = lambda vals: (ctypes.c_void_p * len(vals))(*vals)
+    g = P([A, A + 0x100000])
+    gs = P([A + 0x200000, A + 0x300000])
+    x, h = A + 0x400000, A + 0x500000
+    assert L.smoe_experts_gate_up_q2(2, g, gs, g, gs, x, h, 256, 256, 32, None) == smoe.SMOE_ERR_SHAPE
+    assert L.smoe_experts_gate_up_q2(2, g, gs, g, gs, x, h, 256, 96, 64, None) == smoe.SMOE_ERR_SHAPE
+    assert L.smoe_experts_gate_up_q2(2, None, gs, g, gs, x, h, 256, 256, 64, None) == smoe.SMOE_ERR_NULL
+    assert L.smoe_experts_gate_up_q2(0, None, None, None, None, None, None, 256, 256, 64, None) == smoe.SMOE_OK
+    w = [P([A + 0x1000000 * (6 * e + k) for e in range(2)]) for k in range(6)]
+    x, out, ws = A + 0x40000000, A + 0x41000000, A + 0x42000000
+    need = L.smoe_experts_ffn_workspace_bytes(2, 1536)
+    f = L.smoe_experts_ffn_q2
+    assert f(2, *w, x, out, 4096, 1536, 32, ws, need, None) == smoe.SMOE_ERR_SHAPE     # Q2 groups of 64
+    assert f(2, *w, x, out, 4096, 1536, 64, ws, need - 4, None) == smoe.SMOE_ERR_WORKSPACE
+
+
+def test_noalloc_refusals_before_any_launch(smoe):
+    L = smoe._lib
+    ptrs = [A + 0x1000000 * i for i in range(8)]
+    # a workspace beyond the fixed device array
+    big = 100000
+    assert L.smoe_ffn_batch_workspace_bytes(big, 4096, 1536, 64) > smoe.SMOE_NOALLOC_SCRATCH_BYTES
+    assert L.ffn_batch_q4_noalloc(*ptrs, big, 4096, 1536, 64, None) == smoe.SMOE_ERR_SHAPE
+    assert L.ffn_batch_q4_noalloc(*ptrs, -1, 4096, 1536, 64, None) == smoe.SMOE_ERR_SHAPE
+    assert L.ffn_batch_q4_noalloc(*ptrs, 0, 4096, 1536, 64, None) == smoe.SMOE_OK
