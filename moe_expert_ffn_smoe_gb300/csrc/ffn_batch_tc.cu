@@ -26,10 +26,10 @@
 //    per-thread f32 sums with the tile's scale.  TMEM holds several tiles'
 //    accumulators, so the MMAs run ahead of the epilogue.
 //  * Token tiles of 64 or 128: A goes through shared memory (canonical
-//    no-swizzle K-major layout, proxy fence) and TMEM holds up to 16
+//    no-swizzle K-major layout, proxy fence) and TMEM holds four
 //    accumulators.  Token tiles of 16 or 32: A goes straight into TMEM
-//    (tcgen05.st; 8 stages after 256 columns of accumulators) and the MMAs
-//    read it there.
+//    (tcgen05.st; 8 stages after 256 columns of accumulators, or 4 after 128
+//    when two CTAs share an SM) and the MMAs read it there.
 //
 // Three launches per call, chained with programmatic dependent launch:
 //  1. prep_tokens: X -> B blocks (hi, lo per (token tile, K tile)).
