@@ -52,9 +52,19 @@
  *   error itself stays readable with cudaGetLastError()).
  * Numerics.  Sums are reassociated (lanes, warps, groups), so results are not
  *   bit-identical to a sequential sum; they agree with an exact (f64) result
- *   within 1e-4 * sum_i |w_i x_i| + 1e-6 per output element.  Activations
- *   must be finite: a NaN or infinity in x makes the outputs that read it
- *   NaN.
+ *   within 1e-4 * sum_i |w_i x_i| + 1e-6 per output element for every finite
+ *   x, whatever its dynamic range.  The one-token Q4/Q2 kernels round x per
+ *   16-byte chunk of codes (32 Q4 or 64 Q2 columns) to a power-of-two grid
+ *   that puts the chunk's largest |x| at 2^22 steps or more, take the code x
+ *   x products exactly in integers and fold the scales in f32; the rounding
+ *   adds at most 5.8e-5 (Q4) or 2.3e-5 (Q2) of sum |w x| in the worst case.
+ *   The batch kernels use exact weights (code - Z)/2^b times x split into
+ *   two bf16 halves (tensor cores) or f32 x (CUDA cores).  Activations must
+ *   be finite: a NaN or infinity in x makes the outputs that read it NaN.
+ * Devices.  The library looks up, once per device, the device addresses of
+ *   its own device variables (the status word, the no-allocation workspace);
+ *   after cudaDeviceReset() on a device the library must not be called
+ *   again on that device in the same process.
  */
 #ifndef SMOE_H
 #define SMOE_H
@@ -264,8 +274,11 @@ int matvec_bf16_batch(int n, const uint16_t *const *w, const float *const *x,
  * Bytes of device workspace ffn_batch_q4 and ffn_batch_q2 need for these
  * sizes (the token operand and the hidden activations in the tensor-core
  * operand form, or the hidden activations [T x d_ff] f32 on the CUDA-core
- * path), rounded up to 256.
- * Returns 0 for T <= 0 and (size_t)-1 for sizes the call would refuse.
+ * path), rounded up to 256.  The size depends on d_model (the split token
+ * operand is T x d_model) and on the group and shape (which path runs), not
+ * only on T and d_ff, so all four sizes are arguments.
+ * Returns (size_t)-1 for shapes the call would refuse (checked first, for
+ * any T) and 0 for T <= 0.
  */
 size_t smoe_ffn_batch_workspace_bytes(int T, int d_model, int d_ff, int group);
 
@@ -407,7 +420,8 @@ int smoe_combine(int k, const float *expert_out, const float *top_w,
  * Same arguments, results and checks as ffn_batch_q4, without `workspace`:
  * the workspace is a file-scope device array of SMOE_NOALLOC_SCRATCH_BYTES
  * inside the library, which every GPU that loads the library holds until
- * the process exits.  Calls whose workspace need,
+ * the process exits.  Shapes are checked first, as in ffn_batch_q4 (T == 0
+ * with an invalid shape is refused too).  Calls whose workspace need,
  * smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group), exceeds that size
  * are refused with SMOE_ERR_SHAPE before anything is launched (at
  * d_model = 4096, d_ff = 1536 every T up to 256 fits; for T >= 2 the

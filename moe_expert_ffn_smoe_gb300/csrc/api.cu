@@ -529,10 +529,10 @@ int matvec_bf16_batch(int n, const uint16_t *const *w, const float *const *x, fl
 
 size_t smoe_ffn_batch_workspace_bytes(int T, int d_model, int d_ff, int group)
 {
-    if (T <= 0) return 0;
     if (check_q_shape(4, d_ff, d_model, group) != SMOE_OK ||
         check_q_shape(4, d_model, d_ff, group) != SMOE_OK)
         return static_cast<size_t>(-1);
+    if (T <= 0) return 0;
     return smoe::ffn_batch_workspace(T, d_model, d_ff, group);
 }
 

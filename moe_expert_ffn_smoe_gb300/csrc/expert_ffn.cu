@@ -22,10 +22,11 @@
 // completed launch leaves them zero for the next one; a launch that starts
 // while the previous one still runs touches them only after
 // griddepcontrol.wait, i.e. after that launch has completed.
-// The waits assume all CTAs of the grid are resident together: the grid
-// never exceeds one CTA per SM and each CTA needs most of an SM's shared
-// memory.  A wait that gives up (about two seconds) records a status and
-// skips phase 2; the counters must then be zeroed again by the caller.
+// The waits need all CTAs of the grid resident together: the grid never
+// exceeds one CTA per SM, and it is a cooperative launch, so CUDA starts it
+// only when every CTA can be resident (and refuses a grid that never
+// could).  A wait that still gives up (about two seconds) records a status
+// and skips phase 2; the counters must then be zeroed again by the caller.
 #include "regdot.cuh"
 
 namespace smoe {
@@ -42,7 +43,7 @@ struct FFNArgs {
     int d_model, d_ff, group;
     int ns;                // ring slots per warp
     uint32_t slot_bytes;
-    uint32_t off_info, off_gmax, off_bars, off_slots;
+    uint32_t off_info, off_bars, off_slots;
 };
 
 namespace {
@@ -145,7 +146,7 @@ __global__ void __launch_bounds__(384, 1) expert_ffn(const __grid_constant__ FFN
     if (first > 0) issue(0, 0);  // weights never depend on an earlier kernel
 
     pdl_wait();
-    stage_x_digits<BITS>(a.x, a.d_model, a.group, smem, a.off_info, a.off_gmax);
+    stage_x_digits<BITS>(a.x, a.d_model, a.group, smem, a.off_info);
     __syncthreads();
     if (threadIdx.x == 0) pdl_launch_dependents();
     for (int s = 1; s < first; ++s) issue(s, s);
@@ -213,8 +214,7 @@ __global__ void __launch_bounds__(384, 1) expert_ffn(const __grid_constant__ FFN
 
     // ---- phase 2: down rows of hidden_e -> out
     if (ok) {
-        stage_x_digits<BITS, true>(a.hidden + static_cast<size_t>(e) * a.d_ff, a.d_ff, a.group, smem, a.off_info,
-                                   a.off_gmax);
+        stage_x_digits<BITS, true>(a.hidden + static_cast<size_t>(e) * a.d_ff, a.d_ff, a.group, smem, a.off_info);
         __syncthreads();
         const int team = lane / L2;
         const int u = lane % L2;
@@ -350,13 +350,11 @@ cudaError_t launch_expert_ffn(int bits, int n, const uint8_t *const *gc, const f
     a.group = group;
 
     // shared memory: x digits and chunk info sized for the longer of the two
-    // row lengths, group maxima, per-warp barriers, then the rings
+    // row lengths, per-warp barriers, then the rings
     const int kcmax = kc1 > kc2 ? kc1 : kc2;
-    const int ngmax = ng1 > ng2 ? ng1 : ng2;
     const uint32_t xstride = bits == 4 ? DigitFmt<4>::XSTRIDE : DigitFmt<2>::XSTRIDE;
     a.off_info = static_cast<uint32_t>(kcmax) * xstride;
-    a.off_gmax = a.off_info + static_cast<uint32_t>(kcmax) * 16u;
-    a.off_bars = a.off_gmax + round16u(static_cast<uint32_t>(ngmax) * 4u);
+    a.off_bars = a.off_info + static_cast<uint32_t>(kcmax) * 16u;
     const int teams1 = 32 / L1, teams2 = 32 / L2;
     const uint32_t stage1 = 2u * teams1 * (static_cast<uint32_t>(kc1) * 16u + ng1 * 4u);
     const uint32_t stage2 = 2u * teams2 * (static_cast<uint32_t>(kc2) * 16u + ng2 * 4u);
@@ -379,7 +377,9 @@ cudaError_t launch_expert_ffn(int bits, int n, const uint8_t *const *gc, const f
     *unsupported = false;
     cudaError_t err = ensure_dynamic_smem(k, smem);
     if (err != cudaSuccess) return err;
-    return launch_pdl(k, dim3(static_cast<unsigned>(a.cpe * n)), dim3(nw * 32), smem, stream, a);
+    // cooperative: the CTAs of an expert wait on one another, so the grid
+    // starts only when all of them can be resident together
+    return launch_coop_pdl(k, dim3(static_cast<unsigned>(a.cpe * n)), dim3(nw * 32), smem, stream, a);
 }
 
 }  // namespace smoe

@@ -39,8 +39,7 @@ __global__ void __launch_bounds__(256) qgemm_tokens(QTokArgs a)
     extern __shared__ __align__(16) float4 smem4[];
     const int KC = a.K / F::CODES_PER_CHUNK;
     const int nq = a.K >> 2;
-    float4 *xs = smem4;                                                   // [TT][nq]
-    float *sx = reinterpret_cast<float *>(smem4 + static_cast<size_t>(TT) * nq);  // [TT][KC]
+    float4 *xs = smem4;  // [TT][nq]
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -61,17 +60,16 @@ __global__ void __launch_bounds__(256) qgemm_tokens(QTokArgs a)
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
             const int tok = tb + t < a.T ? tb + t : a.T - 1;  // repeat the last token as padding
-            stage_x_chunks<BITS>(a.X + static_cast<size_t>(tok) * a.K, a.K, xs + static_cast<size_t>(t) * nq,
-                                 sx + static_cast<size_t>(t) * KC);
+            stage_x_chunks<BITS>(a.X + static_cast<size_t>(tok) * a.K, a.K, xs + static_cast<size_t>(t) * nq);
         }
         __syncthreads();
 
         for (int unit = blockIdx.x * nwarps + warp; unit < a.units; unit += gridDim.x * nwarps) {
-            float acc1[NMAT][TT], acc2[NMAT][TT];
+            float acc[NMAT][TT];
 #pragma unroll
             for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-                for (int t = 0; t < TT; ++t) acc1[m][t] = acc2[m][t] = 0.f;
+                for (int t = 0; t < TT; ++t) acc[m][t] = 0.f;
 
             for (int cc = lane; cc < KC; cc += 32) {
                 uint4 cw[NMAT];
@@ -94,7 +92,7 @@ __global__ void __launch_bounds__(256) qgemm_tokens(QTokArgs a)
                     for (int m = 0; m < NMAT; ++m) {
                         const uint32_t w = word_of(cw[m], wi);
 #pragma unroll
-                        for (int i = 0; i < F::CODES_PER_WORD; ++i) f[m][i] = code_as_f32<BITS>(w, i);
+                        for (int i = 0; i < F::CODES_PER_WORD; ++i) f[m][i] = code_centred<BITS>(w, i);
                     }
 #pragma unroll
                     for (int t = 0; t < TT; ++t) {
@@ -114,32 +112,24 @@ __global__ void __launch_bounds__(256) qgemm_tokens(QTokArgs a)
                     }
                 }
 #pragma unroll
-                for (int t = 0; t < TT; ++t) {
-                    const float sxc = sx[t * KC + cc];
+                for (int t = 0; t < TT; ++t)
 #pragma unroll
-                    for (int m = 0; m < NMAT; ++m) {
-                        acc1[m][t] = fmaf(sc[m], P[m][t], acc1[m][t]);
-                        acc2[m][t] = fmaf(sc[m], sxc, acc2[m][t]);
-                    }
-                }
+                    for (int m = 0; m < NMAT; ++m) acc[m][t] = fmaf(sc[m], P[m][t], acc[m][t]);
             }
 #pragma unroll
             for (int m = 0; m < NMAT; ++m)
 #pragma unroll
                 for (int t = 0; t < TT; ++t)
 #pragma unroll
-                    for (int off = 16; off > 0; off >>= 1) {
-                        acc1[m][t] += __shfl_xor_sync(FULL_MASK, acc1[m][t], off);
-                        acc2[m][t] += __shfl_xor_sync(FULL_MASK, acc2[m][t], off);
-                    }
+                    for (int off = 16; off > 0; off >>= 1) acc[m][t] += __shfl_xor_sync(FULL_MASK, acc[m][t], off);
             if (lane == 0) {
 #pragma unroll
                 for (int t = 0; t < TT; ++t) {
                     if (tb + t < a.T) {
-                        const float y0 = F::A * acc1[0][t] - (F::A + 1.0f) * acc2[0][t];
+                        const float y0 = F::A * acc[0][t];
                         float out = y0;
                         if (NMAT == 2) {
-                            const float y1 = F::A * acc1[NMAT - 1][t] - (F::A + 1.0f) * acc2[NMAT - 1][t];
+                            const float y1 = F::A * acc[NMAT - 1][t];
                             out = silu_f32(y0) * y1;
                         }
                         a.Y[static_cast<size_t>(tb + t) * a.units + unit] = out;
@@ -160,7 +150,7 @@ cudaError_t launch_tok(const QTokArgs &a, cudaStream_t stream)
     const DeviceInfo *dev = device_info();
     if (!dev) return cudaErrorInvalidDevice;
     const int KC = a.K / F::CODES_PER_CHUNK;
-    const size_t smem = static_cast<size_t>(TT) * (static_cast<size_t>(a.K) + KC) * sizeof(float);
+    const size_t smem = static_cast<size_t>(TT) * static_cast<size_t>(a.K) * sizeof(float);
     if (smem > static_cast<size_t>(dev->max_smem_optin)) return cudaErrorInvalidValue;
     const int warps = 8;
     long long gx = (static_cast<long long>(a.units) + warps - 1) / warps;

@@ -135,6 +135,28 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
+// launch_pdl as a cooperative launch: CUDA starts the grid only when all of
+// its CTAs can be resident at once (and refuses a grid that never could),
+// which a kernel whose CTAs wait on one another needs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                            cudaStream_t stream, Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // launch_pdl with thread-block clusters of (1, 1, cluster_z) CTAs
 // (cluster_z == 1: no cluster attribute).
 template <typename... KArgs, typename... Args>

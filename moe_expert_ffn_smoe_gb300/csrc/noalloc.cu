@@ -14,6 +14,8 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[SMOE_NOALLOC_SC
 
 // Device address of g_noalloc_scratch on the current device, looked up once
 // per device (in host code the symbol itself is only a host-side stand-in).
+// A cudaDeviceReset() unloads the module, so the library is not used again
+// on a device after one (include/smoe.h, "Devices").
 void *scratch_device_address()
 {
     constexpr int kMaxDevices = 64;
@@ -38,8 +40,10 @@ extern "C" int ffn_batch_q4_noalloc(const uint8_t *gate_codes, const float *gate
                                     const float *X, float *Y, int T, int d_model, int d_ff,
                                     int group, void *stream)
 {
+    if (T < 0) return SMOE_ERR_SHAPE;
+    // the shape is checked for every T (T == 0 included), as ffn_batch_q4 does
     const size_t need = smoe_ffn_batch_workspace_bytes(T, d_model, d_ff, group);
-    if (T < 0 || need == static_cast<size_t>(-1)) return SMOE_ERR_SHAPE;
+    if (need == static_cast<size_t>(-1)) return SMOE_ERR_SHAPE;
     if (need > SMOE_NOALLOC_SCRATCH_BYTES) return SMOE_ERR_SHAPE;
     if (T == 0 || d_model == 0) return SMOE_OK;
     void *scratch = scratch_device_address();

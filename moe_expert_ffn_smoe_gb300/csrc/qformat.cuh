@@ -6,16 +6,16 @@
 // each 32-bit word the code of the lowest column sits in the lowest bits
 // (Q4: nibble i of the word is column i; Q2: bit pair i is column i).
 //
-// Fold.  With w = (c - Z) s / Z, the dot of one group is
-//     sum w x = s * (C / Z - Sx),   C = sum c x,  Sx = sum x.
-// The kernels never convert a code with an int->float instruction: a code c
-// of b bits is OR-ed into the top mantissa bits of 1.0f, giving the exact
-// float f = 1 + c / 2^b (2^b = 16 for Q4, 4 for Q2).  The inner loop is then
-// a plain FMA chain P = sum f x = Sx + C / 2^b, and per chunk
-//     s * (C / Z - Sx) = s * (A * P - (A + 1) * Sx),   A = 2^b / Z,
-// so each output row keeps two sums, acc1 = sum s*P and acc2 = sum s*Sx,
-// and finishes with A * acc1 - (A + 1) * acc2.  Sx is computed once per
-// chunk of x and shared by every row.
+// Weights.  The kernels never convert a code with an int->float
+// instruction: a code c of b bits is OR-ed into the top mantissa bits of
+// 1.0f, giving the exact float f = 1 + c / 2^b (2^b = 16 for Q4, 4 for Q2),
+// and f - (1 + Z / 2^b) = (c - Z) / 2^b is exact too (both are multiples of
+// 2^-(b+1) within a factor two of each other).  So the inner loop is a plain
+// FMA chain over the exact centred weights, P = sum (c - Z) / 2^b * x, per
+// chunk acc += s * P, and the row finishes with A * acc, A = 2^b / Z:
+//     sum w x = sum s (c - Z) / Z * x = A * sum s * P.
+// No large terms cancel: every product is the weight's own share of the
+// dot, so the f32 rounding is relative to sum |w x|.
 #pragma once
 
 #include <stdint.h>
@@ -32,6 +32,7 @@ struct QFmt<4> {
     static constexpr int F4_PER_CHUNK = 8;       // float4s of x under one chunk
     static constexpr int SWZ = 3;                // log2(F4_PER_CHUNK)
     static constexpr float A = 16.0f / 7.5f;     // 2^b / Z
+    static constexpr float BIAS = 1.46875f;      // 1 + Z / 2^b
 };
 
 template <>
@@ -41,6 +42,7 @@ struct QFmt<2> {
     static constexpr int F4_PER_CHUNK = 16;
     static constexpr int SWZ = 4;
     static constexpr float A = 4.0f / 1.5f;
+    static constexpr float BIAS = 1.375f;
 };
 
 // f = 1 + c / 2^b for the code of column i (0-based) of a 32-bit word.
@@ -60,6 +62,13 @@ __device__ __forceinline__ float code_as_f32(uint32_t w, int i)
     }
 }
 
+// (c - Z) / 2^b for the code of column i of a 32-bit word, exact.
+template <int BITS>
+__device__ __forceinline__ float code_centred(uint32_t w, int i)
+{
+    return code_as_f32<BITS>(w, i) - QFmt<BITS>::BIAS;
+}
+
 __device__ __forceinline__ uint32_t word_of(const uint4 &v, int i)
 {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -77,27 +86,14 @@ __device__ __forceinline__ int x_slot(int q)
 }
 
 // Stages x[0..K) (f32, 16-byte aligned, K a multiple of 4*F4_PER_CHUNK) into
-// shared memory with the swizzle above, and writes the sum of each chunk's
-// x values into sx[K / CODES_PER_CHUNK].  All threads of the block must call
-// it; blockDim.x must be a multiple of 32.
+// shared memory with the swizzle above.  All threads of the block must call
+// it.
 template <int BITS>
-__device__ __forceinline__ void stage_x_chunks(const float *__restrict__ x, int K, float4 *xs,
-                                               float *sx)
+__device__ __forceinline__ void stage_x_chunks(const float *__restrict__ x, int K, float4 *xs)
 {
     using F = QFmt<BITS>;
     const int nq = K >> 2;
-    for (int base = 0; base < nq; base += blockDim.x) {
-        const int q = base + threadIdx.x;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (q < nq) {
-            v = reinterpret_cast<const float4 *>(x)[q];
-            xs[x_slot<F::SWZ>(q)] = v;
-        }
-        float s = (v.x + v.y) + (v.z + v.w);
-#pragma unroll
-        for (int o = 1; o < F::F4_PER_CHUNK; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (q < nq && (q & (F::F4_PER_CHUNK - 1)) == 0) sx[q >> F::SWZ] = s;
-    }
+    for (int q = threadIdx.x; q < nq; q += blockDim.x) xs[x_slot<F::SWZ>(q)] = reinterpret_cast<const float4 *>(x)[q];
 }
 
 }  // namespace smoe

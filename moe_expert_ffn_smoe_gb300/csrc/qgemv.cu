@@ -19,8 +19,7 @@
 //  * one CTA per SM owns a contiguous, balanced range of row tiles; before
 //    waiting on the previous kernel it issues bulk L2 prefetches of its
 //    whole weight range, so HBM traffic starts while x is still unknown;
-//  * x is staged once per CTA in swizzled shared memory together with the
-//    per-chunk sums Sx.
+//  * x is staged once per CTA in swizzled shared memory.
 #include "common.cuh"
 #include "internal.h"
 #include "qformat.cuh"
@@ -55,7 +54,6 @@ __global__ void __launch_bounds__(256) qgemv_fast(QArgs a)
 
     extern __shared__ __align__(16) float4 smem4[];
     float4 *xs = smem4;
-    float *sx = reinterpret_cast<float *>(smem4 + KC * F::F4_PER_CHUNK);
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -84,7 +82,7 @@ __global__ void __launch_bounds__(256) qgemv_fast(QArgs a)
     }
 
     pdl_wait();
-    stage_x_chunks<BITS>(a.x, a.K, xs, sx);
+    stage_x_chunks<BITS>(a.x, a.K, xs);
     __syncthreads();
     pdl_launch_dependents();
 
@@ -118,15 +116,14 @@ __global__ void __launch_bounds__(256) qgemv_fast(QArgs a)
             }
         }
 
-        float acc1[NMAT][RPT], acc2[NMAT][RPT];
+        float acc[NMAT][RPT];
 #pragma unroll
         for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-            for (int r = 0; r < RPT; ++r) acc1[m][r] = acc2[m][r] = 0.f;
+            for (int r = 0; r < RPT; ++r) acc[m][r] = 0.f;
 
 #pragma unroll
         for (int j = 0; j < CPL; ++j) {
-            const float sxc = sx[u + L * j];
             float P[NMAT][RPT];
 #pragma unroll
             for (int m = 0; m < NMAT; ++m)
@@ -151,15 +148,14 @@ __global__ void __launch_bounds__(256) qgemv_fast(QArgs a)
                         const uint32_t w = word_of(cw[m][r][j], wi);
 #pragma unroll
                         for (int i = 0; i < F::CODES_PER_WORD; ++i)
-                            P[m][r] = fmaf(code_as_f32<BITS>(w, i), xv[i], P[m][r]);
+                            P[m][r] = fmaf(code_centred<BITS>(w, i), xv[i], P[m][r]);
                     }
             }
 #pragma unroll
             for (int m = 0; m < NMAT; ++m)
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) {
-                    acc1[m][r] = fmaf(sc[m][r][j], P[m][r], acc1[m][r]);
-                    acc2[m][r] = fmaf(sc[m][r][j], sxc, acc2[m][r]);
+                    acc[m][r] = fmaf(sc[m][r][j], P[m][r], acc[m][r]);
                 }
         }
 
@@ -168,19 +164,16 @@ __global__ void __launch_bounds__(256) qgemv_fast(QArgs a)
 #pragma unroll
             for (int r = 0; r < RPT; ++r)
 #pragma unroll
-                for (int off = L / 2; off > 0; off >>= 1) {
-                    acc1[m][r] += __shfl_xor_sync(FULL_MASK, acc1[m][r], off);
-                    acc2[m][r] += __shfl_xor_sync(FULL_MASK, acc2[m][r], off);
-                }
+                for (int off = L / 2; off > 0; off >>= 1) acc[m][r] += __shfl_xor_sync(FULL_MASK, acc[m][r], off);
 
         if (u == 0) {
 #pragma unroll
             for (int r = 0; r < RPT; ++r) {
                 const int unit = tile * UPT + r * TEAMS + team;
                 if (unit < a.units) {
-                    const float y0 = F::A * acc1[0][r] - (F::A + 1.0f) * acc2[0][r];
+                    const float y0 = F::A * acc[0][r];
                     if (NMAT == 2) {
-                        const float y1 = F::A * acc1[NMAT - 1][r] - (F::A + 1.0f) * acc2[NMAT - 1][r];
+                        const float y1 = F::A * acc[NMAT - 1][r];
                         a.y[unit] = silu_f32(y0) * y1;
                     } else {
                         a.y[unit] = y0;
@@ -200,7 +193,6 @@ __global__ void __launch_bounds__(256) qgemv_generic(QArgs a)
     extern __shared__ __align__(16) float4 smem4[];
     const int KC = a.K / F::CODES_PER_CHUNK;
     float4 *xs = smem4;
-    float *sx = reinterpret_cast<float *>(smem4 + KC * F::F4_PER_CHUNK);
 
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -210,7 +202,7 @@ __global__ void __launch_bounds__(256) qgemv_generic(QArgs a)
     const size_t row_bytes = static_cast<size_t>(KC) * 16;
 
     pdl_wait();
-    stage_x_chunks<BITS>(a.x, a.K, xs, sx);
+    stage_x_chunks<BITS>(a.x, a.K, xs);
     __syncthreads();
     pdl_launch_dependents();
 
@@ -220,9 +212,9 @@ __global__ void __launch_bounds__(256) qgemv_generic(QArgs a)
     for (int m = 0; m < 8; ++m) xo[m] = static_cast<uint32_t>(m ^ (lane & 7)) * 16u;
 
     for (int unit = blockIdx.x * nwarps + warp; unit < a.units; unit += gridDim.x * nwarps) {
-        float acc1[NMAT], acc2[NMAT];
+        float acc[NMAT];
 #pragma unroll
-        for (int m = 0; m < NMAT; ++m) acc1[m] = acc2[m] = 0.f;
+        for (int m = 0; m < NMAT; ++m) acc[m] = 0.f;
         for (int cc = lane; cc < KC; cc += 32) {
             uint4 cw[NMAT];
             float sc[NMAT];
@@ -252,27 +244,20 @@ __global__ void __launch_bounds__(256) qgemv_generic(QArgs a)
                     const uint32_t w = word_of(cw[m], wi);
 #pragma unroll
                     for (int i = 0; i < F::CODES_PER_WORD; ++i)
-                        P[m] = fmaf(code_as_f32<BITS>(w, i), xv[i], P[m]);
+                        P[m] = fmaf(code_centred<BITS>(w, i), xv[i], P[m]);
                 }
             }
-            const float sxc = sx[cc];
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m) {
-                acc1[m] = fmaf(sc[m], P[m], acc1[m]);
-                acc2[m] = fmaf(sc[m], sxc, acc2[m]);
-            }
+            for (int m = 0; m < NMAT; ++m) acc[m] = fmaf(sc[m], P[m], acc[m]);
         }
 #pragma unroll
         for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                acc1[m] += __shfl_xor_sync(FULL_MASK, acc1[m], off);
-                acc2[m] += __shfl_xor_sync(FULL_MASK, acc2[m], off);
-            }
+            for (int off = 16; off > 0; off >>= 1) acc[m] += __shfl_xor_sync(FULL_MASK, acc[m], off);
         if (lane == 0) {
-            const float y0 = F::A * acc1[0] - (F::A + 1.0f) * acc2[0];
+            const float y0 = F::A * acc[0];
             if (NMAT == 2) {
-                const float y1 = F::A * acc1[NMAT - 1] - (F::A + 1.0f) * acc2[NMAT - 1];
+                const float y1 = F::A * acc[NMAT - 1];
                 a.y[unit] = silu_f32(y0) * y1;
             } else {
                 a.y[unit] = y0;
@@ -322,7 +307,7 @@ cudaError_t launch_q(const QArgs &base, cudaStream_t stream)
     if (!dev) return cudaErrorInvalidDevice;
     QArgs a = base;
     const int KC = a.K / F::CODES_PER_CHUNK;
-    const size_t smem = (static_cast<size_t>(a.K) + KC) * sizeof(float);
+    const size_t smem = static_cast<size_t>(a.K) * sizeof(float);
     constexpr int RPT = 1;
 
     for (const FastPick &p : kFastPicks) {

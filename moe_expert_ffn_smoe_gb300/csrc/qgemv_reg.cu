@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(H == 1 ? 384 : 512, 1) qgemv_reg(const __grid_
     if (first > 0) issue(0, 0);
 
     pdl_wait();
-    stage_x_digits<BITS>(a.x[e], a.K, a.group, smem, a.off_info, a.off_gmax);
+    stage_x_digits<BITS>(a.x[e], a.K, a.group, smem, a.off_info);
     __syncthreads();
     if (threadIdx.x == 0) pdl_launch_dependents();
     for (int k = 1; k < first; ++k) issue(k, k);

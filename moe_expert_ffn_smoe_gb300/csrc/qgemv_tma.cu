@@ -23,19 +23,28 @@
 //  * x is staged once per CTA, converted to exact integer "digits" (below).
 //
 // Arithmetic (an exact integer rewrite of the inner dot):
-//  * Per group of `group` columns, x is scaled by a power of two so its
-//    largest magnitude lies in [2^21, 2^22) and rounded to an integer
-//    xq (|x - xq*q| <= q/2 with q = 2^(e-21), e = floor(log2 max|x|)).
+//  * Per 16-byte chunk of codes (32 Q4 or 64 Q2 columns, never more than
+//    one group), x is scaled by a power of two 1/q so that its largest
+//    magnitude lies in [2^22, 2^23) (one step lower if it would round above
+//    XQ_MAX = 8355711) and rounded to an integer xq: |x - xq*q| <= q/2,
+//    q <= max|x| / 4177856.
 //  * xq is split into three balanced base-256 digits d0 + 256 d1 + 65536 d2,
-//    each a signed byte, so sum(code * xq) over a 16-byte chunk of codes is
-//    computed exactly by dp4a (four byte products + add per instruction);
-//    codes are separated into bytes with one or two logic ops per 32-bit
-//    word (Q4: even / odd nibbles; Q2: the four bit pairs).
-//  * Per chunk: C = A2*65536 + A1*256 + A0 (exact in int32), then
-//    acc1 += s*q*C and acc2 += s*(q*Sxq); the row result is acc1/Z - acc2,
-//    with Sxq the exact integer sum of xq over the chunk.
-// Error: only the rounding of x to xq (at most 2^-22 of the group's largest
-// |x| per element) and the f32 epilogue; far inside 1e-4 * sum|w x|.
+//    each a signed byte, so sum(code * xq) over a chunk is computed exactly
+//    by dp4a (four byte products + add per instruction); codes are
+//    separated into bytes with one or two logic ops per 32-bit word (Q4:
+//    even nibbles, odd nibbles shifted down; Q2: the four bit pairs), every
+//    class on the same grid.
+//  * The chunk's dot is taken on the codes minus OFF (8 for Q4, 2 for Q2):
+//    C' = sum (code - OFF) xq fits in int32 (|C'| <= 8 * 32 * XQ_MAX), so
+//    the modulo-2^32 sums of the digit planes give it exactly.  The chunk
+//    adds s * (q/Z * C' + q * Sxq * (OFF - Z)/Z) to the row, which equals
+//    s * q * (C/Z - Sxq), the page's fold, with no cancellation between
+//    large terms.
+// Error: only the rounding of x to xq and the f32 epilogue.  For a chunk
+// whose largest |x| = X sits on a weight of magnitude >= s/15 (Q4; s/3 for
+// Q2), the rounding error is at most 32 * s * q / 2 <= s X * 3.83e-6 (Q2:
+// 64 codes, s X * 7.7e-6), i.e. at most 5.8e-5 (Q2: 2.3e-5) of the
+// chunk's sum |w x|; the epilogue adds a few units of 2^-24 of it.
 // Non-finite x makes the chunk's q NaN, so the affected outputs are NaN.
 #include "qgemv_tma.cuh"
 
@@ -107,7 +116,7 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
     __syncwarp();
 
     pdl_wait();
-    stage_x_digits<BITS>(a.x[e], a.K, a.group, smem, a.off_info, a.off_gmax);
+    stage_x_digits<BITS>(a.x[e], a.K, a.group, smem, a.off_info);
     __syncthreads();
     if (threadIdx.x == 0) pdl_launch_dependents();
     if (lane == 0)
@@ -127,11 +136,11 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
         const int us = u0 + (warp + k * NW) * R;
         const int n = min(R, u1 - us);
 
-        float acc1[NMAT][RPT], acc2[NMAT][RPT];
+        float acc[NMAT][RPT];
 #pragma unroll
         for (int m = 0; m < NMAT; ++m)
 #pragma unroll
-            for (int r = 0; r < RPT; ++r) acc1[m][r] = acc2[m][r] = 0.f;
+            for (int r = 0; r < RPT; ++r) acc[m][r] = 0.f;
 
         const uint32_t code0 = slot + static_cast<uint32_t>(team) * row_bytes + static_cast<uint32_t>(u) * 16u;
 #pragma unroll 2
@@ -139,47 +148,22 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
             const uint32_t coff = static_cast<uint32_t>(c - u) * 16u;
             const float4 inf = lds128f(info0 + static_cast<uint32_t>(c) * 16u);
             const int g = __float_as_int(inf.z);
+            const float qz = inf.x * D::ZINV;
             const uint32_t xc = sbase + static_cast<uint32_t>(c) * D::XSTRIDE;
-            uint4 cw[NMAT][RPT];
+            uint4 dg[3 * D::NCLASS];
 #pragma unroll
-            for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-                for (int r = 0; r < RPT; ++r)
-                    cw[m][r] = lds128u(code0 + static_cast<uint32_t>(m * R + r * TEAMS) * row_bytes + coff);
-            int A0[NMAT][RPT], A1[NMAT][RPT], A2[NMAT][RPT];
-#pragma unroll
-            for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-                for (int r = 0; r < RPT; ++r) A0[m][r] = A1[m][r] = A2[m][r] = 0;
-#pragma unroll
-            for (int cl = 0; cl < D::NCLASS; ++cl) {
-                const uint4 d0 = lds128u(xc + (3 * cl + 0) * 16);
-                const uint4 d1 = lds128u(xc + (3 * cl + 1) * 16);
-                const uint4 d2 = lds128u(xc + (3 * cl + 2) * 16);
-#pragma unroll
-                for (int m = 0; m < NMAT; ++m)
-#pragma unroll
-                    for (int r = 0; r < RPT; ++r)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const uint32_t cb = D::cls(word_of(cw[m][r], v), cl);
-                            A0[m][r] = dp4a_us(cb, word_of(d0, v), A0[m][r]);
-                            A1[m][r] = dp4a_us(cb, word_of(d1, v), A1[m][r]);
-                            A2[m][r] = dp4a_us(cb, word_of(d2, v), A2[m][r]);
-                        }
-            }
+            for (int t = 0; t < 3 * D::NCLASS; ++t) dg[t] = lds128u(xc + static_cast<uint32_t>(t) * 16u);
 #pragma unroll
             for (int m = 0; m < NMAT; ++m)
 #pragma unroll
                 for (int r = 0; r < RPT; ++r) {
                     const int ul = r * TEAMS + team;
+                    const uint4 cw = lds128u(code0 + static_cast<uint32_t>(m * R + r * TEAMS) * row_bytes + coff);
+                    const int C = chunk_dot<BITS>(cw, dg, __float_as_int(inf.w));  // sum (code - OFF) * xq
                     const float sc =
                         a.scales_tma ? lds_f32(slot + scales_off + static_cast<uint32_t>((m * R + ul) * ngroups + g) * 4u)
                                      : ldg_f32(a.scales[m][e] + static_cast<size_t>(min(us + ul, u1 - 1)) * ngroups + g);
-                    // |C| < 2^31: at most 32 codes x 15 x 2^22 (Q4), 64 x 3 x 2^22 (Q2)
-                    const int C = A2[m][r] * 65536 + A1[m][r] * 256 + A0[m][r];
-                    acc1[m][r] = fmaf(sc * inf.x, static_cast<float>(C), acc1[m][r]);
-                    acc2[m][r] = fmaf(sc, inf.y, acc2[m][r]);
+                    acc[m][r] = fmaf(sc, fmaf(static_cast<float>(C), qz, inf.y), acc[m][r]);
                 }
         }
 #pragma unroll
@@ -187,10 +171,7 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
 #pragma unroll
             for (int r = 0; r < RPT; ++r)
 #pragma unroll
-                for (int off = L / 2; off > 0; off >>= 1) {
-                    acc1[m][r] += __shfl_xor_sync(FULL_MASK, acc1[m][r], off);
-                    acc2[m][r] += __shfl_xor_sync(FULL_MASK, acc2[m][r], off);
-                }
+                for (int off = L / 2; off > 0; off >>= 1) acc[m][r] += __shfl_xor_sync(FULL_MASK, acc[m][r], off);
         __syncwarp();
         if (lane == 0 && k + ns < my) {
             fence_proxy_async_smem();
@@ -201,9 +182,8 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
             for (int r = 0; r < RPT; ++r) {
                 const int ul = r * TEAMS + team;
                 if (ul < n) {
-                    const float y0 = acc1[0][r] * D::ZINV - acc2[0][r];
-                    float out = y0;
-                    if (NMAT == 2) out = silu_f32(y0) * (acc1[NMAT - 1][r] * D::ZINV - acc2[NMAT - 1][r]);
+                    float out = acc[0][r];
+                    if (NMAT == 2) out = silu_f32(acc[0][r]) * acc[NMAT - 1][r];
                     a.y[e][us + ul] = out;
                 }
             }
@@ -320,8 +300,7 @@ cudaError_t launch_tma(QGArgs &a, int n_experts, cudaStream_t stream, bool *unsu
     a.ctas_per_expert = cpe;
     const int max_units = (a.units + cpe - 1) / cpe;
     a.off_info = static_cast<uint32_t>(KC) * D::XSTRIDE;
-    a.off_gmax = a.off_info + static_cast<uint32_t>(KC) * 16u;
-    a.off_bars = a.off_gmax + round16(static_cast<uint32_t>(ngroups) * 4u);
+    a.off_bars = a.off_info + static_cast<uint32_t>(KC) * 16u;
     TmaConfig cfg;
     size_t smem = 0;
     // Row split (gate/up over few rows per CTA): each lane holds the digits

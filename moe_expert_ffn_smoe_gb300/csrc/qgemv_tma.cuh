@@ -25,13 +25,20 @@ struct QGArgs {
     int scales_tma;        // scales travel with the codes (ngroups % 4 == 0)
     int ns;                // ring slots per warp
     uint32_t stage_bytes;  // bytes of one slot
-    uint32_t off_info, off_gmax, off_bars, off_slots;  // shared-memory offsets
+    uint32_t off_info, off_bars, off_slots;  // shared-memory offsets
     uint32_t off_part;     // row-split kernel: partial row sums
 };
 
 template <int BITS>
 struct DigitFmt;
 
+// Per format: the byte classes of a code word, the digit layout of a chunk,
+// and the centring of the integer dot.  A chunk's integer dot is taken on
+// the codes minus OFF (the integer nearest above Z), which keeps it inside
+// int32 for every legal x: sum (c - OFF) xq = C - OFF * Sxq.  The chunk's
+// contribution to the row is then
+//     s q (C / Z - Sxq) = s (q / Z * (C - OFF Sxq) + q Sxq (OFF - Z) / Z),
+// so FOLD = (OFF - Z) / Z multiplies q * Sxq.
 template <>
 struct DigitFmt<4> {
     static constexpr int NCLASS = 2;     // byte classes per code word
@@ -39,15 +46,15 @@ struct DigitFmt<4> {
     static constexpr int CODES_PER_CHUNK = 32;
     static constexpr int WORD_COLS = 8;
     static constexpr float ZINV = 1.0f / 7.5f;
-    // class 0: codes of the even columns, class 1: 16 x the codes of the odd
-    // columns (the high nibbles, masked in place), one per byte.  The digits
-    // of class k are those of x scaled by 2^-SHIFT(k), so the byte products
-    // carry the same weight in both classes.
+    static constexpr int OFF = 8;
+    static constexpr float FOLD = 1.0f / 15.0f;  // (8 - 7.5) / 7.5
+    // class 0: the codes of the even columns (low nibbles), class 1: the
+    // codes of the odd columns (high nibbles moved down), one per byte, so
+    // both classes pair with digits of x on the same grid.
     static __device__ __forceinline__ uint32_t cls(uint32_t w, int k)
     {
-        return w & (k == 0 ? 0x0F0F0F0Fu : 0xF0F0F0F0u);
+        return (k == 0 ? w : (w >> 4)) & 0x0F0F0F0Fu;
     }
-    static constexpr int SHIFT(int k) { return 4 * k; }
     // column (0..7 inside the word) whose digit goes to byte b of class k
     static __device__ __forceinline__ int col(int k, int b) { return 2 * b + k; }
 };
@@ -59,11 +66,12 @@ struct DigitFmt<2> {
     static constexpr int CODES_PER_CHUNK = 64;
     static constexpr int WORD_COLS = 16;
     static constexpr float ZINV = 1.0f / 1.5f;
+    static constexpr int OFF = 2;
+    static constexpr float FOLD = 1.0f / 3.0f;  // (2 - 1.5) / 1.5
     static __device__ __forceinline__ uint32_t cls(uint32_t w, int k)
     {
         return (w >> (2 * k)) & 0x03030303u;
     }
-    static constexpr int SHIFT(int) { return 0; }
     static __device__ __forceinline__ int col(int k, int b) { return 4 * b + k; }
 };
 
@@ -97,7 +105,7 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c)
     return d;
 }
 
-// Balanced base-256 digits of v (|v| <= 2^22): v = d0 + 256 d1 + 65536 d2,
+// Balanced base-256 digits of v (|v| <= XQ_MAX): v = d0 + 256 d1 + 65536 d2,
 // every digit in [-128, 127].
 __device__ __forceinline__ void digits3(int v, int &d0, int &d1, int &d2)
 {
@@ -107,46 +115,61 @@ __device__ __forceinline__ void digits3(int v, int &d0, int &d1, int &d2)
     d2 = (r - d1) >> 8;
 }
 
+// Largest magnitude three balanced base-256 digits hold: 127 * (1 + 256 + 65536).
+constexpr int XQ_MAX = 8355711;
+
 __device__ __forceinline__ uint32_t pack4(int a, int b, int c, int d)
 {
     return (static_cast<uint32_t>(a) & 0xFFu) | ((static_cast<uint32_t>(b) & 0xFFu) << 8) |
            ((static_cast<uint32_t>(c) & 0xFFu) << 16) | ((static_cast<uint32_t>(d) & 0xFFu) << 24);
 }
 
+// c + the exact integer dot of one 16-byte chunk of codes (row word v in
+// component v of cw) with the digits dg[3 * NCLASS] of its x, returned as
+// sum over classes and planes of 256^j * dp4a(class, digit plane j),
+// i.e. c + sum code * xq, in arithmetic modulo 2^32.  Starting from
+// c = -OFF * Sxq, the result is the chunk's sum (code - OFF) * xq, which
+// fits in int32, so the wrap-around of the intermediate sums is harmless.
+template <int BITS>
+__device__ __forceinline__ int chunk_dot(const uint4 &cw, const uint4 *dg, int c)
+{
+    using D = DigitFmt<BITS>;
+    int A0 = c, A1 = 0, A2 = 0;
+#pragma unroll
+    for (int cl = 0; cl < D::NCLASS; ++cl)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+            const uint32_t cb = D::cls(word_of(cw, v), cl);
+            A0 = dp4a_us(cb, word_of(dg[3 * cl + 0], v), A0);
+            A1 = dp4a_us(cb, word_of(dg[3 * cl + 1], v), A1);
+            A2 = dp4a_us(cb, word_of(dg[3 * cl + 2], v), A2);
+        }
+    const uint32_t C = static_cast<uint32_t>(A2) * 65536u + static_cast<uint32_t>(A1) * 256u + static_cast<uint32_t>(A0);
+    return static_cast<int>(C);
+}
+
 // Stages x[0..K) as digits: chunk c occupies XSTRIDE bytes at c*XSTRIDE;
 // inside it, the uint4 at (3k + j)*16 holds digit j of byte class k for the
-// chunk's 4 code words (word v in component v).  info[c] = {q, q*Sxq, group
-// index, 0}.  Called by all threads of the block (blockDim.x % 32 == 0); the
-// caller synchronises the block before reading the result.
-// Thread t of each pass handles word t of x.  When a group spans a power of
-// two of at most 32 words, its words lie in consecutive lanes of one warp and
-// the group maximum is a shuffle reduction over values already in registers
-// (one read of x, no block barrier); otherwise a first pass gathers the group
-// maxima in shared memory with atomics.
+// chunk's 4 code words (word v in component v).  info[c] = {q, q * Sxq *
+// FOLD, group index, -OFF * Sxq (int bits)}.  Called by all threads of the
+// block (blockDim.x % 32 == 0); the caller synchronises the block before
+// reading the result.
+//
+// Rounding grid.  Each 16-byte chunk of codes (32 Q4 or 64 Q2 columns) has
+// its own power-of-two step q, the smallest for which the chunk's largest
+// |x| rounds to at most XQ_MAX steps: that largest |x| is then at least
+// 4177856 q, and every x of the chunk is xq * q + r with |r| <= q / 2.
+// Thread t of each pass handles word t of x, so a chunk's four words are
+// four consecutive lanes and its maximum is two shuffles.
 // COHERENT: x was written by other CTAs of the running grid (read through L2
 // only, never through the read-only path).
 template <int BITS, bool COHERENT = false>
-__device__ void stage_x_digits(const float *__restrict__ x, int K, int group, uint8_t *smem, uint32_t off_info,
-                               uint32_t off_gmax)
+__device__ void stage_x_digits(const float *__restrict__ x, int K, int group, uint8_t *smem, uint32_t off_info)
 {
     using D = DigitFmt<BITS>;
-    const int nwords = K / D::WORD_COLS;
-    const int gw = group / D::WORD_COLS;  // words per group
-    const bool in_warp = gw <= 32 && (gw & (gw - 1)) == 0;
-    unsigned *gmax = reinterpret_cast<unsigned *>(smem + off_gmax);
+    const int nwords = K / D::WORD_COLS;  // a multiple of 4: K is a multiple of the chunk
     float4 *info = reinterpret_cast<float4 *>(smem + off_info);
 
-    // largest |x| of a word, +inf when any entry is not finite
-    auto word_max = [](const float (&f)[D::WORD_COLS]) {
-        float m = 0.f;
-        bool finite = true;
-#pragma unroll
-        for (int i = 0; i < D::WORD_COLS; ++i) {
-            m = fmaxf(m, fabsf(f[i]));
-            finite = finite && isfinite(f[i]);
-        }
-        return finite ? m : __uint_as_float(0x7F800000u);
-    };
     auto load_word = [&](int v, float (&f)[D::WORD_COLS]) {
         const float4 *p = reinterpret_cast<const float4 *>(x + static_cast<size_t>(v) * D::WORD_COLS);
 #pragma unroll
@@ -159,17 +182,6 @@ __device__ void stage_x_digits(const float *__restrict__ x, int K, int group, ui
         }
     };
 
-    if (!in_warp) {
-        const int ngroups = K / group;
-        for (int g = threadIdx.x; g < ngroups; g += blockDim.x) gmax[g] = 0u;
-        __syncthreads();
-        for (int v = threadIdx.x; v < nwords; v += blockDim.x) {
-            float f[D::WORD_COLS];
-            load_word(v, f);
-            atomicMax(&gmax[(v * D::WORD_COLS) / group], __float_as_uint(word_max(f)));
-        }
-        __syncthreads();
-    }
     for (int base = 0; base < nwords; base += blockDim.x) {
         const int v = base + threadIdx.x;
         const bool valid = v < nwords;
@@ -180,38 +192,42 @@ __device__ void stage_x_digits(const float *__restrict__ x, int K, int group, ui
 #pragma unroll
             for (int i = 0; i < D::WORD_COLS; ++i) f[i] = 0.f;
         }
-        const int g = valid ? (v * D::WORD_COLS) / group : 0;
-        unsigned mb;
-        if (in_warp) {
-            // a group's gw words are gw consecutive lanes (base is a
-            // multiple of 32 and groups are aligned to gw words)
-            float m = word_max(f);
-            for (int off = 1; off < gw; off <<= 1) m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, off));
-            mb = __float_as_uint(m);
-        } else {
-            mb = valid ? gmax[g] : 0u;
+        // largest |x| of the chunk, +inf when any entry is not finite
+        float m = 0.f;
+        bool finite = true;
+#pragma unroll
+        for (int i = 0; i < D::WORD_COLS; ++i) {
+            m = fmaxf(m, fabsf(f[i]));
+            finite = finite && isfinite(f[i]);
         }
+        if (!finite) m = __uint_as_float(0x7F800000u);
+        m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(FULL_MASK, m, 2));
+        const unsigned mb = __float_as_uint(m);
+        const int g = valid ? (v * D::WORD_COLS) / group : 0;
         int S = 0;
         float q = 1.f;
         if (valid) {
+            // e = floor(log2 max|x|), at least -104 so that q stays a normal float
             int e = static_cast<int>(mb >> 23) - 127;
-            if (e < -105) e = -105;
-            const bool finite = mb < 0x7F800000u;
-            const float scale = finite ? __uint_as_float(static_cast<unsigned>(127 + 21 - e) << 23) : 0.f;
-            q = finite ? __uint_as_float(static_cast<unsigned>(127 + e - 21) << 23) : __uint_as_float(0x7FC00000u);
-            // column i of the word is in byte class i % NCLASS; class k is
-            // rounded at 2^SHIFT(k) times the step q
+            if (e < -104) e = -104;
+            const bool fin = mb < 0x7F800000u;
+            // scale = 1 / q = 2^(22 - e) puts max|x| in [2^22, 2^23); one
+            // step coarser when it would round above XQ_MAX
+            float scale = __uint_as_float(static_cast<unsigned>(127 + 22 - e) << 23);
+            if (m * scale > static_cast<float>(XQ_MAX)) {
+                scale *= 0.5f;
+                ++e;
+            }
+            q = fin ? __uint_as_float(static_cast<unsigned>(127 + e - 22) << 23) : __uint_as_float(0x7FC00000u);
             int xq[D::WORD_COLS];
 #pragma unroll
-            for (int i = 0; i < D::WORD_COLS; ++i) {
-                const float sk = scale * __uint_as_float(static_cast<unsigned>(127 - D::SHIFT(i % D::NCLASS)) << 23);
-                xq[i] = finite ? __float2int_rn(f[i] * sk) : 0;
-            }
+            for (int i = 0; i < D::WORD_COLS; ++i) xq[i] = fin ? __float2int_rn(f[i] * scale) : 0;
             int d[3][D::WORD_COLS];
 #pragma unroll
             for (int i = 0; i < D::WORD_COLS; ++i) {
                 digits3(xq[i], d[0][i], d[1][i], d[2][i]);
-                S += xq[i] * (1 << D::SHIFT(i % D::NCLASS));
+                S += xq[i];
             }
             uint8_t *chunk = smem + static_cast<size_t>(v >> 2) * D::XSTRIDE + (v & 3) * 4;
 #pragma unroll
@@ -223,7 +239,11 @@ __device__ void stage_x_digits(const float *__restrict__ x, int K, int group, ui
         }
         S += __shfl_xor_sync(FULL_MASK, S, 1);
         S += __shfl_xor_sync(FULL_MASK, S, 2);
-        if (valid && (v & 3) == 0) info[v >> 2] = make_float4(q, static_cast<float>(S) * q, __int_as_float(g), 0.f);
+        if (valid && (v & 3) == 0) {
+            // |S| <= 64 XQ_MAX, so OFF * S fits in int32
+            const int negoff = static_cast<int>(0u - static_cast<uint32_t>(D::OFF) * static_cast<uint32_t>(S));
+            info[v >> 2] = make_float4(q, static_cast<float>(S) * q * D::FOLD, __int_as_float(g), __int_as_float(negoff));
+        }
     }
 }
 

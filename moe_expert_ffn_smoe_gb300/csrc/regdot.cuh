@@ -29,9 +29,10 @@ struct RegDot {
 
     uint4 dg[CPL][ND];
     float qz[CPL], qs[CPL];
+    int c0[CPL];
     uint32_t soff[CPL];
 
-    // Lane u's digits, q / Z, q * Sxq and scale byte offsets from x staged at
+    // Lane u's digits, q / Z, q * Sxq * FOLD, -OFF * Sxq and scale byte offsets from x staged at
     // sbase (digits) and sbase + off_info (chunk info).  The rows streamed
     // may be a part of x's length: chunks chunk0 .. chunk0 + KC - 1 of x,
     // whose scales start at group `group0` of the full row.
@@ -46,6 +47,7 @@ struct RegDot {
             const float4 inf = lds128f(sbase + off_info + static_cast<uint32_t>(c) * 16u);
             qz[j] = inf.x * D::ZINV;
             qs[j] = inf.y;
+            c0[j] = __float_as_int(inf.w);
             soff[j] = static_cast<uint32_t>(__float_as_int(inf.z) - group0) * 4u;
         }
     }
@@ -71,21 +73,10 @@ struct RegDot {
                     // row m R + r TEAMS + team, chunk u + j L
                     const uint4 cw = lds128u(code_lane + static_cast<uint32_t>((m * R + r * TEAMS) * ROW_BYTES +
                                                                                j * L * 16));
-                    int A0 = 0, A1 = 0, A2 = 0;
-#pragma unroll
-                    for (int cl = 0; cl < D::NCLASS; ++cl)
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const uint32_t cb = D::cls(word_of(cw, v), cl);
-                            A0 = dp4a_us(cb, word_of(dg[j][3 * cl + 0], v), A0);
-                            A1 = dp4a_us(cb, word_of(dg[j][3 * cl + 1], v), A1);
-                            A2 = dp4a_us(cb, word_of(dg[j][3 * cl + 2], v), A2);
-                        }
-                    // |C| < 2^31: at most 32 codes x 15 x 2^22 (Q4), 64 x 3 x 2^22 (Q2)
-                    const int C = A2 * 65536 + A1 * 256 + A0;
+                    const int C = chunk_dot<BITS>(cw, dg[j], c0[j]);  // sum (code - OFF) * xq
                     const float sc =
                         lds_f32(scale_lane + static_cast<uint32_t>(m * R + r * TEAMS) * sbytes_row + soff[j]);
-                    acc[m][r] = fmaf(sc, fmaf(static_cast<float>(C), qz[j], -qs[j]), acc[m][r]);
+                    acc[m][r] = fmaf(sc, fmaf(static_cast<float>(C), qz[j], qs[j]), acc[m][r]);
                 }
         }
 #pragma unroll

@@ -35,5 +35,6 @@ def check(got, ref, absdot, what, eps=EPS, floor=FLOOR):
 
 def hidden_bound_absdot(r):
     """The first-order absdot of hidden for oracle.gate_up() output r."""
-    silu_g = r["g"] / (1.0 + np.exp(-r["g"]))
+    with np.errstate(over="ignore"):  # exp(-g) = inf for g << 0 gives SiLU(g) = -0, as it should
+        silu_g = r["g"] / (1.0 + np.exp(-r["g"]))
     return 1.1 * np.abs(r["u"]) * r["g_abs"] + np.abs(silu_g) * r["u_abs"]

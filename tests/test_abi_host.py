@@ -316,3 +316,7 @@ def test_noalloc_refusals_before_any_launch(smoe):
     assert L.ffn_batch_q4_noalloc(*ptrs, big, 4096, 1536, 64, None) == smoe.SMOE_ERR_SHAPE
     assert L.ffn_batch_q4_noalloc(*ptrs, -1, 4096, 1536, 64, None) == smoe.SMOE_ERR_SHAPE
     assert L.ffn_batch_q4_noalloc(*ptrs, 0, 4096, 1536, 64, None) == smoe.SMOE_OK
+    # the shape is checked before the empty batch returns, as in ffn_batch_q4
+    assert L.ffn_batch_q4_noalloc(*ptrs, 0, 4096, 1536, 48, None) == smoe.SMOE_ERR_SHAPE
+    assert L.ffn_batch_q4(*ptrs[:8], 0, 4096, 1536, 48, None, 0, None) == smoe.SMOE_ERR_SHAPE
+    assert L.smoe_ffn_batch_workspace_bytes(0, 4096, 1536, 48) == ctypes.c_size_t(-1).value
