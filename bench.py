@@ -555,6 +555,8 @@ def rows_breakdown(smoe, dev, steps, pattern=""):
         experts_batch_row(smoe, dev, steps, out, hbm_peak, timed, s)
     if pattern in "route_128x4096_top8":
         route_row(smoe, dev, steps, out, timed, s)
+    if pattern in "moe_layer_routed_128e_top8":
+        routed_layer_row(smoe, dev, steps, out, s)
     if pattern in "q4_ffn_256":
         small_row(smoe, dev, steps, out, timed, s)
     return out
@@ -568,7 +570,8 @@ def q2_row(smoe, dev, steps, out, hbm_peak):
     q2.capture()
     q2.run(5)
     n = max(50, steps // 4)
-    t = time_steps(lambda k: q2.run(k), n, q2.stream)
+    nc = len(q2.copies)
+    t = time_steps(lambda k: q2.run(k), n, q2.stream, hold=n // nc + n % nc)
     sb = step_bytes(2)
     # each grouped kernel alone, in a chain of launches on rotating copies
     nc = len(q2.copies)
@@ -720,6 +723,83 @@ def route_row(smoe, dev, steps, out, timed, s, n=128, d=D_MODEL, k=N_EXPERTS):
                                     "us_per_logits_matvec": round(t_l / nl * 1e6, 3),
                                     "us_per_combine": round(t_c / nl * 1e6, 3)}
     del gs
+    torch.cuda.empty_cache()
+
+
+def routed_layer_row(smoe, dev, steps, out, s, n=128, k=N_EXPERTS, ntok=16):
+    """A whole MoE layer per token with the selection on the device: router
+    (bf16 gate n x 4096, top-k), the routed FFN of the k selected Q4 experts
+    (smoe_experts_ffn_routed_q4 out of device pointer tables), combine.  One
+    CUDA graph holds the layers of ntok different tokens back to back; the
+    device time per layer is timed with the stream held.  End to end: the
+    token copied in from pinned host memory and the layer output copied back
+    (smoe_copy), one graph replay per token, host submission included."""
+    import torch
+    keys = ("gate_codes", "gate_scales", "up_codes", "up_scales", "down_codes", "down_scales")
+    ex = [{kk: torch.from_numpy(v).to(dev) for kk, v in inp.expert(4, D_MODEL, D_FF, GROUP, 12, e).items()}
+          for e in range(n)]
+    tabs = [smoe.pointer_table([t[kk] for t in ex], dev) for kk in keys]
+    gate = torch.from_numpy(inp.bf16_rows(n, D_MODEL, 12, 1).view(np.int16)).to(dev)
+    X = torch.from_numpy(inp.activations((ntok, D_MODEL), 12)).to(dev)
+    logits = torch.empty(n, device=dev)
+    idx = torch.empty(k, dtype=torch.int32, device=dev)
+    w = torch.empty(k, device=dev)
+    wsb = smoe.smoe_experts_ffn_routed_workspace_bytes(k, D_FF)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    eo = torch.empty((k, D_MODEL), device=dev)
+    y = torch.empty(D_MODEL, device=dev)
+
+    def layer(x):
+        smoe.smoe_route_topk_bf16(gate, x, n, D_MODEL, k, logits, idx, w, stream=s)
+        smoe.smoe_experts_ffn_routed_q4(n, k, *tabs, idx, x, eo, D_MODEL, D_FF, GROUP, ws, wsb, stream=s)
+        smoe.smoe_combine(k, eo, w, y, D_MODEL, stream=s)
+
+    with torch.cuda.stream(s):
+        for i in range(ntok):
+            layer(X[i])
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for i in range(ntok):
+            layer(X[i])
+    reps = max(4, min(steps // ntok, 200))
+    with torch.cuda.stream(s):
+        g.replay()
+        t = time_steps(lambda r: [g.replay() for _ in range(r)], reps, s, hold=reps * ntok)
+    per = t / (reps * ntok)
+    layer_bytes = n * D_MODEL * 2 + D_MODEL * 4 + k * expert_bytes(4, D_MODEL, D_FF, GROUP) + k * D_MODEL * 4 \
+        + D_MODEL * 4
+    # end to end: token in from pinned host memory, output back to it
+    x_host = torch.from_numpy(inp.activations(D_MODEL, 13)).pin_memory()
+    y_host = torch.empty(D_MODEL).pin_memory()
+    xd = torch.empty(D_MODEL, device=dev)
+
+    def e2e_body():
+        smoe.smoe_copy(xd, x_host, D_MODEL * 4, stream=s)
+        layer(xd)
+        smoe.smoe_copy(y_host, y, D_MODEL * 4, stream=s)
+
+    with torch.cuda.stream(s):
+        e2e_body()
+    s.synchronize()
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge, stream=s, capture_error_mode="thread_local"):
+        e2e_body()
+    ne = max(20, min(steps, 500))
+    with torch.cuda.stream(s):
+        ge.replay()
+        te = time_steps(lambda r: [ge.replay() for _ in range(r)], ne, s)
+    torch.cuda.synchronize()
+    if not torch.equal(y_host, y.cpu()):
+        raise RuntimeError("routed layer: the output copied to host memory differs from the device's")
+    out[f"moe_layer_routed_{n}e_top{k}"] = {
+        "us_per_layer": round(per * 1e6, 3), "GB/s": round(layer_bytes / per / 1e9, 1),
+        "bytes_per_layer": layer_bytes, "launches_per_layer": 6,
+        "e2e": {"us_per_layer": round(te / ne * 1e6, 3), "h2d_bytes": D_MODEL * 4, "d2h_bytes": D_MODEL * 4,
+                "launch": "one graph replay per token: smoe_copy in, route, routed FFN, combine, smoe_copy out"},
+        "how": f"{ntok} layers on {ntok} tokens in one CUDA graph, {reps} replays, stream held; "
+               f"{n} experts x {D_FF}x{D_MODEL} Q4 resident ({n * expert_bytes(4, D_MODEL, D_FF, GROUP) / 1e9:.2f} GB)"}
+    del ex, tabs
     torch.cuda.empty_cache()
 
 

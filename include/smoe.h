@@ -76,7 +76,7 @@
 extern "C" {
 #endif
 
-#define SMOE_ABI_VERSION 1
+#define SMOE_ABI_VERSION 2
 
 /* Largest `cols` (input length) any call accepts: the input vector of a
  * call is staged whole in one SM's shared memory (f32). */
@@ -91,7 +91,9 @@ typedef enum smoe_status {
     SMOE_ERR_LAUNCH = 5,    /* CUDA refused a launch or a device query          */
     SMOE_ERR_TIMEOUT = 6,   /* a device-side bounded wait gave up               */
     SMOE_ERR_ALIAS = 7,     /* an output overlaps an input or another output    */
-    SMOE_ERR_MEMORY = 8     /* a buffer is not accessible from the device       */
+    SMOE_ERR_MEMORY = 8,    /* a buffer is not accessible from the device       */
+    SMOE_ERR_ROUTE = 9      /* a device-side expert index or table entry was
+                               invalid (reported by smoe_last_device_status)  */
 } smoe_status;
 
 /* ABI version (SMOE_ABI_VERSION of the built library). */
@@ -406,6 +408,75 @@ int smoe_route_topk_bf16(const uint16_t *gate_w, const float *x, int n_experts,
 int smoe_combine(int k, const float *expert_out, const float *top_w,
                  float *out, int d_model, void *stream);
 
+/* Most selected experts one routed call serves. */
+#define SMOE_MAX_ROUTED_SLOTS 64
+
+/*
+ * Bytes of device workspace smoe_experts_ffn_routed_q4/q2 need: the hidden
+ * activations [k x d_ff] f32, rounded up to 256.  (size_t)-1 for k < 0,
+ * k > SMOE_MAX_ROUTED_SLOTS or d_ff < 0.
+ */
+size_t smoe_experts_ffn_routed_workspace_bytes(int k, int d_ff);
+
+/*
+ * Routed expert FFN of one token with the selection on the device
+ * ("Grouped Expert Dispatch": all ready experts in one submission, with the
+ * "exact-routing gate matvec" feeding it): for r < k, with e = top_idx[r],
+ *
+ *   out[r] = down_e . (SiLU(gate_e . x) * (up_e . x))
+ *
+ * so that smoe_route_topk_bf16 -> smoe_experts_ffn_routed_q4 -> smoe_combine
+ * is a whole MoE layer with no host round trip (it can be captured in one
+ * CUDA graph).  The expert indices are read on the device, after the
+ * previous kernel in the stream has completed (top_idx is typically written
+ * by smoe_route_topk_bf16 just before).
+ *
+ * gate_codes .. down_scales: DEVICE arrays of n_experts device pointers (a
+ *   table built once when the weights are loaded, 8-byte aligned); entry e
+ *   points to expert e's tensors with the layouts of smoe_gate_up_q4 and
+ *   smoe_down_q4, 16-byte aligned.  The host cannot read these tables: an
+ *   index outside [0, n_experts) or a table entry that is null or not
+ *   16-byte aligned is caught on the device, before any load through it;
+ *   that slot's outputs are then NaN and smoe_last_device_status returns
+ *   SMOE_ERR_ROUTE.  Entries must otherwise point to tensors of the stated
+ *   sizes.
+ * top_idx: int32 [k] on the device.  x: f32 [d_model].  out: f32
+ *   [k x d_model], written (row r for the r-th selected expert).
+ * workspace: at least smoe_experts_ffn_routed_workspace_bytes(k, d_ff)
+ *   bytes, 16-byte aligned (hidden activations; contents unspecified on
+ *   return).  Calls in flight at once need separate workspaces.
+ * 0 <= k <= SMOE_MAX_ROUTED_SLOTS; layout contract of the Q4 (Q2) calls;
+ * d_model and d_ff multiples of 256 (Q4) or 512 (Q2), at most 8192 (rows of
+ * whole multiples of 8 chunks of 16 bytes, which the bulk-copy decode
+ * kernels take; e.g. d_model 4096, d_ff 1536), else SMOE_ERR_SHAPE.
+ * k == 0 or d_model == 0: no-op; d_ff == 0: out is zeroed.
+ * Two launches (gate/up of the k slots, then their down projections).
+ */
+int smoe_experts_ffn_routed_q4(int n_experts, int k,
+                               const uint8_t *const *gate_codes,
+                               const float *const *gate_scales,
+                               const uint8_t *const *up_codes,
+                               const float *const *up_scales,
+                               const uint8_t *const *down_codes,
+                               const float *const *down_scales,
+                               const int *top_idx, const float *x, float *out,
+                               int d_model, int d_ff, int group,
+                               void *workspace, size_t workspace_bytes,
+                               void *stream);
+
+/* The same for Q2 weights (Z = 1.5, layout contract of smoe_gate_up_q2). */
+int smoe_experts_ffn_routed_q2(int n_experts, int k,
+                               const uint8_t *const *gate_codes,
+                               const float *const *gate_scales,
+                               const uint8_t *const *up_codes,
+                               const float *const *up_scales,
+                               const uint8_t *const *down_codes,
+                               const float *const *down_scales,
+                               const int *top_idx, const float *x, float *out,
+                               int d_model, int d_ff, int group,
+                               void *workspace, size_t workspace_bytes,
+                               void *stream);
+
 /* Size of the device array ffn_batch_q4_noalloc uses as its workspace. */
 #define SMOE_NOALLOC_SCRATCH_BYTES (32u << 20)
 
@@ -447,8 +518,9 @@ int ffn_batch_q4_noalloc(const uint8_t *gate_codes, const float *gate_scales,
  * after synchronising `stream`.  Kernels that wait on the device (bounded
  * mbarrier waits of the tensor-core batch path) set it when a wait gives up
  * instead of hanging; such a kernel skips its remaining work and exits.
- * Returns SMOE_OK, SMOE_ERR_TIMEOUT, or SMOE_ERR_LAUNCH if the stream or the
- * status word cannot be read.
+ * Returns SMOE_OK, SMOE_ERR_TIMEOUT, SMOE_ERR_ROUTE (a routed call met an
+ * invalid expert index or table entry), or SMOE_ERR_LAUNCH if the stream or
+ * the status word cannot be read.
  */
 int smoe_last_device_status(void *stream);
 

@@ -12,22 +12,23 @@ Pointer arguments accept a torch.Tensor (its data_ptr()), an int device
 address, or None (NULL).  `stream` accepts a torch.cuda.Stream, an int
 cudaStream_t, or None for torch's current stream on the current device.
 
-One MoE layer for one token, every step on the GPU::
+One MoE layer for one token, every step on the GPU and no host round trip
+(the four calls can be captured in one CUDA graph)::
 
     import moe_expert_ffn_smoe_gb300 as smoe
-    # gate: bf16 bits [n_experts, d_model] as int16; x: f32 [d_model]
+    # once, when the weights are loaded: device tables of expert pointers
+    tabs = [smoe.pointer_table(ts, dev) for ts in (gc, gs, uc, us, dc, ds)]
+    # per token; gate: bf16 bits [n_experts, d_model] as int16; x: f32 [d_model]
     smoe.smoe_route_topk_bf16(gate, x, n_experts, d_model, k, logits, idx, w)
-    sel = idx.tolist()          # the selection comes to the host (a sync)
-    smoe.smoe_experts_ffn_q4([gc[e] for e in sel], [gs[e] for e in sel],
-                             [uc[e] for e in sel], [us[e] for e in sel],
-                             [dc[e] for e in sel], [ds[e] for e in sel],
-                             x, expert_out, d_model, d_ff, group, ws, ws_bytes)
+    smoe.smoe_experts_ffn_routed_q4(n_experts, k, *tabs, idx, x, expert_out,
+                                    d_model, d_ff, group, ws, ws_bytes)
     smoe.smoe_combine(k, expert_out, w, out, d_model)
 
-(`ws`: smoe_experts_ffn_workspace_bytes(k, d_ff) bytes whose first
-SMOE_FFN_SYNC_BYTES are zero before the first call.)  Several tokens per
-expert go through smoe_experts_ffn_batch_q4/q2; a dense bf16 matvec is
-matvec_bf16, many of them in one submission matvec_bf16_batch.
+(`ws`: smoe_experts_ffn_routed_workspace_bytes(k, d_ff) bytes.)  With the
+selection on the host, smoe_experts_ffn_q4 takes host lists of the selected
+experts' tensors instead.  Several tokens per expert go through
+smoe_experts_ffn_batch_q4/q2; a dense bf16 matvec is matvec_bf16, many of
+them in one submission matvec_bf16_batch.
 """
 import ctypes
 import os
@@ -51,6 +52,8 @@ SMOE_ERR_LAUNCH = 5
 SMOE_ERR_TIMEOUT = 6
 SMOE_ERR_ALIAS = 7
 SMOE_ERR_MEMORY = 8
+SMOE_ERR_ROUTE = 9
+SMOE_MAX_ROUTED_SLOTS = 64
 SMOE_MAX_COLS = 32768
 SMOE_NOALLOC_SCRATCH_BYTES = 32 << 20
 SMOE_FFN_SYNC_BYTES = 512
@@ -78,6 +81,9 @@ _SIGS = {
     "smoe_ffn_batch_workspace_bytes": ([_I, _I, _I, _I], _SZ),
     "ffn_batch_q4": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
     "ffn_batch_q2": ([_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _SZ, _P], _I),
+    "smoe_experts_ffn_routed_workspace_bytes": ([_I, _I], _SZ),
+    "smoe_experts_ffn_routed_q4": ([_I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
+    "smoe_experts_ffn_routed_q2": ([_I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _P, _SZ, _P], _I),
     "smoe_route_topk_bf16": ([_P, _P, _I, _I, _I, _P, _P, _P, _P], _I),
     "smoe_combine": ([_I, _P, _P, _P, _I, _P], _I),
     "smoe_experts_ffn_batch_workspace_bytes": ([_I, _P, _I, _I, _I], _SZ),
@@ -274,6 +280,39 @@ def ffn_batch_q2(gate_codes, gate_scales, up_codes, up_scales, down_codes, down_
 
 SMOE_MAX_TOP_K = 64
 SMOE_MAX_ROUTE_EXPERTS = 8192
+
+
+def pointer_table(tensors, device):
+    """A device array (torch int64 [n]) of the tensors' data pointers: the
+    table argument of smoe_experts_ffn_routed_q4/q2, built once."""
+    import torch
+    return torch.tensor([t.data_ptr() for t in tensors], dtype=torch.int64, device=device)
+
+
+def smoe_experts_ffn_routed_workspace_bytes(k, d_ff):
+    return _lib.smoe_experts_ffn_routed_workspace_bytes(k, d_ff)
+
+
+def smoe_experts_ffn_routed_q4(n_experts, k, gate_codes, gate_scales, up_codes, up_scales, down_codes,
+                               down_scales, top_idx, x, out, d_model, d_ff, group, workspace, workspace_bytes,
+                               stream=None):
+    """Tables: device arrays of n_experts pointers (pointer_table); top_idx:
+    int32 [k] on the device; out [k, d_model]."""
+    _check(_lib.smoe_experts_ffn_routed_q4(n_experts, k, _ptr(gate_codes), _ptr(gate_scales), _ptr(up_codes),
+                                           _ptr(up_scales), _ptr(down_codes), _ptr(down_scales), _ptr(top_idx),
+                                           _ptr(x), _ptr(out), d_model, d_ff, group, _ptr(workspace),
+                                           workspace_bytes, _stream(stream)),
+           "smoe_experts_ffn_routed_q4")
+
+
+def smoe_experts_ffn_routed_q2(n_experts, k, gate_codes, gate_scales, up_codes, up_scales, down_codes,
+                               down_scales, top_idx, x, out, d_model, d_ff, group, workspace, workspace_bytes,
+                               stream=None):
+    _check(_lib.smoe_experts_ffn_routed_q2(n_experts, k, _ptr(gate_codes), _ptr(gate_scales), _ptr(up_codes),
+                                           _ptr(up_scales), _ptr(down_codes), _ptr(down_scales), _ptr(top_idx),
+                                           _ptr(x), _ptr(out), d_model, d_ff, group, _ptr(workspace),
+                                           workspace_bytes, _stream(stream)),
+           "smoe_experts_ffn_routed_q2")
 
 
 def smoe_route_topk_bf16(gate_w, x, n_experts, d_model, k, logits, top_idx, top_w, stream=None):

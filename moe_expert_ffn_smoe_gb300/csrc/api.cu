@@ -376,6 +376,75 @@ int experts_batch_impl(int bits, int n, const uint8_t *const *gc, const float *c
                                                     workspace, static_cast<cudaStream_t>(stream)));
 }
 
+// Routed FFN: hidden[k x d_ff] in the workspace, out[k x d_model].
+size_t routed_hidden_bytes(int k, int d_ff)
+{
+    const size_t b = static_cast<size_t>(k) * static_cast<size_t>(d_ff) * sizeof(float);
+    return (b + 255u) & ~static_cast<size_t>(255u);
+}
+
+int experts_ffn_routed_impl(int bits, int n_experts, int k, const uint8_t *const *gc, const float *const *gs,
+                            const uint8_t *const *uc, const float *const *us, const uint8_t *const *dc,
+                            const float *const *ds, const int *top_idx, const float *x, float *out, int d_model,
+                            int d_ff, int group, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (n_experts < 0 || k < 0 || k > SMOE_MAX_ROUTED_SLOTS) return SMOE_ERR_SHAPE;
+    int st = check_q_shape(bits, d_ff, d_model, group);
+    if (st != SMOE_OK) return st;
+    st = check_q_shape(bits, d_model, d_ff, group);
+    if (st != SMOE_OK) return st;
+    // rows the bulk-copy decode kernels take: whole multiples of 8 chunks of
+    // 16 bytes, at most 8192 columns (their staging then always fits)
+    const int unit = bits == 4 ? 256 : 512;
+    if (d_model % unit || d_ff % unit || d_model > 8192 || d_ff > 8192) return SMOE_ERR_SHAPE;
+    if (k == 0 || d_model == 0) return SMOE_OK;
+    if (n_experts == 0) return SMOE_ERR_SHAPE;  // no index could be valid
+    if (!out || !top_idx) return SMOE_ERR_NULL;
+    if (!aligned16(out) || (reinterpret_cast<uintptr_t>(top_idx) & 3u)) return SMOE_ERR_ALIGN;
+    const size_t out_bytes = static_cast<size_t>(k) * static_cast<size_t>(d_model) * sizeof(float);
+    const Span idx_span = {top_idx, static_cast<size_t>(k) * sizeof(int)};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d_ff == 0) {
+        // every output is an empty sum
+        if (overlap(Span{out, out_bytes}, idx_span)) return SMOE_ERR_ALIAS;
+        return to_status(cudaMemsetAsync(out, 0, out_bytes, s));
+    }
+    if (!gc || !gs || !uc || !us || !dc || !ds || !x) return SMOE_ERR_NULL;
+    const void *tabs[6] = {gc, gs, uc, us, dc, ds};
+    for (const void *t : tabs)
+        if (reinterpret_cast<uintptr_t>(t) & 7u) return SMOE_ERR_ALIGN;
+    if (!aligned16(x)) return SMOE_ERR_ALIGN;
+    const size_t need = routed_hidden_bytes(k, d_ff);
+    if (!workspace || workspace_bytes < need) return SMOE_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return SMOE_ERR_ALIGN;
+    const size_t tab_bytes = static_cast<size_t>(n_experts) * sizeof(void *);
+    const Span outs[2] = {{out, out_bytes}, {workspace, need}};
+    const Span ins[8] = {{x, static_cast<size_t>(d_model) * sizeof(float)}, idx_span,
+                         {gc, tab_bytes}, {gs, tab_bytes}, {uc, tab_bytes}, {us, tab_bytes},
+                         {dc, tab_bytes}, {ds, tab_bytes}};
+    if (any_alias(outs, 2, ins, 8)) return SMOE_ERR_ALIAS;
+    float *hidden = static_cast<float *>(workspace);
+    const float *xs[SMOE_MAX_ROUTED_SLOTS];
+    float *ys[SMOE_MAX_ROUTED_SLOTS];
+    for (int e = 0; e < k; ++e) {
+        xs[e] = x;
+        ys[e] = hidden + static_cast<size_t>(e) * d_ff;
+    }
+    bool unsupported = true;
+    cudaError_t err = smoe::launch_qgemv_routed(bits, 2, k, gc, uc, gs, us, top_idx, n_experts, xs, ys, d_ff,
+                                                d_model, group, s, &unsupported);
+    if (unsupported) return SMOE_ERR_SHAPE;
+    if (err != cudaSuccess) return SMOE_ERR_LAUNCH;
+    for (int e = 0; e < k; ++e) {
+        xs[e] = hidden + static_cast<size_t>(e) * d_ff;
+        ys[e] = out + static_cast<size_t>(e) * d_model;
+    }
+    err = smoe::launch_qgemv_routed(bits, 1, k, dc, dc, ds, ds, top_idx, n_experts, xs, ys, d_model, d_ff, group,
+                                    s, &unsupported);
+    if (unsupported) return SMOE_ERR_SHAPE;
+    return to_status(err);
+}
+
 }  // namespace
 
 extern "C" {
@@ -446,6 +515,7 @@ const char *smoe_status_string(int status)
     case SMOE_ERR_TIMEOUT: return "a device-side bounded wait gave up";
     case SMOE_ERR_ALIAS: return "an output overlaps an input or another output";
     case SMOE_ERR_MEMORY: return "a buffer is not accessible from the device";
+    case SMOE_ERR_ROUTE: return "a device-side expert index or table entry was invalid";
     default: return "unknown status";
     }
 }
@@ -586,6 +656,36 @@ int smoe_experts_ffn_batch_q2(int n_experts, const uint8_t *const *gate_codes, c
                               X, Y, T, d_model, d_ff, group, workspace, workspace_bytes, stream);
 }
 
+size_t smoe_experts_ffn_routed_workspace_bytes(int k, int d_ff)
+{
+    if (k < 0 || k > SMOE_MAX_ROUTED_SLOTS || d_ff < 0) return static_cast<size_t>(-1);
+    return routed_hidden_bytes(k, d_ff);
+}
+
+int smoe_experts_ffn_routed_q4(int n_experts, int k, const uint8_t *const *gate_codes,
+                               const float *const *gate_scales, const uint8_t *const *up_codes,
+                               const float *const *up_scales, const uint8_t *const *down_codes,
+                               const float *const *down_scales, const int *top_idx, const float *x, float *out,
+                               int d_model, int d_ff, int group, void *workspace, size_t workspace_bytes,
+                               void *stream)
+{
+    return experts_ffn_routed_impl(4, n_experts, k, gate_codes, gate_scales, up_codes, up_scales, down_codes,
+                                   down_scales, top_idx, x, out, d_model, d_ff, group, workspace, workspace_bytes,
+                                   stream);
+}
+
+int smoe_experts_ffn_routed_q2(int n_experts, int k, const uint8_t *const *gate_codes,
+                               const float *const *gate_scales, const uint8_t *const *up_codes,
+                               const float *const *up_scales, const uint8_t *const *down_codes,
+                               const float *const *down_scales, const int *top_idx, const float *x, float *out,
+                               int d_model, int d_ff, int group, void *workspace, size_t workspace_bytes,
+                               void *stream)
+{
+    return experts_ffn_routed_impl(2, n_experts, k, gate_codes, gate_scales, up_codes, up_scales, down_codes,
+                                   down_scales, top_idx, x, out, d_model, d_ff, group, workspace, workspace_bytes,
+                                   stream);
+}
+
 int smoe_route_topk_bf16(const uint16_t *gate_w, const float *x, int n_experts, int d_model, int k, float *logits,
                          int *top_idx, float *top_w, void *stream)
 {
@@ -646,6 +746,7 @@ int smoe_last_device_status(void *stream)
     unsigned v = 0;
     if (smoe::read_and_clear_device_status(static_cast<cudaStream_t>(stream), &v) != cudaSuccess)
         return SMOE_ERR_LAUNCH;
+    if (v == smoe::kStatusRoute) return SMOE_ERR_ROUTE;
     return v ? SMOE_ERR_TIMEOUT : SMOE_OK;
 }
 

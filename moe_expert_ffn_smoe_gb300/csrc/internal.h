@@ -33,6 +33,20 @@ cudaError_t launch_qgemv_experts(int bits, int nmat, int n_experts, const uint8_
                                  const float *const *scales1, const float *const *x, float *const *y,
                                  int units, int K, int group, cudaStream_t stream, bool *unsupported);
 
+// The same kernels for a routed launch: slot e (of n_slots <= 64) uses the
+// weights of expert route[e] (a device array written by an earlier kernel)
+// from device tables of n_route pointers; x[e], y[e] are the slot's input
+// and output.  Sets *unsupported (and launches nothing) for shapes these
+// kernels do not take.
+cudaError_t launch_qgemv_routed(int bits, int nmat, int n_slots, const uint8_t *const *tab_codes0,
+                                const uint8_t *const *tab_codes1, const float *const *tab_scales0,
+                                const float *const *tab_scales1, const int *route, int n_route,
+                                const float *const *x, float *const *y, int units, int K, int group,
+                                cudaStream_t stream, bool *unsupported);
+
+// Device status word value of a routed index outside its table.
+constexpr unsigned kStatusRoute = 16u;
+
 // The fused routed-expert FFN over n <= 64 experts in one launch
 // (expert_ffn.cu): hidden [n x d_ff] and the hand-off counters `sync`
 // (2 x 64 words, zero on entry, zero again on completion) live in the

@@ -68,22 +68,21 @@ __global__ void __launch_bounds__(H == 1 ? 384 : 512, 1) qgemv_reg(const __grid_
     const uint8_t *src0 = nullptr;
     size_t src_step = 0;
     uint32_t row_b = 0, dst_off = 0;
-    if (role_any) {
+    auto set_sources = [&](const uint8_t *const (&cm)[2], const float *const (&sm)[2]) {
+        if (!role_any) return;
         const int m = role_m < NMAT ? role_m : 0;
         const size_t first_row = static_cast<size_t>(u0) + static_cast<size_t>(warp) * R;
         if (role_codes) {
-            const uint8_t *c = (NMAT == 2 && m == 1) ? a.codes[1][e] : a.codes[0][e];
-            src0 = c + first_row * ROW_BYTES;
+            src0 = cm[m] + first_row * ROW_BYTES;
             row_b = ROW_BYTES;
             dst_off = static_cast<uint32_t>(m * R) * ROW_BYTES;
         } else {
-            const float *sc = (NMAT == 2 && m == 1) ? a.scales[1][e] : a.scales[0][e];
-            src0 = reinterpret_cast<const uint8_t *>(sc + first_row * ngroups);
+            src0 = reinterpret_cast<const uint8_t *>(sm[m] + first_row * ngroups);
             row_b = sbytes_row;
             dst_off = scales_off + static_cast<uint32_t>(m * R) * sbytes_row;
         }
         src_step = static_cast<size_t>(NW) * R * row_b;
-    }
+    };
 
     // The whole warp: the copies of its k-th stage into slot `si`.
     auto issue = [&](int k, int si) {
@@ -102,12 +101,27 @@ __global__ void __launch_bounds__(H == 1 ? 384 : 512, 1) qgemv_reg(const __grid_
     }
     __syncwarp();
     // Weights never depend on an earlier kernel: the first stage goes out
-    // before waiting for it.  The rest of the first wave follows the staging
-    // of x, whose loads would otherwise queue behind it.
+    // before waiting for it (unless the weights themselves are chosen by the
+    // previous kernel: a routed launch).  The rest of the first wave follows
+    // the staging of x, whose loads would otherwise queue behind it.
     const int first = my < ns ? my : ns;
-    if (first > 0) issue(0, 0);
+    const uint8_t *wc[2];
+    const float *ws[2];
+    if (!a.route) {
+        slot_weights(a, e, NMAT, wc, ws);
+        set_sources(wc, ws);
+        if (first > 0) issue(0, 0);
+    }
 
     pdl_wait();
+    if (a.route) {
+        if (!slot_weights(a, e, NMAT, wc, ws)) {
+            fail_route(a, a.y[e], r0, r1);
+            return;
+        }
+        set_sources(wc, ws);
+        if (first > 0) issue(0, 0);
+    }
     stage_x_digits<BITS>(a.x[e], a.K, a.group, smem, a.off_info);
     __syncthreads();
     if (threadIdx.x == 0) pdl_launch_dependents();

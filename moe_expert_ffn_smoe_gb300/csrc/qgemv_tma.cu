@@ -85,6 +85,9 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
     const uint32_t slots = sbase + a.off_slots + static_cast<uint32_t>(warp * ns) * a.stage_bytes;
     const uint32_t scales_off = static_cast<uint32_t>(NMAT * R) * row_bytes;
 
+    // this slot's weights (a routed launch resolves them after the wait)
+    const uint8_t *mc[2];
+    const float *ms[2];
     // lane 0: the bulk copies of this warp's k-th stage into slot k % ns
     auto issue = [&](int k) {
         const int us = u0 + (warp + k * NW) * R;
@@ -97,25 +100,35 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
 #pragma unroll
         for (int m = 0; m < NMAT; ++m) {
             bulk_g2s(slot + static_cast<uint32_t>(m * R) * row_bytes,
-                     a.codes[m][e] + static_cast<size_t>(us) * row_bytes, cb, bar);
+                     mc[m] + static_cast<size_t>(us) * row_bytes, cb, bar);
             if (sb)
                 bulk_g2s(slot + scales_off + static_cast<uint32_t>(m * R * ngroups) * 4u,
-                         a.scales[m][e] + static_cast<size_t>(us) * ngroups, sb, bar);
+                         ms[m] + static_cast<size_t>(us) * ngroups, sb, bar);
         }
     };
 
     // Weights never depend on an earlier kernel: the first stage goes out
-    // before waiting for it; the rest of the first wave follows the staging
-    // of x, whose loads would otherwise queue behind it.
+    // before waiting for it (unless a routed launch's previous kernel chose
+    // them); the rest of the first wave follows the staging of x, whose
+    // loads would otherwise queue behind it.
     const int first = my < ns ? my : ns;
+    if (!a.route) slot_weights(a, e, NMAT, mc, ms);
     if (lane == 0) {
         for (int i = 0; i < ns; ++i) mbar_init(bars + 8u * i, 1);
         fence_mbar_init();
-        if (first > 0) issue(0);
+        if (first > 0 && !a.route) issue(0);
     }
     __syncwarp();
 
     pdl_wait();
+    if (a.route) {
+        if (!slot_weights(a, e, NMAT, mc, ms)) {
+            fail_route(a, a.y[e], u0, u1);
+            return;
+        }
+        if (lane == 0 && first > 0) issue(0);
+        __syncwarp();
+    }
     stage_x_digits<BITS>(a.x[e], a.K, a.group, smem, a.off_info);
     __syncthreads();
     if (threadIdx.x == 0) pdl_launch_dependents();
@@ -162,7 +175,7 @@ __global__ void __launch_bounds__(512, 1) qgemv_tma(const __grid_constant__ QGAr
                     const int C = chunk_dot<BITS>(cw, dg, __float_as_int(inf.w));  // sum (code - OFF) * xq
                     const float sc =
                         a.scales_tma ? lds_f32(slot + scales_off + static_cast<uint32_t>((m * R + ul) * ngroups + g) * 4u)
-                                     : ldg_f32(a.scales[m][e] + static_cast<size_t>(min(us + ul, u1 - 1)) * ngroups + g);
+                                     : ldg_f32(ms[m] + static_cast<size_t>(min(us + ul, u1 - 1)) * ngroups + g);
                     acc[m][r] = fmaf(sc, fmaf(static_cast<float>(C), qz, inf.y), acc[m][r]);
                 }
         }
@@ -355,6 +368,17 @@ cudaError_t launch_tma(QGArgs &a, int n_experts, cudaStream_t stream, bool *unsu
 
 }  // namespace
 
+namespace {
+
+cudaError_t launch_any(QGArgs &a, int bits, int nmat, int n, cudaStream_t stream, bool *unsupported)
+{
+    if (bits == 4)
+        return nmat == 2 ? launch_tma<4, 2>(a, n, stream, unsupported) : launch_tma<4, 1>(a, n, stream, unsupported);
+    return nmat == 2 ? launch_tma<2, 2>(a, n, stream, unsupported) : launch_tma<2, 1>(a, n, stream, unsupported);
+}
+
+}  // namespace
+
 cudaError_t launch_qgemv_experts(int bits, int nmat, int n_experts, const uint8_t *const *codes0,
                                  const uint8_t *const *codes1, const float *const *scales0,
                                  const float *const *scales1, const float *const *x, float *const *y,
@@ -373,11 +397,31 @@ cudaError_t launch_qgemv_experts(int bits, int nmat, int n_experts, const uint8_
     a.units = units;
     a.K = K;
     a.group = group;
-    if (bits == 4)
-        return nmat == 2 ? launch_tma<4, 2>(a, n_experts, stream, unsupported)
-                         : launch_tma<4, 1>(a, n_experts, stream, unsupported);
-    return nmat == 2 ? launch_tma<2, 2>(a, n_experts, stream, unsupported)
-                     : launch_tma<2, 1>(a, n_experts, stream, unsupported);
+    return launch_any(a, bits, nmat, n_experts, stream, unsupported);
+}
+
+cudaError_t launch_qgemv_routed(int bits, int nmat, int n_slots, const uint8_t *const *tab_codes0,
+                                const uint8_t *const *tab_codes1, const float *const *tab_scales0,
+                                const float *const *tab_scales1, const int *route, int n_route,
+                                const float *const *x, float *const *y, int units, int K, int group,
+                                cudaStream_t stream, bool *unsupported)
+{
+    QGArgs a = {};
+    for (int i = 0; i < n_slots && i < QG_MAX_EXPERTS; ++i) {
+        a.x[i] = x[i];
+        a.y[i] = y[i];
+    }
+    a.route_codes[0] = tab_codes0;
+    a.route_codes[1] = nmat == 2 ? tab_codes1 : tab_codes0;
+    a.route_scales[0] = tab_scales0;
+    a.route_scales[1] = nmat == 2 ? tab_scales1 : tab_scales0;
+    a.route = route;
+    a.n_route = n_route;
+    a.status = device_status_word();
+    a.units = units;
+    a.K = K;
+    a.group = group;
+    return launch_any(a, bits, nmat, n_slots, stream, unsupported);
 }
 
 }  // namespace smoe

@@ -17,6 +17,13 @@ struct QGArgs {
     const float *scales[2][QG_MAX_EXPERTS];
     const float *x[QG_MAX_EXPERTS];
     float *y[QG_MAX_EXPERTS];
+    // Routed launches (route != nullptr): slot e's weights are entry route[e]
+    // of device tables of n_route pointers, read after griddepcontrol.wait
+    // (the indices come from the previous kernel); codes/scales are unused.
+    const uint8_t *const *route_codes[2];
+    const float *const *route_scales[2];
+    const int *route;
+    int n_route;
     unsigned *status;      // device status word (bounded waits)
     int ctas_per_expert;
     int units;             // output rows per expert
@@ -247,6 +254,42 @@ __device__ void stage_x_digits(const float *__restrict__ x, int K, int group, ui
     }
 }
 
+
+// The weights of slot e: the launch's own pointers, or for a routed launch
+// (called after griddepcontrol.wait) the table entries of expert route[e].
+// Returns false for a routed index outside [0, n_route) or a table entry
+// that is null or not 16-byte aligned; the caller then records
+// kStatusRoute and writes NaN to the slot's outputs.
+__device__ __forceinline__ bool slot_weights(const QGArgs &a, int e, int nmat, const uint8_t *(&c)[2],
+                                             const float *(&s)[2])
+{
+    if (!a.route) {
+        c[0] = a.codes[0][e];
+        c[1] = a.codes[nmat - 1][e];
+        s[0] = a.scales[0][e];
+        s[1] = a.scales[nmat - 1][e];
+        return true;
+    }
+    const int idx = a.route[e];
+    if (idx < 0 || idx >= a.n_route) return false;
+    c[0] = a.route_codes[0][idx];
+    c[1] = a.route_codes[nmat - 1][idx];
+    s[0] = a.route_scales[0][idx];
+    s[1] = a.route_scales[nmat - 1][idx];
+    // the bulk copies need 16-byte aligned sources: a table entry that is
+    // null or misaligned is refused like a bad index, before any copy
+    const uintptr_t bad = (reinterpret_cast<uintptr_t>(c[0]) | reinterpret_cast<uintptr_t>(c[1]) |
+                           reinterpret_cast<uintptr_t>(s[0]) | reinterpret_cast<uintptr_t>(s[1])) & 15u;
+    return bad == 0 && c[0] && c[1] && s[0] && s[1];
+}
+
+// Every thread of the block: NaN into y[r0, r1) (a routed slot whose index
+// is out of range), and one thread records the status.
+__device__ __forceinline__ void fail_route(const QGArgs &a, float *y, int r0, int r1)
+{
+    for (int i = r0 + static_cast<int>(threadIdx.x); i < r1; i += blockDim.x) y[i] = __uint_as_float(0x7FC00000u);
+    if (threadIdx.x == 0 && a.status) atomicExch(a.status, kStatusRoute);
+}
 
 using QGKernelFn = void (*)(QGArgs);
 

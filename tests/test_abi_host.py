@@ -41,9 +41,9 @@ def test_library_exports_every_declared_function(smoe):
 
 
 def test_abi_version_and_status_strings(smoe):
-    assert smoe.smoe_abi_version() == 1
-    for s in range(8):
-        assert smoe.smoe_status_string(s)
+    assert smoe.smoe_abi_version() == 2
+    for s in range(10):
+        assert smoe.smoe_status_string(s) != "unknown status"
     assert smoe.smoe_status_string(99) == "unknown status"
 
 
@@ -320,3 +320,44 @@ def test_noalloc_refusals_before_any_launch(smoe):
     assert L.ffn_batch_q4_noalloc(*ptrs, 0, 4096, 1536, 48, None) == smoe.SMOE_ERR_SHAPE
     assert L.ffn_batch_q4(*ptrs[:8], 0, 4096, 1536, 48, None, 0, None) == smoe.SMOE_ERR_SHAPE
     assert L.smoe_ffn_batch_workspace_bytes(0, 4096, 1536, 48) == ctypes.c_size_t(-1).value
+
+
+@pytest.mark.parametrize("bits", [4, 2])
+def test_routed_refusals_before_any_launch(smoe, bits):
+    """smoe_experts_ffn_routed_q4/q2: every host-side check returns its
+    status without launching (fake, aligned device addresses)."""
+    L = smoe._lib
+    f = L.smoe_experts_ffn_routed_q4 if bits == 4 else L.smoe_experts_ffn_routed_q2
+    tabs = [A + 0x100000 * i for i in range(6)]
+    idx, x, out, ws = A + 0x1000000, A + 0x2000000, A + 0x3000000, A + 0x4000000
+    need = L.smoe_experts_ffn_routed_workspace_bytes(8, 1536)
+    assert need == 8 * 1536 * 4
+    assert L.smoe_experts_ffn_routed_workspace_bytes(65, 1536) == ctypes.c_size_t(-1).value
+    assert L.smoe_experts_ffn_routed_workspace_bytes(-1, 1536) == ctypes.c_size_t(-1).value
+
+    def call(n=128, k=8, tabs=tabs, idx=idx, x=x, out=out, d_model=4096, d_ff=1536, group=64, ws=ws,
+             wsb=need):
+        return f(n, k, *tabs, idx, x, out, d_model, d_ff, group, ws, wsb, None)
+
+    assert call(k=0) == smoe.SMOE_OK                       # nothing selected: no-op
+    assert call(k=65) == smoe.SMOE_ERR_SHAPE               # beyond SMOE_MAX_ROUTED_SLOTS
+    assert call(k=-1) == smoe.SMOE_ERR_SHAPE
+    assert call(n=0) == smoe.SMOE_ERR_SHAPE                # no index could be valid
+    assert call(group=48) == smoe.SMOE_ERR_SHAPE
+    assert call(d_model=4096 + 16) == smoe.SMOE_ERR_SHAPE
+    assert call(idx=None) == smoe.SMOE_ERR_NULL
+    assert call(out=None) == smoe.SMOE_ERR_NULL
+    assert call(tabs=[None] + tabs[1:]) == smoe.SMOE_ERR_NULL
+    assert call(tabs=[A + 4] + tabs[1:]) == smoe.SMOE_ERR_ALIGN   # tables are pointer arrays
+    assert call(idx=idx + 2) == smoe.SMOE_ERR_ALIGN
+    assert call(out=out + 8) == smoe.SMOE_ERR_ALIGN
+    assert call(ws=None) == smoe.SMOE_ERR_WORKSPACE
+    assert call(wsb=need - 4) == smoe.SMOE_ERR_WORKSPACE
+    assert call(out=ws) == smoe.SMOE_ERR_ALIAS             # out over the workspace
+    assert call(out=x) == smoe.SMOE_ERR_ALIAS              # out over the token
+    assert call(idx=out + 64) == smoe.SMOE_ERR_ALIAS       # out over the indices
+    # rows the bulk-copy decode kernels do not take: not whole multiples of
+    # 8 chunks, or longer than 8192 columns
+    assert call(d_model=256, d_ff=96 if bits == 4 else 192, group=32 if bits == 4 else 64) == smoe.SMOE_ERR_SHAPE
+    assert call(d_model=16384) == smoe.SMOE_ERR_SHAPE
+    assert call(d_ff=1536 + (128 if bits == 4 else 256)) == smoe.SMOE_ERR_SHAPE
