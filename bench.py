@@ -545,7 +545,9 @@ def rows_breakdown(smoe, dev, steps, pattern=""):
             bf16_row(smoe, dev, steps, out, hbm_peak, timed, s, rows, cols, seed)
     if pattern in "bf16_batch_8x512x4096":
         bf16_batch_row(smoe, dev, steps, out, hbm_peak, timed, s)
-    for T in inp.CONFIGS["q4_token_batch"]["tokens"]:
+    # the workload's token counts, plus 2, 4 and 8 (the decode-slot path
+    # below the measured crossover with the tensor cores)
+    for T in sorted(set(inp.CONFIGS["q4_token_batch"]["tokens"]) | {2, 4, 8}):
         if pattern in f"q4_token_batch_T{T}":
             batch_row(smoe, dev, steps, out, hbm_peak, timed, s, T)
     for T in (16, 256):

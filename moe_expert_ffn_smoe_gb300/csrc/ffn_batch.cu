@@ -3,12 +3,14 @@
 // every row of X [T x d_model], gate/up+SiLU into H [T x d_ff] (the caller's
 // workspace), then down into Y [T x d_model].
 //
-// Paths: one token goes through the decode kernels (qgemv.cu); two or more
-// tokens go to the tensor cores (ffn_batch_tc.cu) when the group size and
-// both dimensions are multiples of 64; other shapes use the CUDA-core
-// multi-token GEMV below, in which a warp unpacks each 16-byte chunk of
-// codes once and applies it to TT tokens whose x rows are staged in shared
-// memory.
+// Paths: one token goes through the decode kernels (qgemv.cu); 2 to 8
+// tokens go through the grouped decode kernels with one slot per token
+// (qgemv_tma.cu / qgemv_reg.cu) when both row lengths are whole multiples of
+// 8 chunks; more tokens go to the tensor cores (ffn_batch_tc.cu) when the
+// group size and both dimensions are multiples of 64; other shapes use the
+// CUDA-core multi-token GEMV below, in which a warp unpacks each 16-byte
+// chunk of codes once and applies it to TT tokens whose x rows are staged in
+// shared memory.
 #include <mutex>
 
 #include "common.cuh"
@@ -198,12 +200,41 @@ cudaError_t launch_qgemm_tokens(int bits, int nmat, const uint8_t *const codes[2
     return nmat == 2 ? launch_tok_pick<2>(a, stream) : launch_tok_pick<1>(a, stream);
 }
 
+namespace {
+
+// Token counts from 2 to kSlotTokens run as T one-token decodes of the same
+// expert: the grouped decode kernels with one slot per token, all slots
+// sharing the expert's weights (read from DRAM once, the other slots' reads
+// hit L2).  Below the measured crossover this is faster than the tensor
+// cores, whose per-call latency (token prep, first K tile, split-K finish)
+// does not shrink with T.
+constexpr int kSlotTokens = 8;
+
+// Shapes the grouped decode kernels take for both projections: rows of
+// whole multiples of 8 chunks of 16 bytes, at most 8192 columns.
+bool slot_path(int bits, int T, int d_model, int d_ff)
+{
+    const int unit = bits == 4 ? 256 : 512;
+    return T >= 2 && T <= kSlotTokens && d_model > 0 && d_ff > 0 && d_model % unit == 0 && d_ff % unit == 0 &&
+           d_model <= 8192 && d_ff <= 8192;
+}
+
+}  // namespace
+
 size_t ffn_batch_workspace(int T, int d_model, int d_ff, int group)
 {
     if (T <= 0) return 0;
-    if (T > 1 && tc_batch_supported(T, d_model, d_ff, group)) return tc_batch_workspace(T, d_model, d_ff);
-    const size_t hidden = static_cast<size_t>(T) * static_cast<size_t>(d_ff) * sizeof(float);
-    return (hidden + 255) & ~static_cast<size_t>(255);
+    // the slot path and the CUDA-core path need hidden f32 [T x d_ff]; the
+    // size does not depend on the code width, so a token count that a Q4
+    // call runs on the slots while a Q2 call of the same shape takes the
+    // tensor cores gets the larger of the two
+    const size_t hidden = (static_cast<size_t>(T) * static_cast<size_t>(d_ff) * sizeof(float) + 255) &
+                          ~static_cast<size_t>(255);
+    if (T > 1 && tc_batch_supported(T, d_model, d_ff, group)) {
+        const size_t tc = tc_batch_workspace(T, d_model, d_ff);
+        return tc > hidden ? tc : hidden;
+    }
+    return hidden;
 }
 
 cudaError_t launch_ffn_batch(int bits, const uint8_t *const gu_codes[2], const float *const gu_scales[2],
@@ -219,6 +250,30 @@ cudaError_t launch_ffn_batch(int bits, const uint8_t *const gu_codes[2], const f
         if (d_ff > 0) e = launch_qgemv(bits, 2, gu_codes, gu_scales, X, H, d_ff, d_model, group, stream);
         if (e != cudaSuccess) return e;
         return launch_qgemv(bits, 1, dc, ds, H, Y, d_model, d_ff, group, stream);
+    }
+    if (slot_path(bits, T, d_model, d_ff)) {
+        const uint8_t *c0[kSlotTokens], *c1[kSlotTokens];
+        const float *s0[kSlotTokens], *s1[kSlotTokens], *xs[kSlotTokens];
+        float *ys[kSlotTokens];
+        for (int t = 0; t < T; ++t) {
+            c0[t] = gu_codes[0];
+            c1[t] = gu_codes[1];
+            s0[t] = gu_scales[0];
+            s1[t] = gu_scales[1];
+            xs[t] = X + static_cast<size_t>(t) * d_model;
+            ys[t] = H + static_cast<size_t>(t) * d_ff;
+        }
+        bool unsupported = true;
+        e = launch_qgemv_experts(bits, 2, T, c0, c1, s0, s1, xs, ys, d_ff, d_model, group, stream, &unsupported);
+        if (e != cudaSuccess || unsupported) return unsupported ? cudaErrorInvalidValue : e;
+        for (int t = 0; t < T; ++t) {
+            c0[t] = down_codes;
+            s0[t] = down_scales;
+            xs[t] = H + static_cast<size_t>(t) * d_ff;
+            ys[t] = Y + static_cast<size_t>(t) * d_model;
+        }
+        e = launch_qgemv_experts(bits, 1, T, c0, c0, s0, s0, xs, ys, d_model, d_ff, group, stream, &unsupported);
+        return unsupported ? cudaErrorInvalidValue : e;
     }
     if (tc_batch_supported(T, d_model, d_ff, group))
         return launch_ffn_batch_tc(bits, gu_codes, gu_scales, down_codes, down_scales, X, Y, T, d_model, d_ff,

@@ -159,8 +159,8 @@ __device__ __forceinline__ int chunk_dot(const uint4 &cw, const uint4 *dg, int c
 // inside it, the uint4 at (3k + j)*16 holds digit j of byte class k for the
 // chunk's 4 code words (word v in component v).  info[c] = {q, q * Sxq *
 // FOLD, group index, -OFF * Sxq (int bits)}.  Called by all threads of the
-// block (blockDim.x % 32 == 0); the caller synchronises the block before
-// reading the result.
+// block (blockDim.x % 32 == 0), or by one whole warp; the caller
+// synchronises them before reading the result.
 //
 // Rounding grid.  Each 16-byte chunk of codes (32 Q4 or 64 Q2 columns) has
 // its own power-of-two step q, the smallest for which the chunk's largest
@@ -170,9 +170,16 @@ __device__ __forceinline__ int chunk_dot(const uint4 &cw, const uint4 *dg, int c
 // four consecutive lanes and its maximum is two shuffles.
 // COHERENT: x was written by other CTAs of the running grid (read through L2
 // only, never through the read-only path).
+// tid / nthreads: this thread's index among the threads that stage (all of
+// the block by default, or one warp: lane and 32); nthreads % 32 == 0.
 template <int BITS, bool COHERENT = false>
-__device__ void stage_x_digits(const float *__restrict__ x, int K, int group, uint8_t *smem, uint32_t off_info)
+__device__ void stage_x_digits(const float *__restrict__ x, int K, int group, uint8_t *smem, uint32_t off_info,
+                               int tid = -1, int nthreads = 0)
 {
+    if (tid < 0) {
+        tid = static_cast<int>(threadIdx.x);
+        nthreads = static_cast<int>(blockDim.x);
+    }
     using D = DigitFmt<BITS>;
     const int nwords = K / D::WORD_COLS;  // a multiple of 4: K is a multiple of the chunk
     float4 *info = reinterpret_cast<float4 *>(smem + off_info);
@@ -189,16 +196,18 @@ __device__ void stage_x_digits(const float *__restrict__ x, int K, int group, ui
         }
     };
 
-    for (int base = 0; base < nwords; base += blockDim.x) {
-        const int v = base + threadIdx.x;
+    // the words of the next pass are loaded before the current one is
+    // converted, so the passes' loads overlap (one warp staging a vector
+    // takes several passes)
+    float fn[D::WORD_COLS];
+    if (tid < nwords) load_word(tid, fn);
+    for (int base = 0; base < nwords; base += nthreads) {
+        const int v = base + tid;
         const bool valid = v < nwords;
         float f[D::WORD_COLS];
-        if (valid) {
-            load_word(v, f);
-        } else {
 #pragma unroll
-            for (int i = 0; i < D::WORD_COLS; ++i) f[i] = 0.f;
-        }
+        for (int i = 0; i < D::WORD_COLS; ++i) f[i] = valid ? fn[i] : 0.f;
+        if (v + nthreads < nwords) load_word(v + nthreads, fn);
         // largest |x| of the chunk, +inf when any entry is not finite
         float m = 0.f;
         bool finite = true;

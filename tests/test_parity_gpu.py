@@ -338,6 +338,20 @@ def test_token_batch_ragged_shapes(smoe, dev, d_model, d_ff, group, T):
     check(Y, ref, a, f"batch {d_model}/{d_ff} g{group} T={T}")
 
 
+@pytest.mark.parametrize("bits,T", [(4, 2), (4, 5), (4, 8), (4, 9), (2, 4), (2, 8)])
+def test_token_batch_slots(smoe, dev, bits, T):
+    """2 to 8 tokens run as one decode slot per token (the grouped decode
+    kernels sharing the expert's weights); 9 tokens go to the tensor cores."""
+    d_model, d_ff, group = 4096, 1536, 64
+    e = inp.expert(bits, d_model, d_ff, group, 17, 0)
+    X = inp.activations((T, d_model), 17)
+    Y = _batch(smoe, dev, T, e, X, d_model, d_ff, group, bits=bits)
+    _, y_ref, y_abs = oracle.ffn_batch(bits, e["gate_codes"], e["gate_scales"], e["up_codes"], e["up_scales"],
+                                       e["down_codes"], e["down_scales"], T, d_model, d_ff, group,
+                                       X.astype(np.float64))
+    check(Y, y_ref, y_abs, f"Q{bits} batch of {T} tokens")
+
+
 @pytest.mark.parametrize("T", [1, 2, 16, 64, 100, 256])
 def test_token_batch_q2(smoe, dev, T):
     """Q2 codes through the same tiles: eight K tiles per code chunk, and the
