@@ -246,7 +246,6 @@ QGKernelFn qgemv_reg_kernel(int bits, int nmat, int L, int cpl, int rpt)
         return bits == 4 ? pick_l<4, 2, 1>(L, cpl) : pick_l<2, 2, 1>(L, cpl);
     }
     if (rpt == 1) return bits == 4 ? pick_l<4, 1, 1>(L, cpl) : pick_l<2, 1, 1>(L, cpl);
-    if (rpt == 2) return bits == 4 ? pick_l<4, 1, 2>(L, cpl) : pick_l<2, 1, 2>(L, cpl);
     return nullptr;
 }
 

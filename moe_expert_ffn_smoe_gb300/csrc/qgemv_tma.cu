@@ -338,13 +338,16 @@ cudaError_t launch_tma(QGArgs &a, int n_experts, cudaStream_t stream, bool *unsu
     }
     // Register-digit kernel when a lane's share of the row is at most
     // reg_kernel_max_cpl(BITS) chunks: the largest team (L) that divides KC.
+    // One row per team and stage: the 8-expert down projection (4.5 stages
+    // per warp with two rows) took 8.1 us, with one row 7.4 us (finer
+    // stages even out the warps' last stages).
     int rl = 0;
     for (int l = 32; l >= 8; l >>= 1)
         if (KC % l == 0 && KC / l <= reg_kernel_max_cpl(BITS)) {
             rl = l;
             break;
         }
-    if (rl != 0 && a.scales_tma && pick_config<BITS, NMAT>(a, 32 / rl, max_units, dev->max_smem_optin, 12, NMAT == 2 ? 1 : 2, &cfg,
+    if (rl != 0 && a.scales_tma && pick_config<BITS, NMAT>(a, 32 / rl, max_units, dev->max_smem_optin, 12, 1, &cfg,
                                            &a.stage_bytes, &a.off_slots, &smem)) {
         QGKernelFn rk = qgemv_reg_kernel(BITS, NMAT, rl, KC / rl, cfg.rpt);
         if (rk) {
