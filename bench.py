@@ -437,21 +437,27 @@ def gpu_arm(args, rank, world, local):
     out_host = torch.empty((N_EXPERTS, D_MODEL)).pin_memory()
     h2d, d2h = D_MODEL * 4, N_EXPERTS * D_MODEL * 4
 
-    # (1) through the library's SM copies (smoe_copy): one CUDA graph per
-    # weight copy holds the whole step, copy in, the two grouped calls, copy out
+    # (1) one CUDA graph per weight copy holds the whole step: smoe_copy of
+    # the token into device memory (every CTA of gate/up reads it), the two
+    # grouped calls, the down projection writing its outputs straight into
+    # the pinned host buffer (each output crosses the host link once)
+    def e2e_body(c, s):
+        ex = wl.copies[c]
+        smoe.smoe_copy(wl.x, x_host, h2d, stream=s)
+        wl.g_gate_up([t["gate_codes"] for t in ex], [t["gate_scales"] for t in ex], [t["up_codes"] for t in ex],
+                     [t["up_scales"] for t in ex], wl.x, wl.hidden, D_FF, D_MODEL, GROUP, stream=s)
+        wl.g_down([t["down_codes"] for t in ex], [t["down_scales"] for t in ex], wl.hidden, out_host,
+                  D_MODEL, D_FF, GROUP, stream=s)
+
     with torch.cuda.stream(wl.stream):
         for c in range(len(wl.copies)):
-            smoe.smoe_copy(wl.x, x_host, h2d, stream=wl.stream)
-            wl.calls(c, wl.stream)
-            smoe.smoe_copy(out_host, wl.out, d2h, stream=wl.stream)
+            e2e_body(c, wl.stream)
     wl.stream.synchronize()
     e2e_graphs = []
     for c in range(len(wl.copies)):
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=wl.stream, capture_error_mode="thread_local"):
-            smoe.smoe_copy(wl.x, x_host, h2d, stream=wl.stream)
-            wl.calls(c, wl.stream)
-            smoe.smoe_copy(out_host, wl.out, d2h, stream=wl.stream)
+            e2e_body(c, wl.stream)
         e2e_graphs.append(g)
 
     def e2e_steps(k):
@@ -469,6 +475,14 @@ def gpu_arm(args, rank, world, local):
     with torch.cuda.stream(wl.stream):
         e2e_steps(3)
         t_e2e = time_steps(e2e_steps, e2e_n, wl.stream)
+        # the last step's outputs, written to host memory by the down
+        # projection, against the same step computed into device memory
+        torch.cuda.synchronize()
+        host_out = out_host.clone()
+        wl.calls((e2e_n - 1) % len(wl.copies), wl.stream)
+        torch.cuda.synchronize()
+        if not torch.equal(host_out, wl.out.cpu()):
+            raise RuntimeError("end-to-end step: the outputs written to host memory differ from the device's")
         e2e_ce_steps(3)
         t_ce = time_steps(e2e_ce_steps, e2e_n, wl.stream)
     t_e2e = max_over_ranks(t_e2e, world, dev)
@@ -480,8 +494,8 @@ def gpu_arm(args, rank, world, local):
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
            "us_per_step": round(t_e2e / e2e_n * 1e6, 3),
            "launch": "one CUDA graph replay per step: smoe_copy of the token from pinned host memory, "
-                     "the 2 grouped C-ABI calls, smoe_copy of the outputs to pinned host memory (copies "
-                     "by the SMs over the host link, chained with programmatic dependent launch)",
+                     "the 2 grouped C-ABI calls, the down projection writing the outputs straight into "
+                     "pinned host memory (over the host link, chained with programmatic dependent launch)",
            "copy_engine": {"us_per_step": round(t_ce / e2e_n * 1e6, 3),
                            "launch": "per step: cudaMemcpyAsync in, one graph replay, cudaMemcpyAsync out"}}
 
@@ -751,10 +765,10 @@ def routed_layer_row(smoe, dev, steps, out, s, n=128, k=N_EXPERTS, ntok=16):
     eo = torch.empty((k, D_MODEL), device=dev)
     y = torch.empty(D_MODEL, device=dev)
 
-    def layer(x):
+    def layer(x, out=None):
         smoe.smoe_route_topk_bf16(gate, x, n, D_MODEL, k, logits, idx, w, stream=s)
         smoe.smoe_experts_ffn_routed_q4(n, k, *tabs, idx, x, eo, D_MODEL, D_FF, GROUP, ws, wsb, stream=s)
-        smoe.smoe_combine(k, eo, w, y, D_MODEL, stream=s)
+        smoe.smoe_combine(k, eo, w, y if out is None else out, D_MODEL, stream=s)
 
     with torch.cuda.stream(s):
         for i in range(ntok):
@@ -771,15 +785,15 @@ def routed_layer_row(smoe, dev, steps, out, s, n=128, k=N_EXPERTS, ntok=16):
     per = t / (reps * ntok)
     layer_bytes = n * D_MODEL * 2 + D_MODEL * 4 + k * expert_bytes(4, D_MODEL, D_FF, GROUP) + k * D_MODEL * 4 \
         + D_MODEL * 4
-    # end to end: token in from pinned host memory, output back to it
+    # end to end: token in from pinned host memory (smoe_copy), the combine
+    # writing the layer output straight into pinned host memory
     x_host = torch.from_numpy(inp.activations(D_MODEL, 13)).pin_memory()
     y_host = torch.empty(D_MODEL).pin_memory()
     xd = torch.empty(D_MODEL, device=dev)
 
     def e2e_body():
         smoe.smoe_copy(xd, x_host, D_MODEL * 4, stream=s)
-        layer(xd)
-        smoe.smoe_copy(y_host, y, D_MODEL * 4, stream=s)
+        layer(xd, y_host)
 
     with torch.cuda.stream(s):
         e2e_body()
@@ -792,13 +806,17 @@ def routed_layer_row(smoe, dev, steps, out, s, n=128, k=N_EXPERTS, ntok=16):
         ge.replay()
         te = time_steps(lambda r: [ge.replay() for _ in range(r)], ne, s)
     torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        layer(xd)  # the same token's layer into device memory
+    torch.cuda.synchronize()
     if not torch.equal(y_host, y.cpu()):
-        raise RuntimeError("routed layer: the output copied to host memory differs from the device's")
+        raise RuntimeError("routed layer: the output written to host memory differs from the device's")
     out[f"moe_layer_routed_{n}e_top{k}"] = {
         "us_per_layer": round(per * 1e6, 3), "GB/s": round(layer_bytes / per / 1e9, 1),
         "bytes_per_layer": layer_bytes, "launches_per_layer": 6,
         "e2e": {"us_per_layer": round(te / ne * 1e6, 3), "h2d_bytes": D_MODEL * 4, "d2h_bytes": D_MODEL * 4,
-                "launch": "one graph replay per token: smoe_copy in, route, routed FFN, combine, smoe_copy out"},
+                "launch": "one graph replay per token: smoe_copy in, route, routed FFN, combine into pinned "
+                          "host memory"},
         "how": f"{ntok} layers on {ntok} tokens in one CUDA graph, {reps} replays, stream held; "
                f"{n} experts x {D_FF}x{D_MODEL} Q4 resident ({n * expert_bytes(4, D_MODEL, D_FF, GROUP) / 1e9:.2f} GB)"}
     del ex, tabs

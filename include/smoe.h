@@ -14,7 +14,12 @@
  *   query functions and the two buffers of smoe_copy (which may also be
  *   pinned host memory) is a DEVICE pointer owned by the caller.  The library
  *   allocates no memory of its own on any call and keeps no pointer after the
- *   call returns.
+ *   call returns.  An OUTPUT (out, y, hidden, top_idx, ...) may also be
+ *   page-locked host memory mapped into the device's address space (unified
+ *   addressing, e.g. cudaHostAlloc or torch's pin_memory on a node whose GPU
+ *   reaches host memory over a coherent link): the kernels then write each
+ *   result over the host link once, with no copy afterwards.  Inputs must be
+ *   device memory (weights, tokens and hidden vectors are read by many CTAs).
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = the legacy
  *   default stream).  Calls enqueue their kernels on it and return at once;
  *   results are ready when the stream's work has completed.  Kernels are

@@ -59,3 +59,40 @@ def test_copy_tail_is_untouched(smoe):
     torch.cuda.synchronize()
     assert torch.equal(dst[:1000], src[:1000])
     assert (dst[1000:] == 7).all()
+
+
+def test_outputs_written_straight_into_pinned_host_memory(smoe):
+    """Outputs may be page-locked host memory the device addresses: the
+    kernels write them over the host link, bit for bit what they write into
+    device memory (grouped down, single down, combine, bf16 matvec)."""
+    import smoe_inputs as inp
+    dev = torch.device("cuda:0")
+    d_model, d_ff, group, n = 1024, 512, 64, 3
+    ex = [{k: torch.from_numpy(v).to(dev) for k, v in inp.expert(4, d_model, d_ff, group, 51, e).items()}
+          for e in range(n)]
+    h = torch.from_numpy(inp.activations((n, d_ff), 52)).to(dev)
+    out_dev = torch.empty((n, d_model), device=dev)
+    out_host = torch.full((n, d_model), float("nan")).pin_memory()
+    args = ([t["down_codes"] for t in ex], [t["down_scales"] for t in ex], h)
+    smoe.smoe_experts_down_q4(*args, out_dev, d_model, d_ff, group)
+    smoe.smoe_experts_down_q4(*args, out_host, d_model, d_ff, group)
+    one_dev = torch.empty(d_model, device=dev)
+    one_host = torch.full((d_model,), float("nan")).pin_memory()
+    smoe.smoe_down_q4(ex[0]["down_codes"], ex[0]["down_scales"], h[0], one_dev, d_model, d_ff, group)
+    smoe.smoe_down_q4(ex[0]["down_codes"], ex[0]["down_scales"], h[0], one_host, d_model, d_ff, group)
+    w = torch.tensor([0.5, 0.3, 0.2], device=dev)
+    comb_dev = torch.empty(d_model, device=dev)
+    comb_host = torch.full((d_model,), float("nan")).pin_memory()
+    smoe.smoe_combine(n, out_dev, w, comb_dev, d_model)
+    smoe.smoe_combine(n, out_dev, w, comb_host, d_model)
+    wb = torch.from_numpy(inp.bf16_rows(64, 512, 53, 1).view(np.int16)).to(dev)
+    xb = torch.from_numpy(inp.activations(512, 53)).to(dev)
+    mv_dev = torch.empty(64, device=dev)
+    mv_host = torch.full((64,), float("nan")).pin_memory()
+    smoe.matvec_bf16(wb, xb, mv_dev, 64, 512)
+    smoe.matvec_bf16(wb, xb, mv_host, 64, 512)
+    torch.cuda.synchronize()
+    assert torch.equal(out_host, out_dev.cpu())
+    assert torch.equal(one_host, one_dev.cpu())
+    assert torch.equal(comb_host, comb_dev.cpu())
+    assert torch.equal(mv_host, mv_dev.cpu())
