@@ -17,7 +17,7 @@ rows of the hot path (Q2 decode, bf16 matvec shapes, token batch, the small
 256/256 expert) each timed the same way.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--no-rows] [--no-cpu] [--rows PATTERN]
+                  [--no-rows] [--no-cpu] [--rows PATTERN] [--rows-only]
 """
 import argparse
 import hashlib
@@ -571,6 +571,9 @@ def rows_breakdown(smoe, dev, steps, pattern=""):
         experts_batch_row(smoe, dev, steps, out, hbm_peak, timed, s)
     if pattern in "route_128x4096_top8":
         route_row(smoe, dev, steps, out, timed, s)
+    for bits in (4, 2):
+        if pattern in f"q{bits}_gate_up_38experts_sustained":
+            sustained_row(smoe, dev, steps, out, hbm_peak, bits)
     if pattern in "moe_layer_routed_128e_top8":
         routed_layer_row(smoe, dev, steps, out, s)
     if pattern in "q4_ffn_256":
@@ -823,6 +826,29 @@ def routed_layer_row(smoe, dev, steps, out, s, n=128, k=N_EXPERTS, ntok=16):
     torch.cuda.empty_cache()
 
 
+def sustained_row(smoe, dev, steps, out, hbm_peak, bits=4, n=38):
+    """The grouped gate/up kernel over n experts in one launch (n = 38: four
+    CTAs per expert, 384 rows each, about 32 stages per warp), so that the
+    launch's ramp and tail are a small part of it: the kernel's streaming
+    rate in steady state.  Two weight copies alternate (> 2 x L2)."""
+    import torch
+    ncp = 2
+    sets = [[{k: torch.from_numpy(v).to(dev) for k, v in inp.expert(bits, D_MODEL, D_FF, GROUP, 13 + 1000 * c, e).items()
+              if k.startswith(("gate", "up"))} for e in range(n)] for c in range(ncp)]
+    x = torch.from_numpy(inp.activations(D_MODEL, 13)).to(dev)
+    hid = torch.empty((n, D_FF), device=dev)
+    fn = smoe.smoe_experts_gate_up_q4 if bits == 4 else smoe.smoe_experts_gate_up_q2
+    st = torch.cuda.Stream(device=dev)
+    ptrs = [[[t[k] for t in ex] for k in ("gate_codes", "gate_scales", "up_codes", "up_scales")] for ex in sets]
+    t = kernel_chain_seconds(lambda i: fn(*ptrs[i % ncp], x, hid, D_FF, D_MODEL, GROUP, stream=st), 4, st)
+    b = n * 2 * q_bytes(bits, D_FF, D_MODEL, GROUP) + D_MODEL * 4 + n * D_FF * 4
+    out[f"q{bits}_gate_up_{n}experts_sustained"] = {"us_per_launch": round(t * 1e6, 3), "GB/s": round(b / t / 1e9, 1),
+                                                   "frac": round(b / t / 1e9 / hbm_peak, 4),
+                                                   "bytes_per_launch": b}
+    del sets
+    torch.cuda.empty_cache()
+
+
 def small_row(smoe, dev, steps, out, timed, s):
     """The small 256/256 expert (latency bound)."""
     import torch
@@ -932,6 +958,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--rows", default="", help="run only the breakdown rows whose name contains this")
+    ap.add_argument("--rows-only", action="store_true",
+                    help="run only the breakdown rows (no headline step): for profiling one row's kernels")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -943,6 +971,16 @@ def main():
             print(json.dumps(res), flush=True)
         return
     rank, world, local = dist_setup()
+    if args.rows_only:
+        import torch
+        import __graft_entry__
+        __graft_entry__.build_library()
+        import moe_expert_ffn_smoe_gb300 as smoe
+        dev = torch.device(f"cuda:{local}")
+        torch.cuda.set_device(dev)
+        if rank == 0:
+            print(json.dumps({"rows": rows_breakdown(smoe, dev, args.steps, args.rows)}), flush=True)
+        return
 
     res, wl, smoe, dev = gpu_arm(args, rank, world, local)
     if rank == 0 and world == 1 and not args.no_cpu:
