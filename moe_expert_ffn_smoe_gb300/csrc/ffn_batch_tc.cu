@@ -25,11 +25,12 @@
 //  * Each 64-column tile's accumulator is read back from TMEM and added to
 //    per-thread f32 sums with the tile's scale.  TMEM holds several tiles'
 //    accumulators, so the MMAs run ahead of the epilogue.
-//  * Token tiles of 64 or 128: A goes through shared memory (canonical
-//    no-swizzle K-major layout, proxy fence) and TMEM holds four
-//    accumulators.  Token tiles of 16 or 32: A goes straight into TMEM
-//    (tcgen05.st; 8 stages after 256 columns of accumulators, or 4 after 128
-//    when two CTAs share an SM) and the MMAs read it there.
+//  * Token tiles of 64: A goes through shared memory (canonical no-swizzle
+//    K-major layout, proxy fence) and TMEM holds four accumulators.  Token
+//    tiles of 16, 32 and 128: A goes straight into TMEM (tcgen05.st; up to 8
+//    stages after 256 columns of accumulators, or 4 after 128 when two CTAs
+//    share an SM) and the MMAs read it there, which leaves shared memory
+//    to the token blocks (five stages of 128 tokens instead of three).
 //
 // Three launches per call, chained with programmatic dependent launch:
 //  1. prep_tokens: X -> B blocks (hi, lo per (token tile, K tile)).
@@ -45,8 +46,8 @@
 //     way; each split writes Y for its token columns.
 // Inside a GEMM CTA (608 threads): warps 0-7 epilogue (warp w reads TMEM
 // lane quarter w % 4 = 32 tile rows, columns of half w / 4), warps 8-15
-// convert codes to A tiles (thread = half a tile row: 4 of its 8 Q4 code
-// words, 2 of its 4 Q2 words), warp 16 issues the MMAs, warp 17 streams code
+// convert codes to A tiles in two groups of four that take alternate K
+// tiles (thread = one tile row), warp 16 issues the MMAs, warp 17 streams code
 // chunks with 2-D tensor copies (TMA, 128-byte swizzle: 128 bytes x 64 or
 // 128 rows per chunk), warp 18 streams the token B blocks with bulk copies.
 // Two converter and two epilogue warps per SM sub-partition keep those
@@ -107,15 +108,16 @@ __host__ __device__ constexpr int acc_cols(int nt) { return hilo_shared(nt) ? nt
 // the MMAs of later K tiles rarely wait for the epilogue.
 __host__ __device__ constexpr int accbufs_for(int nt) { return 512 / acc_cols(nt) < 16 ? 512 / acc_cols(nt) : 16; }
 
-// Token tiles of at most 32: the converters store A straight into tensor
-// memory (stages of 32 columns after the accumulators), so a K tile's A
-// makes no round trip through shared memory.  Such a CTA takes all 512
-// columns (256 of accumulators, 8 A stages) and holds an SM alone; with
+// Token tiles of at most 32, and of 128: the converters store A straight
+// into tensor memory (stages of 32 columns after the accumulators), so a K
+// tile's A makes no round trip through shared memory and the MMAs read only
+// the token block there.  Such a CTA takes all 512 columns (256 of
+// accumulators, up to 8 A stages) and holds an SM alone; with
 // tiles of 16 and more tiles than SMs, a CTA takes 256 (128 of
 // accumulators, 4 A stages) so that two share an SM (`two`): two CTAs per
 // SM give each a slower K loop, so this pays only where the tiles would
 // otherwise run in more waves.
-__host__ __device__ constexpr bool a_in_tmem(int nt) { return nt <= 32; }
+__host__ __device__ constexpr bool a_in_tmem(int nt) { return nt <= 32 || nt == 128; }
 __host__ __device__ constexpr uint32_t a_tmem_col0(bool two) { return two ? 128u : 256u; }
 __host__ __device__ constexpr int tc_accbufs(int nt, bool two)
 {
@@ -123,11 +125,17 @@ __host__ __device__ constexpr int tc_accbufs(int nt, bool two)
                                 ? static_cast<int>(a_tmem_col0(two)) / acc_cols(nt) : 8)
                          : accbufs_for(nt);
 }
+__host__ __device__ constexpr uint32_t tc_stage_bytes(int nt) { return a_in_tmem(nt) ? round1024(b_bytes(nt)) : stage_bytes(nt); }
+constexpr size_t kTcAtmSmemBudget = 224 * 1024;
 __host__ __device__ constexpr int tc_stages(int nt, bool two)
 {
-    return a_in_tmem(nt) ? (two ? 4 : 8) : stages_for(nt);
+    return a_in_tmem(nt)
+               ? (two ? 4
+                      : ((kTcAtmSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / tc_stage_bytes(nt) < 8
+                             ? static_cast<int>((kTcAtmSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / tc_stage_bytes(nt))
+                             : 8))
+               : stages_for(nt);
 }
-__host__ __device__ constexpr uint32_t tc_stage_bytes(int nt) { return a_in_tmem(nt) ? round1024(b_bytes(nt)) : stage_bytes(nt); }
 
 // Byte offset of (row, 8-column block k8) in a [rows x 64] bf16 tile laid out
 // as 8x8 core matrices: core (row/8, k8) at ((row/8)*8 + k8)*128, row%8 at 16*(row%8).
@@ -545,7 +553,7 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
             mbar_init(cempty0 + 8 * c, CONV_WARPS);
         }
         for (int s = 0; s < S; ++s) {
-            mbar_init(full0 + 8 * s, CONV_WARPS + 1);
+            mbar_init(full0 + 8 * s, CONV_WARPS / 2 + 1);  // one converter group + the token block
             mbar_init(empty0 + 8 * s, 1);
         }
         for (int b = 0; b < NB; ++b) {
@@ -656,86 +664,93 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
             }
         }
     } else if (warp >= CONV_WARP0) {
-        // ---- codes -> A tiles: thread (r, hf) converts words 4 hf .. 4 hf + 3
-        // (8-column blocks k8 = 4 hf .. 4 hf + 3) of tile row r
+        // ---- codes -> A tiles.  The converter warps form two groups of four
+        // (each group covers the 128 tile rows, i.e. all four TMEM lane
+        // quarters); group g converts the K tiles i with i % 2 == g, so two
+        // tiles are in conversion at once (one group of eight warps on one
+        // tile at a time paced the K loop: 0.3-0.4 us of conversion latency
+        // per tile).  Thread (g, r) converts the whole tile row r.
         const int ct = threadIdx.x - CONV_WARP0 * 32;
-        const int r = ct & (MT - 1), hf = ct >> 7;
+        const int r = ct & (MT - 1), grp = ct >> 7;
         const uint32_t rsw = static_cast<uint32_t>(r & 7);  // 128-byte swizzle of the chunk rows
-        // K tile i: tile `sub` of the chunk in code slot `slot` (fill parity
-        // cpar), stage s (round parity spar); counters instead of divisions
-        int sub = 0, slot = 0, s = 0;
-        uint32_t cpar = 0, spar = 0;
-        for (int i = 0; i < nk; ++i) {
-            if ((sub == 0 && !mbar_wait_bounded(cfull0 + 8 * slot, cpar, a.status, 5u)) ||
+        for (int i = grp; i < nk; i += 2) {
+            // K tile i: tile `sub` of chunk c in code slot `slot` (fill
+            // parity cpar), stage s (round parity spar)
+            const int c = i / CHUNK_KT, sub = i - c * CHUNK_KT;
+            const int slot = c % CODE_SLOTS;
+            const uint32_t cpar = static_cast<uint32_t>(c / CODE_SLOTS) & 1u;
+            const int s = i % S;
+            const uint32_t spar = static_cast<uint32_t>(i / S) & 1u;
+            // the group's first tile of a chunk waits for the chunk (chunks
+            // start at even tiles: that tile is sub == grp)
+            if ((sub == grp && !mbar_wait_bounded(cfull0 + 8 * slot, cpar, a.status, 5u)) ||
                 (i >= S && !mbar_wait_bounded(empty0 + 8 * s, spar ^ 1u, a.status, 5u))) {
                 failed = true;
                 break;
             }
             const uint32_t row = codes0 + slot * CHUNK_BYTES + static_cast<uint32_t>(r) * 128u;
             const uint32_t sa = stage0 + s * SB;
-            if (ATM) {
-                // this thread's 16 columns (32 bf16) of tile row r, in the
-                // K order of the B operand, straight into tensor memory
-                uint32_t v[16];
-                if (BITS == 4) {
+            if (ATM) tc_fence_after();  // after the wait for the MMA that last read this stage
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf) {
+                if (ATM) {
+                    // 16 columns (32 bf16) of tile row r, in the K order of
+                    // the B operand, straight into tensor memory
+                    uint32_t v[16];
+                    if (BITS == 4) {
+                        const uint4 w = lds128v(row + (((2u * sub + static_cast<uint32_t>(hf)) ^ rsw) << 4));
+                        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 cv = q4_word_to_bf16(words[q]);
+                            v[4 * q] = cv.x; v[4 * q + 1] = cv.y; v[4 * q + 2] = cv.z; v[4 * q + 3] = cv.w;
+                        }
+                    } else {
+                        const uint2 w = lds64v(row + ((static_cast<uint32_t>(sub) ^ rsw) << 4) + 8u * hf);
+                        const uint32_t words[2] = {w.x, w.y};
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            uint4 lo, hi;
+                            q2_word_to_bf16(words[q], lo, hi);
+                            v[8 * q] = lo.x; v[8 * q + 1] = lo.y; v[8 * q + 2] = lo.z; v[8 * q + 3] = lo.w;
+                            v[8 * q + 4] = hi.x; v[8 * q + 5] = hi.y; v[8 * q + 6] = hi.z; v[8 * q + 7] = hi.w;
+                        }
+                    }
+                    tmem_st16(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + ACOL0 +
+                                  static_cast<uint32_t>(s * 32 + 16 * hf),
+                              v);
+                } else if (BITS == 4) {
+                    // 16-byte unit 2 sub + hf of the (swizzled) chunk row: 4 words, one block each
                     const uint4 w = lds128v(row + (((2u * sub + static_cast<uint32_t>(hf)) ^ rsw) << 4));
                     const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const uint4 c = q4_word_to_bf16(words[q]);
-                        v[4 * q] = c.x; v[4 * q + 1] = c.y; v[4 * q + 2] = c.z; v[4 * q + 3] = c.w;
-                    }
+                    for (int j = 0; j < 4; ++j) sts128(sa + core_off(r, 4 * hf + j), q4_word_to_bf16(words[j]));
                 } else {
+                    // half hf of 16-byte unit sub: 2 words, two blocks each
                     const uint2 w = lds64v(row + ((static_cast<uint32_t>(sub) ^ rsw) << 4) + 8u * hf);
                     const uint32_t words[2] = {w.x, w.y};
 #pragma unroll
-                    for (int q = 0; q < 2; ++q) {
+                    for (int j = 0; j < 2; ++j) {
                         uint4 lo, hi;
-                        q2_word_to_bf16(words[q], lo, hi);
-                        v[8 * q] = lo.x; v[8 * q + 1] = lo.y; v[8 * q + 2] = lo.z; v[8 * q + 3] = lo.w;
-                        v[8 * q + 4] = hi.x; v[8 * q + 5] = hi.y; v[8 * q + 6] = hi.z; v[8 * q + 7] = hi.w;
+                        q2_word_to_bf16(words[j], lo, hi);
+                        sts128(sa + core_off(r, 4 * hf + 2 * j), lo);
+                        sts128(sa + core_off(r, 4 * hf + 2 * j + 1), hi);
                     }
                 }
-                tc_fence_after();  // after the wait for the MMA that last read this stage
-                tmem_st16(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + ACOL0 +
-                              static_cast<uint32_t>(s * 32 + 16 * hf),
-                          v);
+            }
+            if (ATM) {
                 tmem_wait_st();
                 tc_fence_before();
-            } else if (BITS == 4) {
-                // 16-byte unit 2 sub + hf of the (swizzled) chunk row: 4 words, one block each
-                const uint4 w = lds128v(row + (((2u * sub + static_cast<uint32_t>(hf)) ^ rsw) << 4));
-                const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) sts128(sa + core_off(r, 4 * hf + j), q4_word_to_bf16(words[j]));
             } else {
-                // half hf of 16-byte unit sub: 2 words, two blocks each
-                const uint2 w = lds64v(row + ((static_cast<uint32_t>(sub) ^ rsw) << 4) + 8u * hf);
-                const uint32_t words[2] = {w.x, w.y};
-#pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                    uint4 lo, hi;
-                    q2_word_to_bf16(words[j], lo, hi);
-                    sts128(sa + core_off(r, 4 * hf + 2 * j), lo);
-                    sts128(sa + core_off(r, 4 * hf + 2 * j + 1), hi);
-                }
+                fence_proxy_async_smem();
             }
-            if (!ATM) fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(full0 + 8 * s);
-                if (sub == CHUNK_KT - 1 || i == nk - 1) mbar_arrive(cempty0 + 8 * slot);
-            }
-            if (++s == S) {
-                s = 0;
-                spar ^= 1u;
-            }
-            if (++sub == CHUNK_KT) {
-                sub = 0;
-                if (++slot == CODE_SLOTS) {
-                    slot = 0;
-                    cpar ^= 1u;
-                }
+                // the group's last tile of the chunk releases the code slot
+                // (a group without a tile in the final chunk never arrives
+                // there; nothing waits for that slot again)
+                if (sub + 2 >= CHUNK_KT || i + 2 >= nk) mbar_arrive(cempty0 + 8 * slot);
             }
         }
     } else {
