@@ -78,10 +78,11 @@ constexpr int CODE_SLOTS = 3;
 constexpr int EPI_WARPS = 8;
 constexpr int CONV_WARPS = 8;
 constexpr int CONV_WARP0 = 8;
-constexpr int MMA_WARP = 16;
+constexpr int MMA_WARP = 16;    // issues the MMAs of even K tiles (and owns the TMEM allocation)
 constexpr int CODE_WARP = 17;
 constexpr int BPROD_WARP = 18;
-constexpr int TC_THREADS = 19 * 32;
+constexpr int MMA_WARP2 = 19;   // issues the MMAs of odd K tiles
+constexpr int TC_THREADS = 20 * 32;
 constexpr uint32_t A_BYTES = MT * KT * 2;
 // A holds (c - Z) / DEN exactly (DEN = 16 at Q4, 4 at Q2), so per group
 // sum w x = s (DEN / Z) sum A x: FOLD = DEN / Z.
@@ -94,11 +95,14 @@ constexpr int TC_MAX_EXPERTS = 32;  // experts per launch (grouped token batch)
 __host__ __device__ constexpr uint32_t b_bytes(int nt) { return static_cast<uint32_t>(nt) * 256u; }
 __host__ __device__ constexpr uint32_t round1024(uint32_t v) { return (v + 1023u) & ~1023u; }
 __host__ __device__ constexpr uint32_t stage_bytes(int nt) { return round1024(A_BYTES + b_bytes(nt)); }
+// Stage and accumulator-buffer counts are even: K tiles i and i + S (or
+// i + NB) then always belong to the same MMA issuer and converter group, so
+// every barrier phase has one in-order waiter.
 __host__ __device__ constexpr int stages_for(int nt)
 {
-    return static_cast<int>((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / stage_bytes(nt)) < 8
-               ? static_cast<int>((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / stage_bytes(nt))
-               : 8;
+    return (static_cast<int>((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / stage_bytes(nt)) < 8
+                ? static_cast<int>((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / stage_bytes(nt))
+                : 8) & ~1;
 }
 // hi and lo accumulated into the same columns (token tiles of 128)
 __host__ __device__ constexpr bool hilo_shared(int nt) { return nt == 128; }
@@ -133,7 +137,7 @@ __host__ __device__ constexpr int tc_stages(int nt, bool two)
                ? (two ? 4
                       : ((kTcAtmSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / tc_stage_bytes(nt) < 8
                              ? static_cast<int>((kTcAtmSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / tc_stage_bytes(nt))
-                             : 8))
+                             : 8) & ~1)
                : stages_for(nt);
 }
 
@@ -514,6 +518,8 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
     constexpr int TILE_BYTES = KT * BITS / 8;  // bytes of one row's codes per K tile
     constexpr bool ATM = a_in_tmem(NT);
     static_assert(!TWO || NT == 16, "two CTAs per SM only with 16-token tiles");
+    static_assert(tc_stages(NT, TWO) % 2 == 0 && tc_accbufs(NT, TWO) % 2 == 0,
+                  "even stage and buffer counts: one waiter per barrier phase with two MMA issuers");
     constexpr int NB = tc_accbufs(NT, TWO);
     constexpr uint32_t ACOL0 = a_tmem_col0(TWO);  // first A stage column (ATM)
     constexpr bool HL = hilo_shared(NT);
@@ -622,14 +628,17 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                          full0 + 8 * s);
             }
         }
-    } else if (warp == MMA_WARP) {
-        // ---- MMA issue
+    } else if (warp == MMA_WARP || warp == MMA_WARP2) {
+        // ---- MMA issue: two issuing threads take alternate K tiles, so
+        // one's barrier waits and commits overlap the other's MMAs (one
+        // issuer spent more than half of each tile's time outside the MMAs)
         if (lane == 0) {
             const uint32_t idesc = instr_desc(MT, HL ? NT : 2 * NT);
             constexpr uint32_t LO = static_cast<uint32_t>(NT) * 128u;  // the lo rows of a token block
-            int s = 0, b = 0;
-            uint32_t spar = 0, bpar = 0;  // stage and accumulator buffer, round parities
-            for (int i = 0; i < nk; ++i, ++issued) {
+            const int i0 = warp == MMA_WARP ? 0 : 1;
+            for (int i = i0; i < nk; i += 2, ++issued) {
+                const int s = i % S, b = i % NB;
+                const uint32_t spar = static_cast<uint32_t>(i / S) & 1u, bpar = static_cast<uint32_t>(i / NB) & 1u;
                 if (!mbar_wait_bounded(full0 + 8 * s, spar, a.status, 3u) ||
                     (i >= NB && !mbar_wait_bounded(acce0 + 8 * b, bpar ^ 1u, a.status, 4u))) {
                     failed = true;
@@ -653,14 +662,6 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                 }
                 mma_commit(empty0 + 8 * s);
                 mma_commit(accf0 + 8 * b);
-                if (++s == S) {
-                    s = 0;
-                    spar ^= 1u;
-                }
-                if (++b == NB) {
-                    b = 0;
-                    bpar ^= 1u;
-                }
             }
         }
     } else if (warp >= CONV_WARP0) {
@@ -858,9 +859,10 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
             // only the producer's arrival and the chunk's bytes)
             for (int c = issued > CODE_SLOTS ? issued - CODE_SLOTS : 0; c < issued; ++c)
                 mbar_wait_bounded(cfull0 + 8 * (c % CODE_SLOTS), (c / CODE_SLOTS) & 1, nullptr, 0u);
-        } else if (lane == 0 && warp == MMA_WARP && issued > 0) {
-            // the commit of the last MMA group tracks every earlier one
-            const int i = issued - 1;
+        } else if (lane == 0 && (warp == MMA_WARP || warp == MMA_WARP2) && issued > 0) {
+            // the commit of this issuer's last MMA group tracks every
+            // earlier one it issued
+            const int i = (warp == MMA_WARP ? 0 : 1) + 2 * (issued - 1);
             mbar_wait_bounded(accf0 + 8 * (i % NB), (i / NB) & 1, nullptr, 0u);
         } else if (lane == 0 && warp == BPROD_WARP && issued > 0) {
             // token blocks share their stage's full barrier with the
