@@ -304,8 +304,10 @@ size_t smoe_ffn_batch_workspace_bytes(int T, int d_model, int d_ff, int group);
  * aligned, owned by the caller; its contents on entry do not matter and on
  * return are unspecified.  Two calls in flight at once need two workspaces.
  * The batch is not limited to the page's 64 tokens: any T >= 0 is accepted.
- * For larger T the contraction runs on the tensor cores (codes as exact bf16
- * integers, X split into two bf16 halves, f32 accumulation).
+ * T = 1 runs on the decode kernels, 2 <= T <= 6 as one decode slot per token
+ * (up to 8 where the tensor cores do not take the shape); larger T runs the
+ * contraction on the tensor cores (codes as exact bf16 integers, X split
+ * into two bf16 halves, f32 accumulation).
  */
 int ffn_batch_q4(const uint8_t *gate_codes, const float *gate_scales,
                  const uint8_t *up_codes, const float *up_scales,
@@ -320,7 +322,8 @@ int ffn_batch_q4(const uint8_t *gate_codes, const float *gate_scales,
  * smoe_gate_up_q2, Z = 1.5; d_model, d_ff and group multiples of 64 (the Q2
  * layout contract).  Same arguments, workspace size
  * (smoe_ffn_batch_workspace_bytes), checks and results as ffn_batch_q4;
- * T >= 2 runs on the tensor cores with A = (code - 1.5)/4 exact in bf16.
+ * the same paths by T, the tensor cores with A = (code - 1.5)/4 exact in
+ * bf16.
  */
 int ffn_batch_q2(const uint8_t *gate_codes, const float *gate_scales,
                  const uint8_t *up_codes, const float *up_scales,

@@ -3,8 +3,9 @@
 // every row of X [T x d_model], gate/up+SiLU into H [T x d_ff] (the caller's
 // workspace), then down into Y [T x d_model].
 //
-// Paths: one token goes through the decode kernels (qgemv.cu); 2 to 8
-// tokens go through the grouped decode kernels with one slot per token
+// Paths: one token goes through the decode kernels (qgemv.cu); 2 to 6
+// tokens (8 where the tensor cores do not take the shape) go through the
+// grouped decode kernels with one slot per token
 // (qgemv_tma.cu / qgemv_reg.cu) when both row lengths are whole multiples of
 // 8 chunks; more tokens go to the tensor cores (ffn_batch_tc.cu) when the
 // group size and both dimensions are multiples of 64; other shapes use the
@@ -207,16 +208,21 @@ namespace {
 // sharing the expert's weights (read from DRAM once, the other slots' reads
 // hit L2).  Below the measured crossover this is faster than the tensor
 // cores, whose per-call latency (token prep, first K tile, split-K finish)
-// does not shrink with T.
-constexpr int kSlotTokens = 8;
+// does not shrink with T: one expert at d_model 4096, d_ff 1536 took
+// 16.5 / 18.4 us (slots, T = 6 / 7) against 17.6 / 17.6 us (tensor cores).
+// Shapes the tensor cores do not take keep the slots up to kSlotTokensMax.
+constexpr int kSlotTokens = 6;
+constexpr int kSlotTokensMax = 8;
 
 // Shapes the grouped decode kernels take for both projections: rows of
 // whole multiples of 8 chunks of 16 bytes, at most 8192 columns.
-bool slot_path(int bits, int T, int d_model, int d_ff)
+bool slot_path(int bits, int T, int d_model, int d_ff, int group)
 {
     const int unit = bits == 4 ? 256 : 512;
-    return T >= 2 && T <= kSlotTokens && d_model > 0 && d_ff > 0 && d_model % unit == 0 && d_ff % unit == 0 &&
-           d_model <= 8192 && d_ff <= 8192;
+    if (T < 2 || T > kSlotTokensMax || d_model <= 0 || d_ff <= 0 || d_model % unit || d_ff % unit ||
+        d_model > 8192 || d_ff > 8192)
+        return false;
+    return T <= kSlotTokens || !tc_batch_supported(T, d_model, d_ff, group);
 }
 
 }  // namespace
@@ -251,10 +257,10 @@ cudaError_t launch_ffn_batch(int bits, const uint8_t *const gu_codes[2], const f
         if (e != cudaSuccess) return e;
         return launch_qgemv(bits, 1, dc, ds, H, Y, d_model, d_ff, group, stream);
     }
-    if (slot_path(bits, T, d_model, d_ff)) {
-        const uint8_t *c0[kSlotTokens], *c1[kSlotTokens];
-        const float *s0[kSlotTokens], *s1[kSlotTokens], *xs[kSlotTokens];
-        float *ys[kSlotTokens];
+    if (slot_path(bits, T, d_model, d_ff, group)) {
+        const uint8_t *c0[kSlotTokensMax], *c1[kSlotTokensMax];
+        const float *s0[kSlotTokensMax], *s1[kSlotTokensMax], *xs[kSlotTokensMax];
+        float *ys[kSlotTokensMax];
         for (int t = 0; t < T; ++t) {
             c0[t] = gu_codes[0];
             c1[t] = gu_codes[1];

@@ -327,6 +327,7 @@ def test_token_batch_small_shape_all_tokens(smoe, dev):
     (512, 256, 128, 70),   # groups of 128 columns: one scale per two K tiles
     (768, 384, 192, 40),   # groups of 192: three K tiles per scale, K splits starting mid-group
     (768, 384, 192, 16),   # the same with 16-token tiles (A in tensor memory)
+    (512, 256, 32, 8),     # groups of 32: no tensor-core path, 8 tokens stay on the decode slots
 ])
 def test_token_batch_ragged_shapes(smoe, dev, d_model, d_ff, group, T):
     e = inp.expert(4, d_model, d_ff, group, seed=31)
@@ -338,10 +339,10 @@ def test_token_batch_ragged_shapes(smoe, dev, d_model, d_ff, group, T):
     check(Y, ref, a, f"batch {d_model}/{d_ff} g{group} T={T}")
 
 
-@pytest.mark.parametrize("bits,T", [(4, 2), (4, 5), (4, 8), (4, 9), (2, 4), (2, 8)])
+@pytest.mark.parametrize("bits,T", [(4, 2), (4, 5), (4, 6), (4, 7), (4, 8), (2, 4), (2, 6), (2, 7)])
 def test_token_batch_slots(smoe, dev, bits, T):
-    """2 to 8 tokens run as one decode slot per token (the grouped decode
-    kernels sharing the expert's weights); 9 tokens go to the tensor cores."""
+    """2 to 6 tokens run as one decode slot per token (the grouped decode
+    kernels sharing the expert's weights); 7 and more go to the tensor cores."""
     d_model, d_ff, group = 4096, 1536, 64
     e = inp.expert(bits, d_model, d_ff, group, 17, 0)
     X = inp.activations((T, d_model), 17)
