@@ -552,6 +552,24 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
     const int nk = kt1 > kt0 ? kt1 - kt0 : 0;
     const int nchunks = (nk + CHUNK_KT - 1) / CHUNK_KT;
     const int ngroups = a.K / a.group;
+    // code chunk c into its slot (the weights never depend on an earlier kernel)
+    auto issue_chunk = [&](int c) {
+        const int slot = c % CODE_SLOTS;
+        const uint32_t dst = codes0 + slot * CHUNK_BYTES;
+        const int x = (kt0 + c * CHUNK_KT) * TILE_BYTES;  // byte offset along the row: multiple of 16
+        mbar_arrive_expect_tx(cfull0 + 8 * slot, CHUNK_BYTES);
+        if (GU) {
+            tma_load_2d(dst, &a.tmap[xe][0], x, mtile * 64, cfull0 + 8 * slot);
+            tma_load_2d(dst + CHUNK_BYTES / 2, &a.tmap[xe][1], x, mtile * 64, cfull0 + 8 * slot);
+        } else {
+            tma_load_2d(dst, &a.tmap[xe][0], x, mtile * MT, cfull0 + 8 * slot);
+        }
+    };
+    // the first CODE_SLOTS chunks go out as soon as their barriers exist,
+    // before the tensor-memory allocation and the block barrier (about half
+    // a microsecond earlier; the first chunk's DRAM latency is on every
+    // call's critical path)
+    const int early_chunks = nchunks < CODE_SLOTS ? nchunks : CODE_SLOTS;
 
     if (threadIdx.x == 0) {
         for (int c = 0; c < CODE_SLOTS; ++c) {
@@ -567,6 +585,7 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
             mbar_init(acce0 + 8 * b, EPI_WARPS);
         }
         fence_mbar_init();
+        for (int c = 0; c < early_chunks; ++c) issue_chunk(c);
     }
     if (warp == MMA_WARP) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(tslot), "r"(NCOLS)
@@ -594,22 +613,14 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
     if (warp == CODE_WARP) {
         // ---- code chunks (weights never depend on an earlier kernel)
         if (lane == 0) {
-            for (int c = 0; c < nchunks; ++c, ++issued) {
+            issued = early_chunks;  // issued by thread 0 with the barriers
+            for (int c = early_chunks; c < nchunks; ++c, ++issued) {
                 const int slot = c % CODE_SLOTS;
-                if (c >= CODE_SLOTS &&
-                    !mbar_wait_bounded(cempty0 + 8 * slot, ((c / CODE_SLOTS) - 1) & 1, a.status, 7u)) {
+                if (!mbar_wait_bounded(cempty0 + 8 * slot, ((c / CODE_SLOTS) - 1) & 1, a.status, 7u)) {
                     failed = true;
                     break;
                 }
-                const uint32_t dst = codes0 + slot * CHUNK_BYTES;
-                const int x = (kt0 + c * CHUNK_KT) * TILE_BYTES;  // byte offset along the row: multiple of 16
-                mbar_arrive_expect_tx(cfull0 + 8 * slot, CHUNK_BYTES);
-                if (GU) {
-                    tma_load_2d(dst, &a.tmap[xe][0], x, mtile * 64, cfull0 + 8 * slot);
-                    tma_load_2d(dst + CHUNK_BYTES / 2, &a.tmap[xe][1], x, mtile * 64, cfull0 + 8 * slot);
-                } else {
-                    tma_load_2d(dst, &a.tmap[xe][0], x, mtile * MT, cfull0 + 8 * slot);
-                }
+                issue_chunk(c);
             }
         }
     } else if (warp == BPROD_WARP) {
