@@ -361,6 +361,17 @@ __device__ __forceinline__ void cluster_sync()
     __syncwarp();
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+// The two halves of cluster_sync, for work that may run between them.
+__device__ __forceinline__ void cluster_arrive()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait()
+{
+    __syncwarp();
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t cluster_rank()
 {
@@ -942,6 +953,10 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                 }
             }
             __syncthreads();
+            // this CTA has read every split's partials: it arrives on the
+            // closing cluster barrier now and waits on it only before it
+            // exits, so the barrier's latency overlaps the finish below
+            cluster_arrive();
             if (GU) {
                 // SiLU(gate row c) * up row c for the rank's tokens, in place
                 for (int it = et; it < (n1 - n0) * 64; it += NTH) {
@@ -960,7 +975,7 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                 }
             }
         }
-        cluster_sync();  // no split leaves while another may still read its partials
+        cluster_wait();  // no split leaves while another may still read its partials
     }
     if (!GU && threadIdx.x == 0) pdl_launch_dependents();
     if (warp == MMA_WARP) {
