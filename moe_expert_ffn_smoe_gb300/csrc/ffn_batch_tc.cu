@@ -121,7 +121,7 @@ __host__ __device__ constexpr int accbufs_for(int nt) { return 512 / acc_cols(nt
 // accumulators, 4 A stages) so that two share an SM (`two`): two CTAs per
 // SM give each a slower K loop, so this pays only where the tiles would
 // otherwise run in more waves.
-__host__ __device__ constexpr bool a_in_tmem(int nt) { return nt <= 32 || nt == 128; }
+__host__ __device__ constexpr bool a_in_tmem(int nt) { return nt <= 32 || nt == 64 || nt == 128; }
 __host__ __device__ constexpr uint32_t a_tmem_col0(bool two) { return two ? 128u : 256u; }
 __host__ __device__ constexpr int tc_accbufs(int nt, bool two)
 {
