@@ -18,19 +18,17 @@
 //    lo = bf16(x - hi), stored as one operand of 2 NT rows (hi rows, then
 //    lo rows), x represented to about 2^-17 relative.  Token tiles of 128:
 //    per K step one MMA of N = 128 takes the hi rows and a second the lo
-//    rows, accumulating into the same 128 columns, so four accumulators fit
-//    in TMEM.  Smaller tiles: one MMA of N = 2 NT computes both halves into
+//    rows, accumulating into the same 128 columns, so an accumulator takes
+//    128 TMEM columns.  Smaller tiles: one MMA of N = 2 NT computes both halves into
 //    2 NT columns and the epilogue adds the hi and lo columns (two MMAs of a
 //    small N cost more than one of twice the N).
 //  * Each 64-column tile's accumulator is read back from TMEM and added to
 //    per-thread f32 sums with the tile's scale.  TMEM holds several tiles'
 //    accumulators, so the MMAs run ahead of the epilogue.
-//  * Token tiles of 64: A goes through shared memory (canonical no-swizzle
-//    K-major layout, proxy fence) and TMEM holds four accumulators.  Token
-//    tiles of 16, 32 and 128: A goes straight into TMEM (tcgen05.st; up to 8
-//    stages after 256 columns of accumulators, or 4 after 128 when two CTAs
-//    share an SM) and the MMAs read it there, which leaves shared memory
-//    to the token blocks (five stages of 128 tokens instead of three).
+//  * A goes straight into TMEM (tcgen05.st; up to 8 stages after 256
+//    columns of accumulators, or 4 after 128 when two CTAs share an SM) and
+//    the MMAs read it there, which leaves shared memory to the token blocks
+//    (the canonical no-swizzle K-major layout).
 //
 // Three launches per call, chained with programmatic dependent launch:
 //  1. prep_tokens: X -> B blocks (hi, lo per (token tile, K tile)).
@@ -83,62 +81,47 @@ constexpr int CODE_WARP = 17;
 constexpr int BPROD_WARP = 18;
 constexpr int MMA_WARP2 = 19;   // issues the MMAs of odd K tiles
 constexpr int TC_THREADS = 20 * 32;
-constexpr uint32_t A_BYTES = MT * KT * 2;
 // A holds (c - Z) / DEN exactly (DEN = 16 at Q4, 4 at Q2), so per group
 // sum w x = s (DEN / Z) sum A x: FOLD = DEN / Z.
 template <int BITS>
 constexpr float fold() { return BITS == 4 ? 16.0f / 7.5f : 4.0f / 1.5f; }
-constexpr size_t kTcSmemBudget = 200 * 1024;
 constexpr int TC_MAX_EXPERTS = 32;  // experts per launch (grouped token batch)
 
 // B block of one (token tile, K tile): hi [NT x 64] bf16, then lo.
 __host__ __device__ constexpr uint32_t b_bytes(int nt) { return static_cast<uint32_t>(nt) * 256u; }
 __host__ __device__ constexpr uint32_t round1024(uint32_t v) { return (v + 1023u) & ~1023u; }
-__host__ __device__ constexpr uint32_t stage_bytes(int nt) { return round1024(A_BYTES + b_bytes(nt)); }
-// Stage and accumulator-buffer counts are even: K tiles i and i + S (or
-// i + NB) then always belong to the same MMA issuer and converter group, so
-// every barrier phase has one in-order waiter.
-__host__ __device__ constexpr int stages_for(int nt)
-{
-    return (static_cast<int>((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / stage_bytes(nt)) < 8
-                ? static_cast<int>((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / stage_bytes(nt))
-                : 8) & ~1;
-}
 // hi and lo accumulated into the same columns (token tiles of 128)
 __host__ __device__ constexpr bool hilo_shared(int nt) { return nt == 128; }
 // TMEM columns of one accumulator
 __host__ __device__ constexpr int acc_cols(int nt) { return hilo_shared(nt) ? nt : 2 * nt; }
-// TMEM accumulator buffers: as many as fit in 512 columns (at most 16), so
-// the MMAs of later K tiles rarely wait for the epilogue.
-__host__ __device__ constexpr int accbufs_for(int nt) { return 512 / acc_cols(nt) < 16 ? 512 / acc_cols(nt) : 16; }
-
-// Token tiles of at most 32, and of 128: the converters store A straight
-// into tensor memory (stages of 32 columns after the accumulators), so a K
-// tile's A makes no round trip through shared memory and the MMAs read only
-// the token block there.  Such a CTA takes all 512 columns (256 of
-// accumulators, up to 8 A stages) and holds an SM alone; with
-// tiles of 16 and more tiles than SMs, a CTA takes 256 (128 of
-// accumulators, 4 A stages) so that two share an SM (`two`): two CTAs per
-// SM give each a slower K loop, so this pays only where the tiles would
-// otherwise run in more waves.
-__host__ __device__ constexpr bool a_in_tmem(int nt) { return nt <= 32 || nt == 64 || nt == 128; }
+// The converters store A straight into tensor memory (stages of 32 columns
+// after the accumulators), so a K tile's A makes no round trip through
+// shared memory and the MMAs read only the token block there (measured
+// against A in shared memory: 2% faster at T = 256 and 3% at T = 64, once
+// the converters no longer paced the loop).  A CTA takes all 512 columns
+// (256 of accumulators, up to 8 A stages) and holds an SM alone; with tiles
+// of 16 and more tiles than SMs, a CTA takes 256 (128 of accumulators, 4 A
+// stages) so that two share an SM (`two`): two CTAs per SM give each a
+// slower K loop, so this pays only where the tiles would otherwise run in
+// more waves.
 __host__ __device__ constexpr uint32_t a_tmem_col0(bool two) { return two ? 128u : 256u; }
+// Stage and accumulator-buffer counts are even: K tiles i and i + S (or
+// i + NB) then always belong to the same MMA issuer and converter group, so
+// every barrier phase has one in-order waiter.
 __host__ __device__ constexpr int tc_accbufs(int nt, bool two)
 {
-    return a_in_tmem(nt) ? (static_cast<int>(a_tmem_col0(two)) / acc_cols(nt) < 8
-                                ? static_cast<int>(a_tmem_col0(two)) / acc_cols(nt) : 8)
-                         : accbufs_for(nt);
+    return static_cast<int>(a_tmem_col0(two)) / acc_cols(nt) < 8 ? static_cast<int>(a_tmem_col0(two)) / acc_cols(nt)
+                                                                   : 8;
 }
-__host__ __device__ constexpr uint32_t tc_stage_bytes(int nt) { return a_in_tmem(nt) ? round1024(b_bytes(nt)) : stage_bytes(nt); }
-constexpr size_t kTcAtmSmemBudget = 224 * 1024;
+// A stage in shared memory holds one token block.
+__host__ __device__ constexpr uint32_t tc_stage_bytes(int nt) { return round1024(b_bytes(nt)); }
+constexpr size_t kTcSmemBudget = 224 * 1024;
 __host__ __device__ constexpr int tc_stages(int nt, bool two)
 {
-    return a_in_tmem(nt)
-               ? (two ? 4
-                      : ((kTcAtmSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / tc_stage_bytes(nt) < 8
-                             ? static_cast<int>((kTcAtmSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / tc_stage_bytes(nt))
-                             : 8) & ~1)
-               : stages_for(nt);
+    return two ? 4
+               : ((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / tc_stage_bytes(nt) < 8
+                      ? static_cast<int>((kTcSmemBudget - CODE_SLOTS * CHUNK_BYTES - 2048) / tc_stage_bytes(nt))
+                      : 8) & ~1;
 }
 
 // Byte offset of (row, 8-column block k8) in a [rows x 64] bf16 tile laid out
@@ -177,17 +160,9 @@ __host__ __device__ constexpr uint32_t instr_desc(int m, int n)
            (static_cast<uint32_t>(m >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.u32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem),
-        "l"(a), "l"(b), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-// The same MMA with A read from tensor memory (M = 128 rows in the 128
-// lanes, K along the columns, two bf16 per 32-bit column).
+// tcgen05 MMA, kind::f16, A read from tensor memory (M = 128 rows in the
+// 128 lanes, K along the columns, two bf16 per 32-bit column), B from a
+// shared-memory descriptor, D in tensor memory.
 __device__ __forceinline__ void mma_bf16_ta(uint32_t tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc)
 {
     asm volatile(
@@ -297,12 +272,6 @@ __device__ __forceinline__ void q2_word_to_bf16(uint32_t w, uint4 &lo, uint4 &hi
     hi.y = bf16x2_sub(((w >> 5) & 0x00600060u) | mag, off);  // 5 and 13
     hi.z = bf16x2_sub(((w >> 7) & 0x00600060u) | mag, off);  // 6 and 14
     hi.w = bf16x2_sub(((w >> 9) & 0x00600060u) | mag, off);  // 7 and 15
-}
-
-__device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
-{
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
 }
 
 __device__ __forceinline__ uint4 lds128v(uint32_t addr)
@@ -527,18 +496,16 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
 {
     constexpr int CHUNK_KT = chunk_kt<BITS>();
     constexpr int TILE_BYTES = KT * BITS / 8;  // bytes of one row's codes per K tile
-    constexpr bool ATM = a_in_tmem(NT);
     static_assert(!TWO || NT == 16, "two CTAs per SM only with 16-token tiles");
     static_assert(tc_stages(NT, TWO) % 2 == 0 && tc_accbufs(NT, TWO) % 2 == 0,
                   "even stage and buffer counts: one waiter per barrier phase with two MMA issuers");
     constexpr int NB = tc_accbufs(NT, TWO);
-    constexpr uint32_t ACOL0 = a_tmem_col0(TWO);  // first A stage column (ATM)
+    constexpr uint32_t ACOL0 = a_tmem_col0(TWO);  // first A stage column
     constexpr bool HL = hilo_shared(NT);
     constexpr int AC = acc_cols(NT);  // TMEM columns of one accumulator
-    constexpr uint32_t NCOLS = ATM ? 2u * ACOL0 : NB * AC;  // a power of two in [64, 512]
+    constexpr uint32_t NCOLS = 2u * ACOL0;  // accumulators, then the A stages
     constexpr int S = tc_stages(NT, TWO);
     constexpr uint32_t SB = tc_stage_bytes(NT);
-    constexpr uint32_t B_OFF = ATM ? 0u : A_BYTES;  // B within a stage
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -646,7 +613,7 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                     break;
                 }
                 mbar_arrive_expect_tx(full0 + 8 * s, b_bytes(NT));
-                bulk_g2s(stage0 + s * SB + B_OFF, src + static_cast<size_t>(i) * b_bytes(NT), b_bytes(NT),
+                bulk_g2s(stage0 + s * SB, src + static_cast<size_t>(i) * b_bytes(NT), b_bytes(NT),
                          full0 + 8 * s);
             }
         }
@@ -667,20 +634,13 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sa = stage0 + s * SB;
-                const uint32_t sb = sa + B_OFF;
+                const uint32_t sb = stage0 + s * SB;  // the token block
                 const uint32_t d = tmem + static_cast<uint32_t>(b * AC);
 #pragma unroll
                 for (int kk = 0; kk < KT / 16; ++kk) {
-                    if (ATM) {
-                        const uint32_t at = tmem + ACOL0 + static_cast<uint32_t>(s * 32 + kk * 8);
-                        mma_bf16_ta(d, at, smem_desc(sb + kk * 256), idesc, kk != 0);
-                        if (HL) mma_bf16_ta(d, at, smem_desc(sb + LO + kk * 256), idesc, 1u);
-                    } else {
-                        const uint64_t ad = smem_desc(sa + kk * 256);
-                        mma_bf16(d, ad, smem_desc(sb + kk * 256), idesc, kk != 0);
-                        if (HL) mma_bf16(d, ad, smem_desc(sb + LO + kk * 256), idesc, 1u);
-                    }
+                    const uint32_t at = tmem + ACOL0 + static_cast<uint32_t>(s * 32 + kk * 8);
+                    mma_bf16_ta(d, at, smem_desc(sb + kk * 256), idesc, kk != 0);
+                    if (HL) mma_bf16_ta(d, at, smem_desc(sb + LO + kk * 256), idesc, 1u);
                 }
                 mma_commit(empty0 + 8 * s);
                 mma_commit(accf0 + 8 * b);
@@ -712,61 +672,37 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                 break;
             }
             const uint32_t row = codes0 + slot * CHUNK_BYTES + static_cast<uint32_t>(r) * 128u;
-            const uint32_t sa = stage0 + s * SB;
-            if (ATM) tc_fence_after();  // after the wait for the MMA that last read this stage
+            tc_fence_after();  // after the wait for the MMA that last read this stage
 #pragma unroll
             for (int hf = 0; hf < 2; ++hf) {
-                if (ATM) {
-                    // 16 columns (32 bf16) of tile row r, in the K order of
-                    // the B operand, straight into tensor memory
-                    uint32_t v[16];
-                    if (BITS == 4) {
-                        const uint4 w = lds128v(row + (((2u * sub + static_cast<uint32_t>(hf)) ^ rsw) << 4));
-                        const uint32_t words[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const uint4 cv = q4_word_to_bf16(words[q]);
-                            v[4 * q] = cv.x; v[4 * q + 1] = cv.y; v[4 * q + 2] = cv.z; v[4 * q + 3] = cv.w;
-                        }
-                    } else {
-                        const uint2 w = lds64v(row + ((static_cast<uint32_t>(sub) ^ rsw) << 4) + 8u * hf);
-                        const uint32_t words[2] = {w.x, w.y};
-#pragma unroll
-                        for (int q = 0; q < 2; ++q) {
-                            uint4 lo, hi;
-                            q2_word_to_bf16(words[q], lo, hi);
-                            v[8 * q] = lo.x; v[8 * q + 1] = lo.y; v[8 * q + 2] = lo.z; v[8 * q + 3] = lo.w;
-                            v[8 * q + 4] = hi.x; v[8 * q + 5] = hi.y; v[8 * q + 6] = hi.z; v[8 * q + 7] = hi.w;
-                        }
-                    }
-                    tmem_st16(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + ACOL0 +
-                                  static_cast<uint32_t>(s * 32 + 16 * hf),
-                              v);
-                } else if (BITS == 4) {
-                    // 16-byte unit 2 sub + hf of the (swizzled) chunk row: 4 words, one block each
+                // 16 columns (32 bf16) of tile row r, in the K order of
+                // the B operand, straight into tensor memory
+                uint32_t v[16];
+                if (BITS == 4) {
                     const uint4 w = lds128v(row + (((2u * sub + static_cast<uint32_t>(hf)) ^ rsw) << 4));
                     const uint32_t words[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) sts128(sa + core_off(r, 4 * hf + j), q4_word_to_bf16(words[j]));
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 cv = q4_word_to_bf16(words[q]);
+                        v[4 * q] = cv.x; v[4 * q + 1] = cv.y; v[4 * q + 2] = cv.z; v[4 * q + 3] = cv.w;
+                    }
                 } else {
-                    // half hf of 16-byte unit sub: 2 words, two blocks each
                     const uint2 w = lds64v(row + ((static_cast<uint32_t>(sub) ^ rsw) << 4) + 8u * hf);
                     const uint32_t words[2] = {w.x, w.y};
 #pragma unroll
-                    for (int j = 0; j < 2; ++j) {
+                    for (int q = 0; q < 2; ++q) {
                         uint4 lo, hi;
-                        q2_word_to_bf16(words[j], lo, hi);
-                        sts128(sa + core_off(r, 4 * hf + 2 * j), lo);
-                        sts128(sa + core_off(r, 4 * hf + 2 * j + 1), hi);
+                        q2_word_to_bf16(words[q], lo, hi);
+                        v[8 * q] = lo.x; v[8 * q + 1] = lo.y; v[8 * q + 2] = lo.z; v[8 * q + 3] = lo.w;
+                        v[8 * q + 4] = hi.x; v[8 * q + 5] = hi.y; v[8 * q + 6] = hi.z; v[8 * q + 7] = hi.w;
                     }
                 }
+                tmem_st16(tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + ACOL0 +
+                              static_cast<uint32_t>(s * 32 + 16 * hf),
+                          v);
             }
-            if (ATM) {
-                tmem_wait_st();
-                tc_fence_before();
-            } else {
-                fence_proxy_async_smem();
-            }
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(full0 + 8 * s);
