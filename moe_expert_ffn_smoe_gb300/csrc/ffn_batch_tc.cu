@@ -42,12 +42,13 @@
 //     one down K tile).
 //  3. tc_ffn<BITS, NT, down>: 128 down rows over one K range, split the same
 //     way; each split writes Y for its token columns.
-// Inside a GEMM CTA (608 threads): warps 0-7 epilogue (warp w reads TMEM
+// Inside a GEMM CTA (640 threads): warps 0-7 epilogue (warp w reads TMEM
 // lane quarter w % 4 = 32 tile rows, columns of half w / 4), warps 8-15
 // convert codes to A tiles in two groups of four that take alternate K
-// tiles (thread = one tile row), warp 16 issues the MMAs, warp 17 streams code
-// chunks with 2-D tensor copies (TMA, 128-byte swizzle: 128 bytes x 64 or
-// 128 rows per chunk), warp 18 streams the token B blocks with bulk copies.
+// tiles (thread = one tile row), warps 16 and 19 issue the MMAs of even and
+// odd K tiles, warp 17 streams code chunks with 2-D tensor copies (TMA,
+// 128-byte swizzle: 128 bytes x 64 or 128 rows per chunk), warp 18 streams
+// the token B blocks with bulk copies.
 // Two converter and two epilogue warps per SM sub-partition keep those
 // dependent chains overlapped.  Every hand-off is an mbarrier with one
 // in-order waiter per role, so each awaited phase parity is unambiguous;
