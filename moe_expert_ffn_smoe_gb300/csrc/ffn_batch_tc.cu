@@ -289,6 +289,22 @@ __device__ __forceinline__ uint2 lds64v(uint32_t addr)
     return v;
 }
 
+// L2 prefetch of one box of a 2-D tensor map at (x bytes, y rows); parts
+// outside the tensor are skipped.  x must be a multiple of 16.
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
+// L2 prefetch of `bytes` (a multiple of 16) from a 16-byte aligned global address.
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2-D tensor copy global -> shared of one box at (x bytes, y rows),
 // completing on the mbarrier.  x must be a multiple of 16.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t bar)
@@ -465,6 +481,11 @@ struct alignas(128) TcArgs {  // CUtensorMap members are 128-byte aligned
     int n;                  // experts
     int M;                  // rows per matrix (d_ff for gate/up, d_model for down)
     int K, group, ntiles, kps, nsplit;
+    // gate/up: the down projection's codes (boxes of 128 rows x 128 bytes)
+    // and scales, which the CTAs prefetch into L2 for the next launch
+    CUtensorMap pmap[TC_MAX_EXPERTS];
+    const float *pscales[TC_MAX_EXPERTS];  // null: not prefetched
+    int pM, pK;                            // down rows (d_model) and columns (d_ff); pK = 0: no prefetch
 };
 
 // Gate/up finish: the hidden values of tokens [n0, n1) of this tile (global
@@ -600,6 +621,23 @@ __global__ void __launch_bounds__(TC_THREADS, TWO ? 2 : 1) tc_ffn(const __grid_c
                     break;
                 }
                 issue_chunk(c);
+            }
+            if (GU && !failed && ltile == 0 && a.pK > 0) {
+                // The down projection reads this expert's down weights right
+                // after this launch; this one leaves DRAM mostly idle at
+                // small T, so its CTAs (all issued chunks out) fetch them
+                // into L2 now: each CTA a share of the 128-row x 128-byte
+                // boxes and of the scales.
+                const int rank = mtile + static_cast<int>(gridDim.x) * split;
+                const int nr = static_cast<int>(gridDim.x * gridDim.z);
+                const int rb = (a.pM + MT - 1) / MT, cb = (a.pK * BITS / 8 + 127) / 128;
+                for (int bx = rank; bx < rb * cb; bx += nr) tma_prefetch_2d(&a.pmap[xe], (bx % cb) * 128, (bx / cb) * MT);
+                if (a.pscales[xe]) {
+                    const size_t sb = static_cast<size_t>(a.pM) * (a.pK / a.group) * sizeof(float);  // multiple of 16
+                    const uint8_t *sp = reinterpret_cast<const uint8_t *>(a.pscales[xe]);
+                    for (size_t off = static_cast<size_t>(rank) * 4096u; off < sb; off += static_cast<size_t>(nr) * 4096u)
+                        bulk_prefetch_l2(sp + off, static_cast<uint32_t>(sb - off < 4096u ? sb - off : 4096u));
+                }
             }
         }
     } else if (warp == BPROD_WARP) {
@@ -1215,6 +1253,9 @@ cudaError_t launch_ffn_batch_tc_experts(int bits, int n, const uint8_t *const *g
                  encode_codes(&a->tmap[i][1], uc[e], bits, d_ff, d_model, 64) &&
                  encode_codes(&b->tmap[i][0], dc[e], bits, d_model, d_ff, MT);
             b->tmap[i][1] = b->tmap[i][0];
+            a->pmap[i] = b->tmap[i][0];
+            // scales are prefetched only from a 16-byte aligned start
+            a->pscales[i] = (reinterpret_cast<uintptr_t>(ds[e]) & 15u) == 0 ? ds[e] : nullptr;
             a->scales[i][0] = gs[e];
             a->scales[i][1] = us[e];
             b->scales[i][0] = b->scales[i][1] = ds[e];
@@ -1229,6 +1270,8 @@ cudaError_t launch_ffn_batch_tc_experts(int bits, int n, const uint8_t *const *g
         a->status = b->status = status;
         a->M = d_ff;
         a->K = d_model;
+        a->pM = d_model;
+        a->pK = d_ff;
         b->B = ws + L.hb;
         b->Hb = nullptr;
         b->M = d_model;
