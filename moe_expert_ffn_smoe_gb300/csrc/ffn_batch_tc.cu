@@ -39,7 +39,8 @@
 //     NT/S) of every split's partials (in split order, read through
 //     distributed shared memory), forms SiLU(g) * u and writes it directly
 //     as the B block of the down projection's K tile (64 hidden columns =
-//     one down K tile).
+//     one down K tile).  Its code-streaming warp also prefetches the down
+//     weights into L2 once its own chunks are out.
 //  3. tc_ffn<BITS, NT, down>: 128 down rows over one K range, split the same
 //     way; each split writes Y for its token columns.
 // Inside a GEMM CTA (640 threads): warps 0-7 epilogue (warp w reads TMEM
