@@ -488,6 +488,7 @@ struct alignas(128) TcArgs {  // CUtensorMap members are 128-byte aligned
     const float *pscales[TC_MAX_EXPERTS];  // null: not prefetched
     int pM, pK;                            // down rows (d_model) and columns (d_ff); pK = 0: no prefetch
 };
+static_assert(sizeof(TcArgs) <= 32764, "kernel parameters are limited to 32,764 bytes");
 
 // Gate/up finish: the hidden values of tokens [n0, n1) of this tile (global
 // token tile gtile, the expert's tile ltile of an expert with Te tokens),
